@@ -1,0 +1,183 @@
+/*
+ * gdn.h -- C ABI of one NVFP4 W4A4 Gated DeltaNet (GDN) layer step on one GPU.
+ *
+ * The operation (Rocket blog, "A reduction barrier makes Qwen GDN graph replay
+ * bit exact", setup table): one GDN linear-attention layer as it is served from
+ * an NVFP4 checkpoint -- W4A4 QKVZ/BA projections, a BF16 causal convolution,
+ * an FP32 recurrent state updated by the gated delta rule (state laid out
+ * [v][k], the "pretranspose" decode layout), a z-gated RMSNorm and a W4A4
+ * output projection. NVFP4 (bloomery issue #565, Round 1, #489/#687): packed
+ * E2M1 pairs, one E4M3 scale per 16 values, one FP32 scale per tensor; W4A4
+ * quantises the activations to NVFP4 as well.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument that names a tensor is a DEVICE pointer, 16-byte
+ *   aligned, to row-major storage. The caller owns it; no call frees it.
+ * - BF16 tensors are passed as uint16_t bit patterns, E2M1 codes as bytes
+ *   holding two codes (element 2i in the low nibble of byte i), E4M3 scales as
+ *   one byte per 16 elements of a row.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call
+ *   except gdn_create and gdn_check is asynchronous on it, allocates nothing,
+ *   never synchronises and never reads device memory on the host, so it may be
+ *   captured into a CUDA graph.
+ * - Host-detectable errors (NULL pointers, sizes, alignment, non-finite scales)
+ *   return a status before anything is launched. Errors only the device can see
+ *   (non-finite activations, slot ids out of range or repeated) are written to a
+ *   sticky device status word and read back by gdn_check. Device code never
+ *   traps.
+ * - Numerics: every reduction has a fixed order and no atomics are used, so
+ *   repeated calls on the same inputs give bit-identical results.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_E_NULL = 1,       /* a required pointer is NULL */
+  GDN_E_SHAPE = 2,      /* a size is outside what the call or the context supports */
+  GDN_E_ALIGN = 3,      /* a tensor pointer is not 16-byte aligned */
+  GDN_E_NONFINITE = 4,  /* a scale, epsilon or activation is NaN or infinite */
+  GDN_E_BAD_SCALE = 5,  /* a scale is <= 0, or an E4M3 weight scale byte is NaN */
+  GDN_E_RANGE = 6,      /* a slot id is out of range or repeated within one call */
+  GDN_E_OVERFLOW = 7,   /* a size product overflows the index types */
+  GDN_E_CUDA = 8,       /* a CUDA runtime call failed */
+  GDN_E_OOM = 9,        /* gdn_create could not allocate its device memory */
+  GDN_E_TIMEOUT = 10,   /* a bounded device wait gave up */
+  GDN_E_STATE = 11      /* the context is unusable (creation failed part way) */
+} gdn_status;
+
+/* Short, static, human-readable name of a status ("GDN_E_SHAPE", ...). */
+const char *gdn_status_string(int status);
+
+/* Layer shape and the static quantiser settings of one layer. */
+typedef struct {
+  int hidden;             /* H: model width, multiple of 64 */
+  int n_k_heads;          /* Hk: key/query heads */
+  int n_v_heads;          /* Hv: value heads, a multiple of Hk; value head h reads key head h / (Hv/Hk) */
+  int d_k, d_v;           /* head sizes; d_k == d_v in {32, 64, 128} */
+  int conv_kernel;        /* depthwise causal conv taps; 4 */
+  int max_batch;          /* largest B gdn_decode_step accepts (1..256) */
+  int max_prefill_tokens; /* largest T gdn_prefill accepts (0 = no prefill) */
+  float rms_eps;          /* gated RMSNorm epsilon (inside the square root) */
+  float l2_eps;           /* q/k L2-norm epsilon (inside the square root) */
+  float act_scale_in;     /* FP32 tensor scale of the x quantiser, > 0 */
+  float act_scale_out;    /* FP32 tensor scale of the gated-norm output quantiser, > 0 */
+} gdn_config;
+
+/* One NVFP4 matrix W[rows][cols]: codes [rows][cols/2], scales [rows][cols/16]
+ * (device pointers), value = e2m1(code) * e4m3(scale) * tensor_scale. */
+typedef struct {
+  const uint8_t *codes;
+  const uint8_t *scales;
+  float tensor_scale;
+} gdn_nvfp4;
+
+/* Layer weights (device pointers). Read once by gdn_create; the caller may
+ * free them after it returns.
+ *   qkvz: [2*Hk*d_k + 2*Hv*d_v][H], rows ordered q | k | v | z, heads contiguous
+ *   ba:   [2*Hv][H], rows ordered b | a
+ *   out:  [H][Hv*d_v]
+ *   conv_w: BF16 [C][conv_kernel], C = 2*Hk*d_k + Hv*d_v channels ordered q | k | v,
+ *           taps oldest to newest
+ *   A_log, dt_bias: FP32 [Hv];  norm_w: FP32 [d_v] */
+typedef struct {
+  gdn_nvfp4 qkvz, ba, out;
+  const uint16_t *conv_w;
+  const float *A_log, *dt_bias, *norm_w;
+} gdn_weights;
+
+typedef struct gdn_ctx gdn_ctx;
+
+/* Validate the config and weights, copy the weights into the kernels' layouts
+ * and allocate the context's workspace on the current device. Synchronises
+ * `stream` once (the only call that does besides gdn_check). On failure *out is
+ * NULL and nothing stays allocated. Errors: GDN_E_NULL, GDN_E_SHAPE,
+ * GDN_E_NONFINITE (eps/scales), GDN_E_BAD_SCALE (scale <= 0 or an E4M3 weight
+ * scale byte 0x7F/0xFF), GDN_E_OVERFLOW, GDN_E_OOM, GDN_E_CUDA. */
+gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream, gdn_ctx **out);
+
+/* Free everything the context owns. NULL is accepted. Synchronises the device
+ * work of the context's own allocations (cudaFree). */
+gdn_status gdn_destroy(gdn_ctx *ctx);
+
+/* NVFP4 quantisation of x[rows][cols] (bloomery issue #565, Round 1, #687:
+ * "4-bit activations"). x is BF16 bits (x_is_f32 = 0) or FP32 (x_is_f32 = 1);
+ * cols % 16 == 0. For every 16-block, in FP32 with round-to-nearest-even:
+ *   inv6ts = 1 / (6 * tensor_scale); amax = max |x|; s = E4M3_satfinite(amax * inv6ts);
+ *   if e4m3(s) == 0 the 16 codes are 0, else r = 1 / (e4m3(s) * tensor_scale) and
+ *   code = E2M1_satfinite(x * r), sign kept (-0 is code 8).
+ * Writes codes [rows][cols/2] and scales [rows][cols/16]. A block holding NaN or
+ * infinity gets scale 0 and codes 0 and sets GDN_E_NONFINITE in *dev_status
+ * (a device int32, may be NULL). Errors: GDN_E_NULL, GDN_E_SHAPE (rows < 0,
+ * cols % 16), GDN_E_ALIGN, GDN_E_NONFINITE / GDN_E_BAD_SCALE (tensor_scale). */
+gdn_status nvfp4_quantize(const void *x, int x_is_f32, int rows, int cols, float tensor_scale,
+                          uint8_t *codes, uint8_t *scales, int32_t *dev_status, void *stream);
+
+/* Block-scaled W4A4 product C[M][N] = sum_k A_hat[m][k] * B_hat[n][k], FP32
+ * accumulation, written as BF16 (c_is_bf16 = 1, round to nearest even) or FP32.
+ * A is [M][K], B is [N][K], both NVFP4 (struct fields are device pointers,
+ * the struct itself is host memory). K % 64 == 0, M, N >= 0 (0 is a no-op).
+ * Errors: GDN_E_NULL, GDN_E_SHAPE, GDN_E_ALIGN, GDN_E_BAD_SCALE (tensor
+ * scale <= 0 or non-finite), GDN_E_OVERFLOW. */
+gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int K,
+                      void *C, int c_is_bf16, void *stream);
+
+/* One decode step of B sequences (c1..c16 buckets and larger batches).
+ *   x:          BF16 [B][H]
+ *   slot_ids:   int32 [B] (device), the state slot of each row; -1 marks a padding
+ *               row, whose output row is written as zeros and which touches no state.
+ *               Ids must be distinct; an id >= num_slots or < -1, or a repeated id,
+ *               sets GDN_E_RANGE in the status word and that row is treated as padding.
+ *   out:        BF16 [B][H]
+ *   conv_state: BF16 [num_slots][conv_kernel-1][C], the last conv_kernel-1 raw
+ *               inputs of every channel, oldest first; updated in place
+ *   ssm_state:  FP32 [num_slots][Hv][d_v][d_k]; updated in place
+ * Per active row: x -> NVFP4(act_scale_in) -> W4A4 qkvz/ba -> BF16; conv + SiLU;
+ * q,k L2-normalised (q also scaled by d_k^-1/2); beta = sigmoid(b),
+ * g = -exp(A_log) * softplus(a + dt_bias); per value head S <- exp(g) S,
+ * u = beta (v - S k), S <- S + u k^T, o = S q; y = o * rsqrt(mean(o^2) + rms_eps)
+ * * norm_w * SiLU(z); y -> NVFP4(act_scale_out) -> W4A4 out_proj -> BF16.
+ * Errors: GDN_E_NULL, GDN_E_SHAPE (B < 1 or > max_batch, num_slots < 1),
+ * GDN_E_ALIGN, GDN_E_OVERFLOW, GDN_E_CUDA. */
+gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B,
+                           uint16_t *out, uint16_t *conv_state, float *ssm_state, int num_slots,
+                           void *stream);
+
+/* The token-mixing stage of gdn_decode_step alone, for stage-wise checks and
+ * for callers that run the projections themselves: takes the BF16 projection
+ * outputs qkvz [B][2*Hk*d_k + 2*Hv*d_v] and ba [B][2*Hv] and writes the FP32
+ * gated-norm output y [B][Hv*d_v] (zeros for padding rows); conv_state and
+ * ssm_state as in gdn_decode_step, updated in place. Same errors. */
+gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba,
+                        const int32_t *slot_ids, int B, float *y, uint16_t *conv_state,
+                        float *ssm_state, int num_slots, void *stream);
+
+/* Prefill of T tokens of one sequence held in slot `slot` (host int): the same
+ * arithmetic as T successive decode steps of that sequence (bloomery issue #565,
+ * Round 1, #812: the delta rule of a prompt runs on tensor cores in chunks).
+ * x BF16 [T][H] -> out BF16 [T][H]; init_zero != 0 starts from zero conv and
+ * recurrent state (the slot's state is overwritten), else from the slot's
+ * state. The slot's state is left as after the last token. Errors: GDN_E_NULL,
+ * GDN_E_SHAPE (T < 1 or > max_prefill_tokens), GDN_E_RANGE (slot), GDN_E_ALIGN. */
+gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int init_zero,
+                       uint16_t *out, uint16_t *conv_state, float *ssm_state, int num_slots,
+                       void *stream);
+
+/* Synchronise `stream`, read the context's sticky device status word, clear it
+ * if `clear`, and return it (GDN_OK when nothing was flagged). A CUDA error seen
+ * while synchronising returns GDN_E_CUDA. */
+gdn_status gdn_check(gdn_ctx *ctx, int clear, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

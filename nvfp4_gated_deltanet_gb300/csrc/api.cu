@@ -1,0 +1,455 @@
+// The C ABI of include/gdn.h: validation, the context, and the launch order of
+// each call. Every step of the layer runs in the kernels of this directory.
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+using namespace gdn;
+
+struct gdn_ctx {
+  gdn_config cfg;
+  int Nqkvz, Nba, Nin, C, Vd, prow;
+  int device, num_sms;
+  uint8_t *w_in_codes, *w_in_scales;    // [Nin][H/2], [Nin][H/16]: qkvz rows then ba rows
+  float ts_qkvz, ts_ba;
+  uint8_t *w_out_codes, *w_out_scales;  // [H][Vd/2], [H][Vd/16]
+  float ts_wout;
+  uint16_t *conv_w;                     // [C][K]
+  float *A_log, *dt_bias, *norm_w;
+  uint16_t *proj;                       // [prow][Nin] BF16 projection outputs
+  uint8_t *y_codes, *y_scales;          // [prow][Vd/2], [prow][Vd/16]
+  float *qn, *kn, *v, *beta, *alpha, *o;  // prefill intermediates
+  uint16_t *conv_tmp;                   // [K-1][C]
+  int32_t *status;
+  std::vector<void *> allocs;
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdn_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return GDN_OK;
+  if (e == cudaErrorMemoryAllocation) return GDN_E_OOM;
+  return GDN_E_CUDA;
+}
+
+template <typename T>
+cudaError_t ctx_alloc(gdn_ctx *c, T **p, size_t count) {
+  void *q = nullptr;
+  cudaError_t e = cudaMalloc(&q, count ? count * sizeof(T) : 16);
+  if (e != cudaSuccess) return e;
+  c->allocs.push_back(q);
+  *p = static_cast<T *>(q);
+  return cudaSuccess;
+}
+
+void ctx_free(gdn_ctx *c) {
+  for (void *p : c->allocs) cudaFree(p);
+  c->allocs.clear();
+}
+
+// Sets *bad to 1 when a scale byte is an E4M3 NaN (0x7F or 0xFF).
+__global__ void scan_nan_scales(const uint8_t *s, size_t n, int32_t *bad) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    if ((s[i] & 0x7F) == 0x7F) flag_status(bad, GDN_E_BAD_SCALE);
+}
+
+gdn_status check_nvfp4(const gdn_nvfp4 &m) {
+  if (!m.codes || !m.scales) return GDN_E_NULL;
+  if (!aligned16(m.codes) || !aligned16(m.scales)) return GDN_E_ALIGN;
+  if (!std::isfinite(m.tensor_scale)) return GDN_E_NONFINITE;
+  if (!(m.tensor_scale > 0.0f)) return GDN_E_BAD_SCALE;
+  return GDN_OK;
+}
+
+// W4A4 product of M activation rows (BF16 quantised on the fly, or NVFP4)
+// against the N weight rows, 16 activation rows per pass.
+cudaError_t run_gemv(GemvArgs g, const LaunchCtx &lc, int M) {
+  const int K = g.K;
+  for (int r0 = 0; r0 < M; r0 += 16) {
+    GemvArgs p = g;
+    p.M = M - r0 < 16 ? M - r0 : 16;
+    if (g.a_bf16) p.a_bf16 = g.a_bf16 + (size_t)r0 * K;
+    if (g.a_codes) {
+      p.a_codes = g.a_codes + (size_t)r0 * (K / 2);
+      p.a_scales = g.a_scales + (size_t)r0 * (K / 16);
+    }
+    if (g.row_slot) p.row_slot = g.row_slot + r0;
+    p.c = static_cast<char *>(g.c) + (size_t)r0 * g.ldc * (g.c_is_bf16 ? 2 : 4);
+    cudaError_t e = launch_gemv(p, lc);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+gdn_status check_state_args(gdn_ctx *ctx, const void *x, const void *out, const uint16_t *conv_state,
+                            const float *ssm_state, int num_slots) {
+  if (!ctx || !x || !out || !conv_state || !ssm_state) return GDN_E_NULL;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(conv_state) || !aligned16(ssm_state)) return GDN_E_ALIGN;
+  if (num_slots < 1) return GDN_E_SHAPE;
+  const size_t per_slot = (size_t)ctx->cfg.n_v_heads * ctx->cfg.d_v * ctx->cfg.d_k;
+  if ((size_t)num_slots > ((size_t)1 << 40) / per_slot) return GDN_E_OVERFLOW;
+  return GDN_OK;
+}
+
+MixArgs mix_args(gdn_ctx *c) {
+  MixArgs m{};
+  m.conv_w = c->conv_w;
+  m.A_log = c->A_log;
+  m.dt_bias = c->dt_bias;
+  m.norm_w = c->norm_w;
+  m.Hk = c->cfg.n_k_heads;
+  m.Hv = c->cfg.n_v_heads;
+  m.D = c->cfg.d_k;
+  m.C = c->C;
+  m.Kc = c->cfg.conv_kernel;
+  m.l2_eps = c->cfg.l2_eps;
+  m.rms_eps = c->cfg.rms_eps;
+  m.ts_out = c->cfg.act_scale_out;
+  m.status = c->status;
+  return m;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(int s) {
+  static const char *names[] = {"GDN_OK",          "GDN_E_NULL",     "GDN_E_SHAPE",   "GDN_E_ALIGN",
+                                "GDN_E_NONFINITE", "GDN_E_BAD_SCALE", "GDN_E_RANGE",   "GDN_E_OVERFLOW",
+                                "GDN_E_CUDA",      "GDN_E_OOM",      "GDN_E_TIMEOUT", "GDN_E_STATE"};
+  if (s < 0 || s > 11) return "GDN_E_UNKNOWN";
+  return names[s];
+}
+
+gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream, gdn_ctx **out) {
+  if (!out) return GDN_E_NULL;
+  *out = nullptr;
+  if (!cfg || !w) return GDN_E_NULL;
+  const gdn_config c = *cfg;
+  if (c.hidden <= 0 || c.n_k_heads <= 0 || c.n_v_heads <= 0 || c.max_batch < 1 || c.max_batch > 256 ||
+      c.max_prefill_tokens < 0)
+    return GDN_E_SHAPE;
+  if (c.hidden % 64 || c.n_v_heads % c.n_k_heads || c.n_v_heads / c.n_k_heads > 8) return GDN_E_SHAPE;
+  if (c.d_k != c.d_v || (c.d_k != 32 && c.d_k != 64 && c.d_k != 128)) return GDN_E_SHAPE;
+  if (c.conv_kernel < 2 || c.conv_kernel > 4) return GDN_E_SHAPE;
+  if ((c.n_v_heads * c.d_v) % 64) return GDN_E_SHAPE;
+  if (!std::isfinite(c.rms_eps) || !std::isfinite(c.l2_eps) || !std::isfinite(c.act_scale_in) ||
+      !std::isfinite(c.act_scale_out))
+    return GDN_E_NONFINITE;
+  if (c.rms_eps < 0 || c.l2_eps < 0 || !(c.act_scale_in > 0) || !(c.act_scale_out > 0)) return GDN_E_BAD_SCALE;
+  gdn_status st;
+  if ((st = check_nvfp4(w->qkvz)) != GDN_OK || (st = check_nvfp4(w->ba)) != GDN_OK ||
+      (st = check_nvfp4(w->out)) != GDN_OK)
+    return st;
+  if (!w->conv_w || !w->A_log || !w->dt_bias || !w->norm_w) return GDN_E_NULL;
+  if (!aligned16(w->conv_w) || !aligned16(w->A_log) || !aligned16(w->dt_bias) || !aligned16(w->norm_w))
+    return GDN_E_ALIGN;
+  const long long H = c.hidden, Hk = c.n_k_heads, Hv = c.n_v_heads, D = c.d_k;
+  const long long Nqkvz = 2 * Hk * D + 2 * Hv * D, Nba = 2 * Hv, Nin = Nqkvz + Nba;
+  const long long Cc = 2 * Hk * D + Hv * D, Vd = Hv * D;
+  const long long prow = c.max_batch > c.max_prefill_tokens ? c.max_batch : c.max_prefill_tokens;
+  if (Nin * H > (1LL << 31) || H * Vd > (1LL << 31) || prow * Nin > (1LL << 34) || Vd > 16384 || H > 16384)
+    return GDN_E_OVERFLOW;
+
+  gdn_ctx *ctx = new (std::nothrow) gdn_ctx();
+  if (!ctx) return GDN_E_OOM;
+  ctx->cfg = c;
+  ctx->Nqkvz = (int)Nqkvz;
+  ctx->Nba = (int)Nba;
+  ctx->Nin = (int)Nin;
+  ctx->C = (int)Cc;
+  ctx->Vd = (int)Vd;
+  ctx->prow = (int)prow;
+  ctx->ts_qkvz = w->qkvz.tensor_scale;
+  ctx->ts_ba = w->ba.tensor_scale;
+  ctx->ts_wout = w->out.tensor_scale;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  const long long T = c.max_prefill_tokens;
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_in_codes, Nin * H / 2);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_in_scales, Nin * H / 16);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_out_codes, H * Vd / 2);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_out_scales, H * Vd / 16);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->conv_w, Cc * c.conv_kernel);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->A_log, Hv);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->dt_bias, Hv);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->norm_w, D);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->proj, prow * Nin);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_codes, prow * Vd / 2);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_scales, prow * Vd / 16);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->status, 1);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->conv_tmp, (c.conv_kernel - 1) * Cc);
+  if (T > 0) {
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->qn, T * Hk * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->kn, T * Hk * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->v, T * Hv * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->o, T * Hv * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->beta, T * Hv);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->alpha, T * Hv);
+  }
+  // weights into the kernels' layout: [qkvz; ba] as one matrix for one pass over x
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->w_in_codes, w->qkvz.codes, Nqkvz * H / 2, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ctx->w_in_codes + Nqkvz * H / 2, w->ba.codes, Nba * H / 2, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->w_in_scales, w->qkvz.scales, Nqkvz * H / 16, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ctx->w_in_scales + Nqkvz * H / 16, w->ba.scales, Nba * H / 16, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->w_out_codes, w->out.codes, H * Vd / 2, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->w_out_scales, w->out.scales, H * Vd / 16, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ctx->conv_w, w->conv_w, Cc * c.conv_kernel * 2, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->A_log, w->A_log, Hv * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->dt_bias, w->dt_bias, Hv * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->norm_w, w->norm_w, D * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->status, 0, 4, s);
+  if (e == cudaSuccess) {
+    scan_nan_scales<<<256, 256, 0, s>>>(ctx->w_in_scales, (size_t)(Nin * H / 16), ctx->status);
+    scan_nan_scales<<<256, 256, 0, s>>>(ctx->w_out_scales, (size_t)(H * Vd / 16), ctx->status);
+    e = cudaGetLastError();
+  }
+  int32_t flag = 0;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&flag, ctx->status, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess || flag != 0) {
+    gdn_status r = e != cudaSuccess ? cuda_status(e) : (gdn_status)flag;
+    ctx_free(ctx);
+    delete ctx;
+    return r;
+  }
+  *out = ctx;
+  return GDN_OK;
+}
+
+gdn_status gdn_destroy(gdn_ctx *ctx) {
+  if (!ctx) return GDN_OK;
+  ctx_free(ctx);
+  delete ctx;
+  return GDN_OK;
+}
+
+gdn_status nvfp4_quantize(const void *x, int x_is_f32, int rows, int cols, float tensor_scale, uint8_t *codes,
+                          uint8_t *scales, int32_t *dev_status, void *stream) {
+  if (rows < 0 || cols <= 0 || cols % 16) return GDN_E_SHAPE;
+  if (rows == 0) return GDN_OK;
+  if (!x || !codes || !scales) return GDN_E_NULL;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return GDN_E_ALIGN;
+  if (!std::isfinite(tensor_scale)) return GDN_E_NONFINITE;
+  if (!(tensor_scale > 0)) return GDN_E_BAD_SCALE;
+  if ((long long)rows * cols > (1LL << 40)) return GDN_E_OVERFLOW;
+  return cuda_status(launch_quantize(x, x_is_f32, rows, cols, tensor_scale, codes, scales, dev_status,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int K, void *C, int c_is_bf16,
+                      void *stream) {
+  if (!A || !B) return GDN_E_NULL;
+  if (M < 0 || N < 0 || K <= 0 || K % 64) return GDN_E_SHAPE;
+  if (M == 0 || N == 0) return GDN_OK;
+  gdn_status st;
+  if ((st = check_nvfp4(*A)) != GDN_OK || (st = check_nvfp4(*B)) != GDN_OK) return st;
+  if (!C) return GDN_E_NULL;
+  if (!aligned16(C)) return GDN_E_ALIGN;
+  if ((long long)N * K > (1LL << 31) || (long long)M * K > (1LL << 40) || K > 32768) return GDN_E_OVERFLOW;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if ((size_t)16 * (K >> 6) * (4 * 2 * 16 + 16) > 200 * 1024) return GDN_E_SHAPE;
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), sms};
+  GemvArgs g{};
+  g.a_codes = A->codes;
+  g.a_scales = A->scales;
+  g.ts_a = A->tensor_scale;
+  g.w_codes = B->codes;
+  g.w_scales = B->scales;
+  g.ts_w0 = g.ts_w1 = B->tensor_scale;
+  g.n_split = N;
+  g.c = C;
+  g.c_is_bf16 = c_is_bf16 ? 1 : 0;
+  g.ldc = N;
+  g.N = N;
+  g.K = K;
+  return cuda_status(run_gemv(g, lc, M));
+}
+
+gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *out,
+                           uint16_t *conv_state, float *ssm_state, int num_slots, void *stream) {
+  gdn_status st = check_state_args(ctx, x, out, conv_state, ssm_state, num_slots);
+  if (st != GDN_OK) return st;
+  if (!slot_ids) return GDN_E_NULL;
+  if (!aligned16(slot_ids)) return GDN_E_ALIGN;
+  if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms};
+  const int H = ctx->cfg.hidden;
+  GemvArgs g{};
+  g.a_bf16 = x;
+  g.ts_a = ctx->cfg.act_scale_in;
+  g.row_slot = slot_ids;
+  g.num_slots = num_slots;
+  g.w_codes = ctx->w_in_codes;
+  g.w_scales = ctx->w_in_scales;
+  g.ts_w0 = ctx->ts_qkvz;
+  g.ts_w1 = ctx->ts_ba;
+  g.n_split = ctx->Nqkvz;
+  g.c = ctx->proj;
+  g.c_is_bf16 = 1;
+  g.ldc = ctx->Nin;
+  g.N = ctx->Nin;
+  g.K = H;
+  g.status = ctx->status;
+  cudaError_t e = run_gemv(g, lc, B);
+  if (e != cudaSuccess) return cuda_status(e);
+  MixArgs m = mix_args(ctx);
+  m.qkvz = ctx->proj;
+  m.ld_qkvz = ctx->Nin;
+  m.ba = ctx->proj + ctx->Nqkvz;
+  m.ld_ba = ctx->Nin;
+  m.slot_ids = slot_ids;
+  m.B = B;
+  m.num_slots = num_slots;
+  m.conv_state = conv_state;
+  m.ssm_state = ssm_state;
+  m.y_codes = ctx->y_codes;
+  m.y_scales = ctx->y_scales;
+  m.y_f32 = nullptr;
+  e = launch_mix(m, lc);
+  if (e != cudaSuccess) return cuda_status(e);
+  GemvArgs o{};
+  o.a_codes = ctx->y_codes;
+  o.a_scales = ctx->y_scales;
+  o.ts_a = ctx->cfg.act_scale_out;
+  o.w_codes = ctx->w_out_codes;
+  o.w_scales = ctx->w_out_scales;
+  o.ts_w0 = o.ts_w1 = ctx->ts_wout;
+  o.n_split = H;
+  o.c = out;
+  o.c_is_bf16 = 1;
+  o.ldc = H;
+  o.N = H;
+  o.K = ctx->Vd;
+  o.status = ctx->status;
+  return cuda_status(run_gemv(o, lc, B));
+}
+
+gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, const int32_t *slot_ids, int B,
+                        float *y, uint16_t *conv_state, float *ssm_state, int num_slots, void *stream) {
+  gdn_status st = check_state_args(ctx, qkvz, y, conv_state, ssm_state, num_slots);
+  if (st != GDN_OK) return st;
+  if (!ba || !slot_ids) return GDN_E_NULL;
+  if (!aligned16(ba) || !aligned16(slot_ids)) return GDN_E_ALIGN;
+  if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms};
+  MixArgs m = mix_args(ctx);
+  m.qkvz = qkvz;
+  m.ld_qkvz = ctx->Nqkvz;
+  m.ba = ba;
+  m.ld_ba = ctx->Nba;
+  m.slot_ids = slot_ids;
+  m.B = B;
+  m.num_slots = num_slots;
+  m.conv_state = conv_state;
+  m.ssm_state = ssm_state;
+  m.y_codes = nullptr;
+  m.y_scales = nullptr;
+  m.y_f32 = y;
+  return cuda_status(launch_mix(m, lc));
+}
+
+gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int init_zero, uint16_t *out,
+                       uint16_t *conv_state, float *ssm_state, int num_slots, void *stream) {
+  gdn_status st = check_state_args(ctx, x, out, conv_state, ssm_state, num_slots);
+  if (st != GDN_OK) return st;
+  if (T < 1 || T > ctx->cfg.max_prefill_tokens) return GDN_E_SHAPE;
+  if (slot < 0 || slot >= num_slots) return GDN_E_RANGE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LaunchCtx lc{s, ctx->num_sms};
+  const gdn_config &c = ctx->cfg;
+  const int H = c.hidden, D = c.d_k;
+  uint16_t *cst = conv_state + (size_t)slot * (c.conv_kernel - 1) * ctx->C;
+  float *S = ssm_state + (size_t)slot * c.n_v_heads * D * D;
+  cudaError_t e = cudaSuccess;
+  if (init_zero) {
+    e = cudaMemsetAsync(cst, 0, (size_t)(c.conv_kernel - 1) * ctx->C * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, (size_t)c.n_v_heads * D * D * 4, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  GemvArgs g{};
+  g.a_bf16 = x;
+  g.ts_a = c.act_scale_in;
+  g.w_codes = ctx->w_in_codes;
+  g.w_scales = ctx->w_in_scales;
+  g.ts_w0 = ctx->ts_qkvz;
+  g.ts_w1 = ctx->ts_ba;
+  g.n_split = ctx->Nqkvz;
+  g.c = ctx->proj;
+  g.c_is_bf16 = 1;
+  g.ldc = ctx->Nin;
+  g.N = ctx->Nin;
+  g.K = H;
+  g.status = ctx->status;
+  e = run_gemv(g, lc, T);
+  if (e != cudaSuccess) return cuda_status(e);
+  PrefillArgs p{};
+  p.proj = ctx->proj;
+  p.ld = ctx->Nin;
+  p.T = T;
+  p.conv_state = cst;
+  p.ssm = S;
+  p.conv_w = ctx->conv_w;
+  p.A_log = ctx->A_log;
+  p.dt_bias = ctx->dt_bias;
+  p.norm_w = ctx->norm_w;
+  p.Hk = c.n_k_heads;
+  p.Hv = c.n_v_heads;
+  p.D = D;
+  p.C = ctx->C;
+  p.Kc = c.conv_kernel;
+  p.l2_eps = c.l2_eps;
+  p.rms_eps = c.rms_eps;
+  p.ts_out = c.act_scale_out;
+  p.qn = ctx->qn;
+  p.kn = ctx->kn;
+  p.v = ctx->v;
+  p.beta = ctx->beta;
+  p.alpha = ctx->alpha;
+  p.o = ctx->o;
+  p.y_codes = ctx->y_codes;
+  p.y_scales = ctx->y_scales;
+  p.status = ctx->status;
+  e = launch_prefill_mix(p, ctx->conv_tmp, lc);
+  if (e != cudaSuccess) return cuda_status(e);
+  GemvArgs o{};
+  o.a_codes = ctx->y_codes;
+  o.a_scales = ctx->y_scales;
+  o.ts_a = c.act_scale_out;
+  o.w_codes = ctx->w_out_codes;
+  o.w_scales = ctx->w_out_scales;
+  o.ts_w0 = o.ts_w1 = ctx->ts_wout;
+  o.n_split = H;
+  o.c = out;
+  o.c_is_bf16 = 1;
+  o.ldc = H;
+  o.N = H;
+  o.K = ctx->Vd;
+  o.status = ctx->status;
+  return cuda_status(run_gemv(o, lc, T));
+}
+
+gdn_status gdn_check(gdn_ctx *ctx, int clear, void *stream) {
+  if (!ctx) return GDN_E_NULL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t flag = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&flag, ctx->status, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(ctx->status, 0, 4);
+  if (e != cudaSuccess) return GDN_E_CUDA;
+  return (gdn_status)flag;
+}
+
+}  // extern "C"

@@ -1,0 +1,247 @@
+// Shared device helpers of the GDN kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+#define GDN_DEV __device__ __forceinline__
+
+namespace gdn {
+
+// ---------------------------------------------------------------- status word
+// Sticky: the first non-zero code stays. Only error paths write it.
+GDN_DEV void flag_status(int32_t *status, int code) {
+  if (status) atomicCAS(reinterpret_cast<int *>(status), 0, code);
+}
+
+// ---------------------------------------------------------------- conversions
+GDN_DEV float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+GDN_DEV uint16_t f32_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t *>(&h);
+}
+
+// E4M3 (OCP e4m3fn), round to nearest even, saturate finite values to 448.
+// Returns the byte of `v` (v finite).
+GDN_DEV uint32_t e4m3_from_f32(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xFFu;
+}
+
+// E4M3 byte -> float (exact).
+GDN_DEV float e4m3_to_f32(uint32_t byte) {
+  uint32_t h2;
+  uint16_t in = uint16_t(byte & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFFu)));
+}
+
+// Two floats -> one byte of two E2M1 codes (lo in the low nibble), RNE, satfinite.
+GDN_DEV uint32_t e2m1x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r) : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+// One byte of two E2M1 codes -> half2 (low nibble in .x), exact.
+GDN_DEV __half2 e2m1x2_to_h2(uint32_t byte) {
+  uint32_t h2;
+  uint16_t in = uint16_t(byte & 0xFFu);
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.u8.u16 t, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2) : "h"(in));
+  return *reinterpret_cast<__half2 *>(&h2);
+}
+
+// ---------------------------------------------------------------- NVFP4 block quantiser
+// One 16-element block in FP32, in the fixed order of the library's NVFP4
+// reading: amax, t = amax * inv6ts, s = E4M3(t), d = e4m3(s) * ts, r = 1/d,
+// code = E2M1(x * r). inv6ts = 1 / (6 * ts), both FP32 roundings.
+// Returns false (scale 0, codes 0) when the block holds NaN or infinity.
+GDN_DEV bool quant_block16(const float (&v)[16], float ts, float inv6ts, uint32_t &codes_lo,
+                           uint32_t &codes_hi, uint32_t &scale) {
+  float amax = 0.0f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float a = fabsf(v[i]);
+    finite &= (a <= 3.402823466e38f);  // false for NaN and +inf
+    amax = fmaxf(amax, a);
+  }
+  codes_lo = codes_hi = 0u;
+  scale = 0u;
+  if (!finite) return false;
+  float t = __fmul_rn(amax, inv6ts);
+  scale = e4m3_from_f32(t);
+  float sv = e4m3_to_f32(scale);
+  if (sv == 0.0f) return true;
+  float r = __frcp_rn(__fmul_rn(sv, ts));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t b0 = e2m1x2_from_f32(__fmul_rn(v[2 * i], r), __fmul_rn(v[2 * i + 1], r));
+    uint32_t b1 = e2m1x2_from_f32(__fmul_rn(v[8 + 2 * i], r), __fmul_rn(v[8 + 2 * i + 1], r));
+    codes_lo |= b0 << (8 * i);
+    codes_hi |= b1 << (8 * i);
+  }
+  return true;
+}
+
+GDN_DEV float inv6ts_of(float ts) { return __frcp_rn(__fmul_rn(6.0f, ts)); }
+
+// ---------------------------------------------------------------- reductions
+// xor butterfly: partners add the same two values in either order, so every
+// lane ends with the bit-identical total.
+GDN_DEV float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Reduce NV (power of two, 1..32) per-lane values over the warp with
+// NV - 1 + log2(64/NV) shuffles instead of 5 * NV: each round halves the live
+// values, a lane keeping one half and sending the other to its partner.
+// Afterwards lane l holds the total of value reduce_index<NV>(l), and every
+// lane holding the same value index holds the bit-identical total.
+template <int NV>
+GDN_DEV float warp_transpose_reduce(float (&v)[NV], int lane) {
+  static_assert(NV >= 1 && NV <= 32 && (NV & (NV - 1)) == 0, "NV power of two <= 32");
+  // Halve the live values each round; partner lanes differ in bit `b`.
+  int live = NV;
+#pragma unroll
+  for (int b = 4; b >= 0; --b) {
+    if (live > 1) {
+      const int half = live >> 1;
+      const bool upper = (lane >> b) & 1;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < half) {
+          float send = upper ? v[i] : v[i + half];
+          float keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << b);
+        }
+      }
+      live = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1 << b);
+    }
+  }
+  return v[0];
+}
+
+// Which value's total lane `lane` holds after warp_transpose_reduce<NV>.
+template <int NV>
+GDN_DEV int reduce_index(int lane) {
+  int idx = 0, live = NV;
+#pragma unroll
+  for (int b = 4; b >= 0; --b) {
+    if (live > 1) {
+      const int half = live >> 1;
+      if ((lane >> b) & 1) idx += half;
+      live = half;
+    }
+  }
+  return idx;
+}
+
+// A lane that holds the total of value `idx` after warp_transpose_reduce<NV>.
+template <int NV>
+GDN_DEV int reduce_owner(int idx) {
+  int lane = 0, live = NV;
+#pragma unroll
+  for (int b = 4; b >= 0; --b) {
+    if (live > 1) {
+      const int half = live >> 1;
+      if (idx >= half) { lane |= 1 << b; idx -= half; }
+      live = half;
+    }
+  }
+  return lane;
+}
+
+GDN_DEV float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+GDN_DEV float siluf_(float x) { return x / (1.0f + expf(-x)); }
+GDN_DEV float softplusf_(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
+
+}  // namespace gdn
+
+// ---------------------------------------------------------------- launchers (internal)
+namespace gdn {
+struct LaunchCtx {
+  cudaStream_t stream;
+  int num_sms;
+};
+
+cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, float ts, uint8_t *codes,
+                            uint8_t *scales, int32_t *status, cudaStream_t stream);
+
+// C[M][N] (ldc) = A_hat[M][K] * W_hat[N][K]^T. A is BF16 rows (quantised inside
+// with ts_a; a_rows_valid may mark rows to treat as zero) or NVFP4. Rows of W
+// below n_split use ts_w0, the rest ts_w1. M <= 16.
+struct GemvArgs {
+  const uint16_t *a_bf16;   // [M][K] or null
+  const uint8_t *a_codes;   // [M][K/2] or null
+  const uint8_t *a_scales;  // [M][K/16]
+  float ts_a;
+  const int32_t *row_slot;  // optional: row m is zero when row_slot[m] < 0 or >= num_slots
+  int num_slots;
+  const uint8_t *w_codes, *w_scales;
+  float ts_w0, ts_w1;
+  int n_split;
+  void *c;
+  int c_is_bf16;
+  int ldc;
+  int M, N, K;
+  int32_t *status;
+};
+cudaError_t launch_gemv(const GemvArgs &a, const LaunchCtx &lc);
+
+struct MixArgs {
+  const uint16_t *qkvz;  // [B][ld_qkvz] BF16: q | k | v | z
+  int ld_qkvz;
+  const uint16_t *ba;    // [B][ld_ba] BF16: b | a
+  int ld_ba;
+  const int32_t *slot_ids;
+  int B, num_slots;
+  uint16_t *conv_state;       // [S][K-1][C]
+  float *ssm_state;           // [S][Hv][dv][dk]
+  const uint16_t *conv_w;     // [C][K]
+  const float *A_log, *dt_bias, *norm_w;
+  int Hk, Hv, D, C, Kc;
+  float l2_eps, rms_eps, ts_out;
+  uint8_t *y_codes;   // [B][Hv*dv/2] or null
+  uint8_t *y_scales;  // [B][Hv*dv/16]
+  float *y_f32;       // [B][Hv*dv] or null
+  int32_t *status;
+};
+cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc);
+
+struct PrefillArgs {
+  const uint16_t *proj;  // [T][ld] BF16: q | k | v | z | b | a
+  int ld, T;
+  uint16_t *conv_state;  // this slot's [K-1][C]
+  float *ssm;            // this slot's [Hv][D][D]
+  const uint16_t *conv_w;
+  const float *A_log, *dt_bias, *norm_w;
+  int Hk, Hv, D, C, Kc;
+  float l2_eps, rms_eps, ts_out;
+  float *qn, *kn;        // [T][Hk][D]
+  float *v;              // [T][Hv][D]
+  float *beta, *alpha;   // [T][Hv]
+  float *o;              // [T][Hv][D]
+  uint8_t *y_codes;      // [T][Hv*D/2]
+  uint8_t *y_scales;     // [T][Hv*D/16]
+  int32_t *status;
+};
+cudaError_t launch_prefill_mix(const PrefillArgs &a, uint16_t *tmp, const LaunchCtx &lc);
+
+}  // namespace gdn

@@ -1,0 +1,285 @@
+// Token mixing of one decode step, fused: depthwise causal conv + SiLU, q/k L2
+// norm, the beta/g gates, the gated delta rule on the FP32 state, the z-gated
+// RMSNorm and the NVFP4 quantisation of its output.
+//
+// Work split: one CTA per (row b, value head h, slice of NS) owns R = D/NS rows
+// of that head's state S[h] (stored [d_v][d_k], Rocket blog "A reduction
+// barrier makes Qwen GDN graph replay bit exact": FlashInfer's pretranspose
+// decode layout). Each warp keeps RPW state rows in registers, one row spread
+// over the 32 lanes, so S k and S q are row dot products.
+//
+// A thread-block cluster groups the G = Hv/Hk value heads of one key head and
+// their NS slices. It serves two purposes:
+//  * the q/k conv state of the key head is read by all G*NS CTAs and written
+//    back by cluster rank 0 only after every CTA has passed a cluster barrier
+//    that follows its reads;
+//  * the RMSNorm needs sum(o^2) over all d_v rows of a head: slices exchange
+//    their partial sums through distributed shared memory in a fixed order.
+//
+// Shared-memory reductions keep the value in a register and pass a barrier
+// before the shared slot is reused (the lesson of the same Rocket entry).
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace gdn {
+
+namespace {
+
+constexpr int kRPW = 8;  // state rows per warp
+
+GDN_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+GDN_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+
+template <int D, int NS>
+__global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
+  constexpr int R = D / NS;
+  constexpr int WARPS = R / kRPW;
+  constexpr int EPL = D / 32;
+  static_assert(R % 16 == 0 && WARPS >= 1, "slice must hold whole quantisation blocks");
+
+  __shared__ float s_q[D], s_k[D], s_v[R], s_o[R], s_y[R];
+  __shared__ uint16_t s_qk_new[3][2 * D];  // new conv state of the q/k channels (K_conv <= 4)
+  __shared__ float s_gsum[R / 16];         // sums of o^2 over 16-row groups, read by the peers
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = a.Hv / a.Hk;
+  const int h = blockIdx.x / NS, split = blockIdx.x % NS;
+  const int kh = h / G;
+  const int b = blockIdx.y;
+  const int row0 = split * R;  // first d_v row of this slice
+  const int vd = a.Hv * D;
+
+  // ---- which slot, and is it valid (range, no repeats)
+  const int slot = a.slot_ids[b];
+  bool live = slot >= 0 && slot < a.num_slots;
+  bool bad = slot < -1 || slot >= a.num_slots;
+  if (live) {
+    for (int j = 0; j < a.B; ++j)
+      if (j != b && a.slot_ids[j] == slot) { bad = true; live = false; }
+  }
+  if (bad && tid == 0 && blockIdx.x == 0) flag_status(a.status, GDN_E_RANGE);
+  if (!live) {  // padding: zero y for this slice, touch no state (whole cluster agrees)
+    for (int i = tid; i < R; i += blockDim.x) {
+      if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = 0.0f;
+      if (a.y_codes && (i & 1) == 0) a.y_codes[((size_t)b * vd + h * D + row0 + i) >> 1] = 0;
+      if (a.y_scales && (i & 15) == 0) a.y_scales[((size_t)b * vd + h * D + row0 + i) >> 4] = 0;
+    }
+    return;
+  }
+
+  // ---- conv + SiLU for q, k (key head kh, all D) and v (this slice)
+  const int C = a.C, Kc = a.Kc;
+  const uint16_t *xin = a.qkvz + (size_t)b * a.ld_qkvz;
+  uint16_t *cst = a.conv_state + (size_t)slot * (Kc - 1) * C;
+  const bool qk_writer = cluster.block_rank() == 0;
+  for (int t = tid; t < 2 * D + R; t += blockDim.x) {
+    int ch;
+    if (t < D) ch = kh * D + t;                                   // q
+    else if (t < 2 * D) ch = a.Hk * D + kh * D + (t - D);         // k
+    else ch = 2 * a.Hk * D + h * D + row0 + (t - 2 * D);          // v
+    float win[4];
+    for (int j = 0; j < Kc - 1; ++j) win[j] = bf16_bits_to_f32(cst[(size_t)j * C + ch]);
+    const uint16_t xn_bits = xin[ch];
+    win[Kc - 1] = bf16_bits_to_f32(xn_bits);
+    float pre = 0.0f;
+    for (int j = 0; j < Kc; ++j) pre = fmaf(bf16_bits_to_f32(a.conv_w[(size_t)ch * Kc + j]), win[j], pre);
+    const float out = siluf_(pre);
+    if (t < D) s_q[t] = out;
+    else if (t < 2 * D) s_k[t - D] = out;
+    else s_v[t - 2 * D] = out;
+    // new state: taps shift by one, newest raw input last
+    if (t < 2 * D) {
+      for (int j = 0; j < Kc - 2; ++j) s_qk_new[j][t] = cst[(size_t)(j + 1) * C + ch];
+      s_qk_new[Kc - 2][t] = xn_bits;
+    } else {  // v channels belong to this CTA alone
+      uint16_t nw[3];
+      for (int j = 0; j < Kc - 2; ++j) nw[j] = cst[(size_t)(j + 1) * C + ch];
+      nw[Kc - 2] = xn_bits;
+      for (int j = 0; j < Kc - 1; ++j) cst[(size_t)j * C + ch] = nw[j];
+    }
+  }
+  __syncthreads();
+  cluster_arrive();  // this CTA has read the shared q/k conv state
+
+  // ---- per-warp: normalised q, k in registers; k.q; gates
+  float kr[EPL], qr[EPL];
+  float ssk = 0.0f, ssq = 0.0f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    kr[e] = s_k[lane * EPL + e];
+    qr[e] = s_q[lane * EPL + e];
+    ssk = fmaf(kr[e], kr[e], ssk);
+    ssq = fmaf(qr[e], qr[e], ssq);
+  }
+  ssk = warp_sum(ssk);
+  ssq = warp_sum(ssq);
+  const float rk = 1.0f / sqrtf(ssk + a.l2_eps);
+  const float rq = (1.0f / sqrtf(ssq + a.l2_eps)) * (1.0f / sqrtf((float)D));
+  float kq = 0.0f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    kr[e] *= rk;
+    qr[e] *= rq;
+    kq = fmaf(kr[e], qr[e], kq);
+  }
+  kq = warp_sum(kq);
+  const uint16_t *bain = a.ba + (size_t)b * a.ld_ba;
+  const float beta = sigmoidf_(bf16_bits_to_f32(bain[h]));
+  const float g = -expf(a.A_log[h]) * softplusf_(bf16_bits_to_f32(bain[a.Hv + h]) + a.dt_bias[h]);
+  const float alpha = expf(g);
+
+  // ---- the delta rule on this warp's rows
+  {
+    const int lr0 = warp * kRPW;
+    float *S = a.ssm_state + (((size_t)slot * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
+    float st[kRPW][EPL];
+#pragma unroll
+    for (int j = 0; j < kRPW; ++j) {
+      if (EPL == 4) {
+        float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
+        st[j][0] = t4.x; st[j][1] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
+      } else if (EPL == 2) {
+        float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
+        st[j][0] = t2.x; st[j][1 % EPL] = t2.y;
+      } else {
+        st[j][0] = S[(size_t)j * D];
+      }
+    }
+    float vals[2 * kRPW];
+#pragma unroll
+    for (int j = 0; j < kRPW; ++j) {
+      float dk = 0.0f, dq = 0.0f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        dk = fmaf(st[j][e], kr[e], dk);
+        dq = fmaf(st[j][e], qr[e], dq);
+      }
+      vals[j] = dk;
+      vals[kRPW + j] = dq;
+    }
+    const float tot = warp_transpose_reduce<2 * kRPW>(vals, lane);
+#pragma unroll
+    for (int j = 0; j < kRPW; ++j) {
+      const float Sk = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(j));
+      const float Sq = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(kRPW + j));
+      // S <- alpha S; u = beta (v - S k); S <- S + u k^T; o = S q
+      //   => (alpha S) k = alpha Sk, o = alpha Sq + u (k . q)
+      const float u = beta * (s_v[lr0 + j] - alpha * Sk);
+      const float o = fmaf(u, kq, alpha * Sq);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) st[j][e] = fmaf(u, kr[e], alpha * st[j][e]);
+      if (lane == 0) s_o[lr0 + j] = o;
+    }
+#pragma unroll
+    for (int j = 0; j < kRPW; ++j) {
+      if (EPL == 4) {
+        *reinterpret_cast<float4 *>(S + (size_t)j * D) = make_float4(st[j][0], st[j][1], st[j][2 % EPL], st[j][3 % EPL]);
+      } else if (EPL == 2) {
+        *reinterpret_cast<float2 *>(S + (size_t)j * D) = make_float2(st[j][0], st[j][1 % EPL]);
+      } else {
+        S[(size_t)j * D] = st[j][0];
+      }
+    }
+  }
+
+  // every CTA of the cluster has read the q/k conv state: rank 0 writes it
+  cluster_wait();
+  if (qk_writer) {
+    for (int t = tid; t < 2 * D; t += blockDim.x) {
+      const int ch = t < D ? kh * D + t : a.Hk * D + kh * D + (t - D);
+      for (int j = 0; j < Kc - 1; ++j) cst[(size_t)j * C + ch] = s_qk_new[j][t];
+    }
+  }
+  __syncthreads();  // s_o complete
+
+  // ---- sum of o^2 over the head in one fixed order whatever NS is: 16-row group
+  // sums (rows in order), then the D/16 group sums in order, read from the
+  // slice that owns each group through distributed shared memory
+  if (tid < R / 16) {
+    float p = 0.0f;
+    for (int i = 0; i < 16; ++i) p = fmaf(s_o[tid * 16 + i], s_o[tid * 16 + i], p);
+    s_gsum[tid] = p;
+  }
+  float sumsq = 0.0f;
+  if (NS > 1) {
+    cluster.sync();  // every slice's group sums are written
+    const int gbase = (h % G) * NS;
+    for (int gi = 0; gi < D / 16; ++gi)
+      sumsq += *cluster.map_shared_rank(&s_gsum[gi % (R / 16)], gbase + gi / (R / 16));
+  } else {
+    __syncthreads();
+    for (int gi = 0; gi < D / 16; ++gi) sumsq += s_gsum[gi];
+  }
+  const float rstd = 1.0f / sqrtf(sumsq / (float)D + a.rms_eps);
+
+  // ---- gated RMSNorm -> y (FP32), then NVFP4 blocks of 16 rows
+  const uint16_t *zin = xin + 2 * a.Hk * D + vd + h * D + row0;
+  for (int i = tid; i < R; i += blockDim.x) {
+    const float y = s_o[i] * rstd * a.norm_w[row0 + i] * siluf_(bf16_bits_to_f32(zin[i]));
+    s_y[i] = y;
+    if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = y;
+  }
+  __syncthreads();
+  if (a.y_codes && tid < R / 16) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = s_y[tid * 16 + i];
+    uint32_t lo, hi, s;
+    if (!quant_block16(v, a.ts_out, inv6ts_of(a.ts_out), lo, hi, s)) flag_status(a.status, GDN_E_NONFINITE);
+    const size_t e0 = (size_t)b * vd + h * D + row0 + tid * 16;
+    *reinterpret_cast<uint2 *>(a.y_codes + (e0 >> 1)) = make_uint2(lo, hi);
+    a.y_scales[e0 >> 4] = uint8_t(s);
+  }
+  if (NS > 1) cluster.sync();  // peers may still read this CTA's s_gsum
+}
+
+template <int D, int NS>
+cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
+  const int G = a.Hv / a.Hk;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.Hv * NS, a.B, 1);
+  cfg.blockDim = dim3((D / NS / kRPW) * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = G * NS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mix_kernel<D, NS>, a);
+}
+
+}  // namespace
+
+// Slices per head: more CTAs when the batch is small (the state traffic of one
+// row is spread over more SMs), bounded by the portable cluster size 8.
+cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc) {
+  if (a.B <= 0) return cudaSuccess;
+  const int G = a.Hv / a.Hk;
+  int ns = a.B <= 2 ? 4 : (a.B <= 8 ? 2 : 1);
+  while (ns > 1 && G * ns > 8) ns >>= 1;
+  if (G > 8) return cudaErrorInvalidValue;
+  switch (a.D) {
+    case 128:
+      if (ns == 4) return launch_dn<128, 4>(a, lc);
+      if (ns == 2) return launch_dn<128, 2>(a, lc);
+      return launch_dn<128, 1>(a, lc);
+    case 64:
+      if (ns >= 4) return launch_dn<64, 4>(a, lc);
+      if (ns == 2) return launch_dn<64, 2>(a, lc);
+      return launch_dn<64, 1>(a, lc);
+    case 32:
+      if (ns >= 2) return launch_dn<32, 2>(a, lc);
+      return launch_dn<32, 1>(a, lc);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace gdn

@@ -1,0 +1,59 @@
+// NVFP4 activation quantiser (bloomery issue #565, Round 1, #687: W4A4 runs
+// with 4-bit activations): one thread per 16-element block.
+#include "common.cuh"
+
+namespace gdn {
+
+template <bool F32>
+__global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ x, int rows, int cols, float ts,
+                                                       uint8_t *__restrict__ codes,
+                                                       uint8_t *__restrict__ scales,
+                                                       int32_t *status) {
+  const int nb = cols >> 4;
+  const long long total = (long long)rows * nb;
+  const float inv6ts = inv6ts_of(ts);
+  for (long long blk = blockIdx.x * (long long)blockDim.x + threadIdx.x; blk < total;
+       blk += (long long)gridDim.x * blockDim.x) {
+    const long long r = blk / nb, b = blk % nb;
+    float v[16];
+    if (F32) {
+      const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(x) + r * cols + b * 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float4 q = p[i];
+        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+      }
+    } else {
+      const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + r * cols + b * 16);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint4 q = p[i];
+        uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+          v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      }
+    }
+    uint32_t lo, hi, s;
+    if (!quant_block16(v, ts, inv6ts, lo, hi, s)) flag_status(status, GDN_E_NONFINITE);
+    *reinterpret_cast<uint2 *>(codes + r * (cols >> 1) + b * 8) = make_uint2(lo, hi);
+    scales[r * nb + b] = uint8_t(s);
+  }
+}
+
+cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, float ts, uint8_t *codes,
+                            uint8_t *scales, int32_t *status, cudaStream_t stream) {
+  const long long total = (long long)rows * (cols / 16);
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (x_is_f32)
+    quantize_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(x, rows, cols, ts, codes, scales, status);
+  else
+    quantize_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(x, rows, cols, ts, codes, scales, status);
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
