@@ -1,0 +1,353 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 W4A4 Gated DeltaNet layer step on GB300.
+
+Headline workload: the full-width layer (hidden 2048, 16 key / 32 value heads,
+d 128, conv 4, NVFP4 weights) in decode bucket c1, replayed as a CUDA graph.
+One bench step = one decode step through a stack of L distinct layer
+instances (own weights and state each) whose footprint is > 4x the L2 cache,
+so every layer-step streams its weights and state from HBM. The reported value
+is microseconds per layer-step (lower is better).
+
+Also reported: buckets c2..c16, batch 256 and prefill tokens/s (extra keys),
+the roofline of the dominant kernel (the W4A4 projection GEMV), an
+end-to-end leg through the Python API with host buffers, SM clocks sampled
+during the timed region, and the CPU oracle timed on a bounded sample.
+
+--impl reference times the CPU oracle on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN layer decode us/step at c1..c16 & prefill tok/s; HBM GB/s vs GB300 peak"
+UNIT = "us/step"
+
+# Algorithmic bytes of one decode layer-step: weights once + per active sequence.
+W_BYTES = 14_155_776 + 73_728 + 4_718_592 + 65_536 + 256 + 512      # 19,014,400
+SEQ_BYTES = 4_194_304 + 98_304 + 4_096 + 4_096                       # 4,300,800
+GEMV_IN_BYTES = 12352 * (1024 + 128)                                  # qkvz+ba codes+scales
+
+
+def step_bytes(B: int) -> int:
+    return W_BYTES + B * SEQ_BYTES
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+
+def make_stack(pkg, synth, n_layers, B, max_batch, device="cuda"):
+    """n_layers layer contexts sharing one synthetic weight set (uploaded once
+    per context, so each has its own copy in HBM), each with B slots of state."""
+    import numpy as np
+    import torch
+    w = synth.layer_weights(synth.FULL, 1)
+    layers, states = [], []
+    conv0 = np.stack([synth.conv_state(synth.FULL, synth.slot_seed(s)) for s in range(B)])
+    ssm0 = np.stack([synth.ssm_state(synth.FULL, synth.slot_seed(s)) for s in range(B)])
+    x = np.stack([synth.x_tokens(synth.FULL, synth.slot_seed(s), 1)[0] for s in range(B)])
+    xd = torch.from_numpy(x.view(np.int16)).to(device)
+    for _ in range(n_layers):
+        L = pkg.layer_from_synth(w, max_batch=max_batch)
+        layers.append(L)
+        states.append((torch.from_numpy(conv0.view(np.int16)).to(device), torch.from_numpy(ssm0).to(device)))
+    return w, layers, states, xd
+
+
+def capture_stack(layers, states, xd, B):
+    import torch
+    ids = torch.arange(B, dtype=torch.int32, device="cuda")
+    outs = [torch.empty(B, layers[0].H, dtype=torch.int16, device="cuda") for _ in layers]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for L, (c, m), o in zip(layers, states, outs):
+            L.decode_step(xd[:B], ids, c, m, out=o)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for L, (c, m), o in zip(layers, states, outs):
+            L.decode_step(xd[:B], ids, c, m, out=o)
+    torch.cuda.synchronize()
+    return g, outs
+
+
+def time_graph(g, steps, warmup):
+    import torch
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per bench step
+
+
+def time_gemv(pkg, layers, xcodes, xscales, steps):
+    """The dominant kernel alone: the W4A4 projection GEMV over the stack's
+    qkvz weights (1 activation row, N = 12288 + 64 rows, K = 2048), one launch
+    per layer instance, timed with CUDA events on the launching stream."""
+    import torch
+    import numpy as np
+    from nvfp4_gated_deltanet_gb300 import synth
+    w = synth.layer_weights(synth.FULL, 1)
+    wc = np.concatenate([w.qkvz.codes, w.ba.codes])
+    ws = np.concatenate([w.qkvz.scales, w.ba.scales])
+    mats = [(torch.from_numpy(wc).cuda(), torch.from_numpy(ws).cuda()) for _ in range(len(layers))]
+    c = torch.empty(1, wc.shape[0], dtype=torch.bfloat16, device="cuda")
+    def one_pass():
+        for (a, b) in mats:
+            pkg.nvfp4_gemm(xcodes, xscales, 2.0 ** -8, a, b, 2.0 ** -6, c=c)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        one_pass()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        one_pass()
+    ms = time_graph(g, steps, 3)
+    return ms / len(mats) * 1e3, len(mats)  # us per launch
+
+
+def cpu_baseline_leg(seconds_budget=15.0):
+    """The oracle, single-threaded, on config-1 decode steps: a bounded sample."""
+    code = (
+        "import os,sys,time,json;sys.path.insert(0,%r);"
+        "from nvfp4_gated_deltanet_gb300 import synth;from oracle import gdn;import numpy as np;"
+        "w=synth.layer_weights(synth.FULL,1);L=gdn.Layer(w);x=synth.x_tokens(synth.FULL,101,1000);"
+        "c=synth.conv_state(synth.FULL,101)[None].copy();s=synth.ssm_state(synth.FULL,101)[None].copy();"
+        "L.decode_step(x[0:1],[0],c,s);t=time.time();n=0\n"
+        "while time.time()-t<%f and n<999:\n n+=1;L.decode_step(x[n:n+1],[0],c,s)\n"
+        "print(json.dumps({'n':n,'s':time.time()-t}))" % (ROOT, seconds_budget))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["s"] / d["n"] * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{d['n']} config-1 decode c1 layer-steps (full width), single thread, float64/int64 exact"}
+
+
+def reference_arm(args):
+    """--impl reference: the CPU oracle on the same workload and metric."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+    from nvfp4_gated_deltanet_gb300 import synth
+    from oracle import gdn
+    w = synth.layer_weights(synth.FULL, 1)
+    L = gdn.Layer(w)
+    x = synth.x_tokens(synth.FULL, 101, args.steps + args.warmup + 1)
+    c = synth.conv_state(synth.FULL, 101)[None].copy()
+    s = synth.ssm_state(synth.FULL, 101)[None].copy()
+    for i in range(args.warmup):
+        L.decode_step(x[i:i + 1], [0], c, s)
+    t = time.time()
+    for i in range(args.steps):
+        L.decode_step(x[args.warmup + i:args.warmup + i + 1], [0], c, s)
+    el = time.time() - t
+    us = el / args.steps * 1e6
+    cores = int(os.environ.get("OMP_NUM_THREADS", "0")) or (os.cpu_count() or 1)
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "gdn-decode-c1 full width (H2048 Hk16 Hv32 d128 K4), 1 layer-step per step"},
+            "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} config-1 decode c1 layer-steps"},
+            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="layer instances in the stack (0: > 4x L2)")
+    ap.add_argument("--no-extra", action="store_true", help="skip the c2..c16 / batch / prefill extras")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import nvfp4_gated_deltanet_gb300 as pkg
+    from nvfp4_gated_deltanet_gb300 import synth
+    pkg.lib()
+
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    per_layer = step_bytes(1)
+    n_layers = args.layers or max(4, -(-4 * l2 // per_layer) + 1)
+    w, layers, states, xd = make_stack(pkg, synth, n_layers, 16, 16)
+
+    # ---- headline: c1 through the stack
+    g1, _ = capture_stack(layers, states, xd, 1)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = time_graph(g1, args.steps, args.warmup)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    us_layer = ms * 1e3 / n_layers
+    hbm_peak, peak_kind = peaks()
+    gbs_step = step_bytes(1) / (us_layer * 1e-6) / 1e9
+
+    # ---- dominant kernel: the projection GEMV alone, live
+    xq, xs = pkg.nvfp4_quantize(xd[:1], 2.0 ** -8)
+    us_gemv, _ = time_gemv(pkg, layers, xq, xs, max(20, args.steps // 4))
+    gemv_gbs = GEMV_IN_BYTES / (us_gemv * 1e-6) / 1e9
+
+    # ---- e2e: the Python API with host buffers, copies inside the timed region
+    import numpy as np
+    xh = torch.empty(n_layers, 1, layers[0].H, dtype=torch.int16).pin_memory()
+    xh.copy_(xd[:1].cpu().expand(n_layers, 1, -1))
+    oh = torch.empty(n_layers, 1, layers[0].H, dtype=torch.int16).pin_memory()
+    xdev = torch.empty_like(xh, device="cuda")
+    odev = torch.empty_like(oh, device="cuda")
+    ids = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e2e_steps = max(5, args.steps // 10)
+    for it in range(e2e_steps + 2):
+        if it == 2:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        xdev.copy_(xh, non_blocking=True)
+        for i, (L, (c, m)) in enumerate(zip(layers, states)):
+            L.decode_step(xdev[i], ids, c, m, out=odev[i])
+        oh.copy_(odev, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_us = (time.perf_counter() - t0) / e2e_steps * 1e6 / n_layers
+
+    extra = {}
+    if not args.no_extra:
+        for B in (2, 4, 8, 16):
+            gB, _ = capture_stack(layers, states, xd, B)
+            msB = time_graph(gB, max(10, args.steps // 4), 3)
+            usB = msB * 1e3 / n_layers
+            extra[f"c{B}"] = {"us_per_layer_step": round(usB, 3),
+                              "hbm_gbs": round(step_bytes(B) / (usB * 1e-6) / 1e9, 1),
+                              "frac_of_peak": round(step_bytes(B) / (usB * 1e-6) / 1e9 / hbm_peak, 4)}
+            del gB
+        extra["c1"] = {"us_per_layer_step": round(us_layer, 3), "hbm_gbs": round(gbs_step, 1),
+                       "frac_of_peak": round(gbs_step / hbm_peak, 4)}
+
+    cpu = None if (args.no_cpu or rank != 0) else cpu_baseline_leg()
+    line = {
+        "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4-w4a4 (fp32 accum) + f32 state", "data": "synthetic",
+        "config": {"workload": "gdn-decode-c1", "hidden": 2048, "k_heads": 16, "v_heads": 32, "d": 128,
+                   "conv": 4, "batch": 1, "layers_per_step": n_layers,
+                   "l2_defeat": f"{n_layers} distinct layer instances, {n_layers * per_layer / 1e6:.0f} MB > 4x L2 "
+                                f"({l2 / 1e6:.0f} MB)", "graph": "one CUDA graph per bucket over the stack",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs_step": round(gbs_step, 1), "hbm_frac_step": round(gbs_step / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1> (W4A4 qkvz+ba projection, M=1)",
+                     "achieved": round(gemv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gemv_gbs / hbm_peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "us_per_launch": round(us_gemv, 3), "bytes_per_launch": GEMV_IN_BYTES},
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(xh.numel() * 2),
+                "d2h_bytes_per_step": int(oh.numel() * 2),
+                "path": "GatedDeltaNetLayer.decode_step (ctypes -> C ABI), pinned host x in / out back, eager launches"},
+        "gpu_launches": 3 * n_layers * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+        "extra": extra,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
