@@ -261,7 +261,7 @@ gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int 
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_status(e);
   if ((size_t)16 * (K >> 6) * (4 * 2 * 16 + 16) > 200 * 1024) return GDN_E_SHAPE;
-  LaunchCtx lc{static_cast<cudaStream_t>(stream), sms};
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), sms, false};  // B may come from a preceding kernel
   GemvArgs g{};
   g.a_codes = A->codes;
   g.a_scales = A->scales;
@@ -285,7 +285,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   if (!slot_ids) return GDN_E_NULL;
   if (!aligned16(slot_ids)) return GDN_E_ALIGN;
   if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
-  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms};
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, true};
   const int H = ctx->cfg.hidden;
   GemvArgs g{};
   g.a_bf16 = x;
@@ -344,7 +344,7 @@ gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, 
   if (!ba || !slot_ids) return GDN_E_NULL;
   if (!aligned16(ba) || !aligned16(slot_ids)) return GDN_E_ALIGN;
   if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
-  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms};
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, true};
   MixArgs m = mix_args(ctx);
   m.qkvz = qkvz;
   m.ld_qkvz = ctx->Nqkvz;
@@ -368,7 +368,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   if (T < 1 || T > ctx->cfg.max_prefill_tokens) return GDN_E_SHAPE;
   if (slot < 0 || slot >= num_slots) return GDN_E_RANGE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  LaunchCtx lc{s, ctx->num_sms};
+  LaunchCtx lc{s, ctx->num_sms, true};
   const gdn_config &c = ctx->cfg;
   const int H = c.hidden, D = c.d_k;
   uint16_t *cst = conv_state + (size_t)slot * (c.conv_kernel - 1) * ctx->C;

@@ -168,6 +168,53 @@ GDN_DEV int reduce_owner(int idx) {
   return lane;
 }
 
+// ---------------------------------------------------------------- async copies, mbarriers, PDL
+GDN_DEV uint32_t smem_u32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+GDN_DEV void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+// Make barrier initialisation visible to the async (TMA) proxy.
+GDN_DEV void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
+}
+GDN_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+GDN_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Every wait is bounded: ~2^31 SM cycles (about one second at 2 GHz), then the
+// caller records GDN_E_TIMEOUT and gives up instead of hanging the GPU.
+constexpr long long kWaitCycles = 1LL << 31;
+GDN_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+// Bulk (non-tensor) copy global -> shared, completion counted on `bar`.
+// dst, src 16-byte aligned, bytes a multiple of 16.
+GDN_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Programmatic dependent launch: wait for the preceding grid (no-op when the
+// launch did not ask for it); let the next grid start its prologue.
+GDN_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+GDN_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 GDN_DEV float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
 GDN_DEV float siluf_(float x) { return x / (1.0f + expf(-x)); }
 GDN_DEV float softplusf_(float x) { return x > 20.0f ? x : log1pf(expf(x)); }
@@ -179,6 +226,8 @@ namespace gdn {
 struct LaunchCtx {
   cudaStream_t stream;
   int num_sms;
+  bool pdl;  // launch with programmatic stream serialization (kernels read only
+             // constants -- weights -- before griddepcontrol.wait)
 };
 
 cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, float ts, uint8_t *codes,

@@ -1,13 +1,18 @@
-// Block-scaled W4A4 product for a few activation rows (decode buckets), on the
-// CUDA cores: the weights are streamed from HBM once with 128-bit loads and
-// every activation row is applied to each weight block while it is in
-// registers.
+// Block-scaled W4A4 product for a few activation rows (decode buckets) on the
+// CUDA cores. The weights are read from HBM exactly once: every warp owns a
+// contiguous range of weight rows and streams them, two rows per stage, into
+// its own shared-memory ring with bulk asynchronous copies (cp.async.bulk,
+// completion on an mbarrier). The copies of the first stages are issued before
+// anything else -- before the activation prologue and before waiting on the
+// preceding kernel (programmatic dependent launch), since weights never depend
+// on it -- so the whole matrix is in flight from the first microsecond.
 //
 // Exactness inside a 16-block: E2M1 values are converted to FP16 (exact), each
 // half of an FP16x2 accumulator sums 8 products (|sum| <= 8*36 = 288 on a 1/4
 // grid, exact in FP16), so the block's integer-valued dot product is exact;
 // times the two E4M3 scales it is still exact in FP32. Only the sum over
-// blocks rounds (FP32, fixed order: lane-local chunks, then a fixed warp tree).
+// blocks rounds (FP32, fixed order: lane-local pieces, then a fixed warp tree),
+// so results do not depend on how rows are spread over warps or on M.
 #include "common.cuh"
 
 namespace gdn {
@@ -15,26 +20,97 @@ namespace gdn {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kRowsPerWarp = 2;
+constexpr int kMaxStages = 4;
+constexpr int kBarBytes = kWarps * kMaxStages * 8;  // mbarriers, 256 bytes
 
-// Shared-memory layout of the activations, chosen so a warp's 128-bit loads
-// (lane l reads 64-element chunk c = l + 32 j) are contiguous:
-//   xh[((m * 4 + blk) * 2 + half) * nchunk + c] : uint4 = 4 half2 (8 values)
-//   xs[(m * 4 + blk) * nchunk + c]              : float E4M3 block scale
-struct XSmem {
-  uint4 *xh;
-  float *xs;
-};
+// A "piece" is 32 elements (two 16-blocks): 16 code bytes + 2 scale bytes.
+// Lane l handles pieces l, l+32, ... of a row, so a warp's 128-bit shared loads
+// are contiguous. Activations live in shared memory as FP16 E2M1 values:
+//   xh[((m * 2 + blk) * 2 + half) * npiece + p] : uint4 = 4 half2 (8 values)
+//   xs[(m * 2 + blk) * npiece + p]              : float E4M3 block scale
 
 template <int MB>
-__global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int K = a.K;
-  const int nchunk = K >> 6;
-  XSmem sm{reinterpret_cast<uint4 *>(smem),
-           reinterpret_cast<float *>(smem + (size_t)MB * 4 * 2 * nchunk * sizeof(uint4))};
+GDN_DEV void dot_row(const uint8_t *codes, const uint8_t *scales, int npiece, int M, const uint4 *xh,
+                     const float *xs, int lane, float (&acc)[MB]) {
+  for (int p = lane; p < npiece; p += 32) {
+    const uint4 wc = *reinterpret_cast<const uint4 *>(codes + (size_t)p * 16);
+    const uint32_t ws = *reinterpret_cast<const uint16_t *>(scales + (size_t)p * 2);
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const uint32_t w0 = blk == 0 ? wc.x : wc.z;
+      const uint32_t w1 = blk == 0 ? wc.y : wc.w;
+      __half2 wv[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        wv[i] = e2m1x2_to_h2(w0 >> (8 * i));
+        wv[4 + i] = e2m1x2_to_h2(w1 >> (8 * i));
+      }
+      const float sw = e4m3_to_f32(ws >> (8 * blk));
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        if (m < M) {
+          const uint4 x0 = xh[((m * 2 + blk) * 2 + 0) * npiece + p];
+          const uint4 x1 = xh[((m * 2 + blk) * 2 + 1) * npiece + p];
+          const __half2 *xa = reinterpret_cast<const __half2 *>(&x0);
+          const __half2 *xb = reinterpret_cast<const __half2 *>(&x1);
+          __half2 s2 = __float2half2_rn(0.0f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s2 = __hfma2(wv[i], xa[i], s2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s2 = __hfma2(wv[4 + i], xb[i], s2);
+          const float blocksum = __low2float(s2) + __high2float(s2);
+          acc[m] = fmaf(blocksum, xs[(m * 2 + blk) * npiece + p] * sw, acc[m]);
+        }
+      }
+    }
+  }
+}
 
-  // ---- prologue: the activation rows as FP16 E2M1 values + FP32 block scales
+// TMA = stream weights through the shared ring (K % 256 == 0, so every copy
+// is 16-byte aligned and sized); otherwise lanes read them from global memory.
+template <int MB, bool TMA>
+__global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a, int rows_per_warp, int stages) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int K = a.K, npiece = K >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t cbytes = (size_t)K >> 1, sbytes = (size_t)K >> 4;  // per weight row
+  const int stage_bytes = 2 * (int)(cbytes + sbytes);
+
+  // smem: [barriers kWarps*stages][ring kWarps*stages*stage_bytes][xh][xs]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+  unsigned char *ring = smem + kBarBytes;
+  const size_t ring_bytes = TMA ? (size_t)kWarps * stages * stage_bytes : 0;
+  uint4 *xh = reinterpret_cast<uint4 *>(ring + ring_bytes);
+  float *xs = reinterpret_cast<float *>(ring + ring_bytes + (size_t)MB * 4 * npiece * sizeof(uint4));
+
+  const int gw = blockIdx.x * kWarps + warp;
+  const int r_begin = min(gw * rows_per_warp, a.N);
+  const int r_end = min(r_begin + rows_per_warp, a.N);
+  const int npairs = (r_end - r_begin + 1) >> 1;
+  uint64_t *mybar = bars + warp * stages;
+  unsigned char *myring = ring + (size_t)warp * stages * stage_bytes;
+
+  auto issue = [&](int pair) {
+    const int n0 = r_begin + 2 * pair;
+    const int nr = min(2, r_end - n0);
+    const int st = pair % stages;
+    unsigned char *dst = myring + (size_t)st * stage_bytes;
+    const uint32_t cb = (uint32_t)(nr * cbytes), sb = (uint32_t)(nr * sbytes);
+    mbar_arrive_expect_tx(mybar + st, cb + sb);
+    bulk_g2s(dst, a.w_codes + (size_t)n0 * cbytes, cb, mybar + st);
+    bulk_g2s(dst + 2 * cbytes, a.w_scales + (size_t)n0 * sbytes, sb, mybar + st);
+  };
+  if (TMA && lane == 0) {
+    for (int s = 0; s < stages; ++s) mbar_init(mybar + s, 1);
+    fence_barrier_init();
+    for (int s = 0; s < min(stages, npairs); ++s) issue(s);
+  }
+  __syncwarp();
+
+  // the activations come from the preceding kernel
+  pdl_wait();
+
+  // ---- prologue: activation rows as FP16 E2M1 values + FP32 block scales
   {
     const int nblk = K >> 4;
     const float inv6ts = inv6ts_of(a.ts_a);
@@ -69,7 +145,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a) {
           s = a.a_scales[(size_t)m * nblk + j];
         }
       }
-      const int c = j >> 2, blk = j & 3;
+      const int p = j >> 1, blk = j & 1;
       __half2 h[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -77,81 +153,55 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a) {
         h[4 + i] = e2m1x2_to_h2(hi >> (8 * i));
       }
       const uint4 *hv = reinterpret_cast<const uint4 *>(h);
-      sm.xh[((m * 4 + blk) * 2 + 0) * nchunk + c] = hv[0];
-      sm.xh[((m * 4 + blk) * 2 + 1) * nchunk + c] = hv[1];
-      sm.xs[(m * 4 + blk) * nchunk + c] = e4m3_to_f32(s);
+      xh[((m * 2 + blk) * 2 + 0) * npiece + p] = hv[0];
+      xh[((m * 2 + blk) * 2 + 1) * npiece + p] = hv[1];
+      xs[(m * 2 + blk) * npiece + p] = e4m3_to_f32(s);
     }
   }
   __syncthreads();
+  pdl_launch_dependents();
 
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const int tw = gridDim.x * kWarps;
-  const size_t ldw = (size_t)(K >> 1), lds = (size_t)(K >> 4);
-
-  for (int n0 = gw * kRowsPerWarp; n0 < a.N; n0 += tw * kRowsPerWarp) {
-    float acc[kRowsPerWarp][MB];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
-#pragma unroll
-      for (int m = 0; m < MB; ++m) acc[r][m] = 0.0f;
-
-    for (int c = lane; c < nchunk; c += 32) {
-      uint4 wc[kRowsPerWarp][2];
-      uint32_t ws[kRowsPerWarp];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-        const int n = min(n0 + r, a.N - 1);
-        const uint4 *pc = reinterpret_cast<const uint4 *>(a.w_codes + n * ldw + (size_t)c * 32);
-        wc[r][0] = __ldcs(pc);
-        wc[r][1] = __ldcs(pc + 1);
-        ws[r] = __ldcs(reinterpret_cast<const unsigned int *>(a.w_scales + n * lds + (size_t)c * 4));
+  constexpr int NV = 2 * MB;
+  bool ok = true;
+  for (int pair = 0; pair < npairs; ++pair) {
+    const int n0 = r_begin + 2 * pair;
+    const int nr = min(2, r_end - n0);
+    const int st = pair % stages;
+    const unsigned char *codes0, *scales0;
+    if (TMA) {
+      if (!mbar_wait(mybar + st, (uint32_t)((pair / stages) & 1))) {
+        // give up on this warp's rows; let its copies still in flight land
+        // (each wait bounded) before the CTA's shared memory goes away
+        ok = false;
+        for (int q = pair + 1; q < min(pair + stages, npairs); ++q)
+          (void)mbar_wait(mybar + q % stages, (uint32_t)((q / stages) & 1));
+        break;
       }
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) {
-          const uint32_t w0 = (blk < 2) ? (blk == 0 ? wc[r][0].x : wc[r][0].z) : (blk == 2 ? wc[r][1].x : wc[r][1].z);
-          const uint32_t w1 = (blk < 2) ? (blk == 0 ? wc[r][0].y : wc[r][0].w) : (blk == 2 ? wc[r][1].y : wc[r][1].w);
-          __half2 wv[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            wv[i] = e2m1x2_to_h2(w0 >> (8 * i));
-            wv[4 + i] = e2m1x2_to_h2(w1 >> (8 * i));
-          }
-          const float sw = e4m3_to_f32(ws[r] >> (8 * blk));
-#pragma unroll
-          for (int m = 0; m < MB; ++m) {
-            if (m < a.M) {
-              const uint4 x0 = sm.xh[((m * 4 + blk) * 2 + 0) * nchunk + c];
-              const uint4 x1 = sm.xh[((m * 4 + blk) * 2 + 1) * nchunk + c];
-              const __half2 *xa = reinterpret_cast<const __half2 *>(&x0);
-              const __half2 *xb = reinterpret_cast<const __half2 *>(&x1);
-              __half2 s2 = __float2half2_rn(0.0f);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) s2 = __hfma2(wv[i], xa[i], s2);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) s2 = __hfma2(wv[4 + i], xb[i], s2);
-              const float blocksum = __low2float(s2) + __high2float(s2);
-              acc[r][m] = fmaf(blocksum, sm.xs[(m * 4 + blk) * nchunk + c] * sw, acc[r][m]);
-            }
-          }
-        }
-      }
+      codes0 = myring + (size_t)st * stage_bytes;
+      scales0 = codes0 + 2 * cbytes;
+    } else {
+      codes0 = a.w_codes + (size_t)n0 * cbytes;
+      scales0 = a.w_scales + (size_t)n0 * sbytes;
     }
-
-    // ---- warp reduction of the kRowsPerWarp * MB partial sums, then store
-    constexpr int NV = kRowsPerWarp * MB;
     float v[NV];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
+    for (int r = 0; r < 2; ++r) {
+      float acc[MB];
 #pragma unroll
-      for (int m = 0; m < MB; ++m) v[r * MB + m] = acc[r][m];
+      for (int m = 0; m < MB; ++m) acc[m] = 0.0f;
+      if (r < nr) dot_row<MB>(codes0 + r * cbytes, scales0 + r * sbytes, npiece, a.M, xh, xs, lane, acc);
+#pragma unroll
+      for (int m = 0; m < MB; ++m) v[r * MB + m] = acc[m];
+    }
+    if (TMA) {
+      __syncwarp();  // every lane is done with this stage before it is refilled
+      if (lane == 0 && pair + stages < npairs) issue(pair + stages);
+    }
     const float tot = warp_transpose_reduce<NV>(v, lane);
     const int idx = reduce_index<NV>(lane);
     const int r = idx / MB, m = idx % MB;
     const int n = n0 + r;
-    if (lane == reduce_owner<NV>(idx) && m < a.M && n < a.N) {
+    if (lane == reduce_owner<NV>(idx) && m < a.M && r < nr) {
       const float tsw = n < a.n_split ? a.ts_w0 : a.ts_w1;
       const float y = tot * (a.ts_a * tsw);
       if (a.c_is_bf16)
@@ -160,23 +210,59 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a) {
         static_cast<float *>(a.c)[(size_t)m * a.ldc + n] = y;
     }
   }
+  if (TMA && !ok) {
+    if (lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+  }
+}
+
+template <int MB, bool TMA>
+cudaError_t launch_cfg(const GemvArgs &a, const LaunchCtx &lc) {
+  const int npiece = a.K >> 5;
+  const size_t act = (size_t)MB * npiece * (4 * sizeof(uint4) + 2 * sizeof(float));
+  const size_t stage_bytes = 2 * ((size_t)a.K / 2 + a.K / 16);
+  const size_t budget = 200 * 1024;
+  // rows per warp: spread the rows over every warp that fits (2 CTAs per SM
+  // when shared memory allows), in whole row pairs; the ring has at most as
+  // many stages as a warp has row pairs
+  int stages = TMA ? kMaxStages : 1, rpw = 2;
+  size_t smem = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    if (TMA)
+      while (stages > 1 && kBarBytes + act + kWarps * stages * stage_bytes > budget) --stages;
+    smem = kBarBytes + (TMA ? kWarps * stages * stage_bytes : 0) + act;
+    const int ctas_per_sm = smem * 2 <= 220 * 1024 ? 2 : 1;
+    const int warps_total = lc.num_sms * ctas_per_sm * kWarps;
+    rpw = (a.N + warps_total - 1) / warps_total;
+    rpw = (rpw + 1) & ~1;
+    if (rpw < 2) rpw = 2;
+    if (TMA && stages > rpw / 2) stages = rpw / 2;
+  }
+  smem = kBarBytes + (TMA ? kWarps * stages * stage_bytes : 0) + act;
+  if (smem > budget) return cudaErrorInvalidValue;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MB, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int ctas = (a.N + kWarps * rpw - 1) / (kWarps * rpw);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(kWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<MB, TMA>, a, rpw, stages);
 }
 
 template <int MB>
 cudaError_t launch_mb(const GemvArgs &a, const LaunchCtx &lc) {
-  const size_t smem = (size_t)MB * (a.K >> 6) * (4 * 2 * sizeof(uint4) + 4 * sizeof(float));
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  int ctas = (a.N + kWarps * kRowsPerWarp - 1) / (kWarps * kRowsPerWarp);
-  const int cap = lc.num_sms * 4;
-  if (ctas > cap) ctas = cap;
-  gemv_kernel<MB><<<ctas, kWarps * 32, smem, lc.stream>>>(a);
-  return cudaGetLastError();
+  if (a.K % 256 == 0) return launch_cfg<MB, true>(a, lc);
+  return launch_cfg<MB, false>(a, lc);
 }
 
 }  // namespace

@@ -37,8 +37,11 @@ template <int D, int NS>
 __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   constexpr int R = D / NS;
   constexpr int WARPS = R / kRPW;
+  constexpr int THREADS = WARPS * 32;
   constexpr int EPL = D / 32;
-  static_assert(R % 16 == 0 && WARPS >= 1, "slice must hold whole quantisation blocks");
+  constexpr int NCH = 2 * D + R;                        // conv channels this CTA needs
+  constexpr int CPT = (NCH + THREADS - 1) / THREADS;    // channels per thread
+  static_assert(R % 16 == 0 && WARPS >= 1 && R <= THREADS, "slice must hold whole quantisation blocks");
 
   __shared__ float s_q[D], s_k[D], s_v[R], s_o[R], s_y[R];
   __shared__ uint16_t s_qk_new[3][2 * D];  // new conv state of the q/k channels (K_conv <= 4)
@@ -52,9 +55,38 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   const int b = blockIdx.y;
   const int row0 = split * R;  // first d_v row of this slice
   const int vd = a.Hv * D;
+  const int C = a.C, Kc = a.Kc;
+
+  // ---- constants first (written by no kernel): conv taps, gate and norm params
+  int ch[CPT];
+  float cw[CPT][4];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int t = tid + c * THREADS;
+    int q = 0;
+    if (t < D) q = kh * D + t;                                  // q
+    else if (t < 2 * D) q = a.Hk * D + kh * D + (t - D);        // k
+    else if (t < NCH) q = 2 * a.Hk * D + h * D + row0 + (t - 2 * D);  // v
+    ch[c] = q;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cw[c][j] = (t < NCH && j < Kc) ? bf16_bits_to_f32(a.conv_w[(size_t)q * Kc + j]) : 0.0f;
+  }
+  const float A_log = a.A_log[h], dt_bias = a.dt_bias[h];
+  const float nw = tid < R ? a.norm_w[row0 + tid] : 0.0f;
+
+  // ---- then what the preceding kernel produced: projections (and slot ids)
+  pdl_wait();
+  const int slot = a.slot_ids[b];
+  const uint16_t *xin = a.qkvz + (size_t)b * a.ld_qkvz;
+  uint16_t xn[CPT];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) xn[c] = (tid + c * THREADS < NCH) ? xin[ch[c]] : uint16_t(0);
+  const float zv = tid < R ? bf16_bits_to_f32(xin[2 * a.Hk * D + vd + h * D + row0 + tid]) : 0.0f;
+  const uint16_t *bain = a.ba + (size_t)b * a.ld_ba;
+  const float b_raw = bf16_bits_to_f32(bain[h]);
+  const float a_raw = bf16_bits_to_f32(bain[a.Hv + h]);
 
   // ---- which slot, and is it valid (range, no repeats)
-  const int slot = a.slot_ids[b];
   bool live = slot >= 0 && slot < a.num_slots;
   bool bad = slot < -1 || slot >= a.num_slots;
   if (live) {
@@ -63,6 +95,7 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   }
   if (bad && tid == 0 && blockIdx.x == 0) flag_status(a.status, GDN_E_RANGE);
   if (!live) {  // padding: zero y for this slice, touch no state (whole cluster agrees)
+    pdl_launch_dependents();
     for (int i = tid; i < R; i += blockDim.x) {
       if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = 0.0f;
       if (a.y_codes && (i & 1) == 0) a.y_codes[((size_t)b * vd + h * D + row0 + i) >> 1] = 0;
@@ -71,35 +104,56 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
     return;
   }
 
-  // ---- conv + SiLU for q, k (key head kh, all D) and v (this slice)
-  const int C = a.C, Kc = a.Kc;
-  const uint16_t *xin = a.qkvz + (size_t)b * a.ld_qkvz;
+  // ---- state loads, all issued before any use: conv taps and this warp's rows of S
   uint16_t *cst = a.conv_state + (size_t)slot * (Kc - 1) * C;
+  uint16_t tap[CPT][3];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c)
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+      tap[c][j] = (tid + c * THREADS < NCH && j < Kc - 1) ? cst[(size_t)j * C + ch[c]] : uint16_t(0);
+  const int lr0 = warp * kRPW;
+  float *S = a.ssm_state + (((size_t)slot * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
+  float st[kRPW][EPL];
+#pragma unroll
+  for (int j = 0; j < kRPW; ++j) {
+    if (EPL == 4) {
+      float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
+      st[j][0] = t4.x; st[j][1 % EPL] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
+    } else if (EPL == 2) {
+      float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
+      st[j][0] = t2.x; st[j][1 % EPL] = t2.y;
+    } else {
+      st[j][0] = S[(size_t)j * D];
+    }
+  }
+
+  // ---- conv + SiLU for q, k (key head kh, all D) and v (this slice)
   const bool qk_writer = cluster.block_rank() == 0;
-  for (int t = tid; t < 2 * D + R; t += blockDim.x) {
-    int ch;
-    if (t < D) ch = kh * D + t;                                   // q
-    else if (t < 2 * D) ch = a.Hk * D + kh * D + (t - D);         // k
-    else ch = 2 * a.Hk * D + h * D + row0 + (t - 2 * D);          // v
-    float win[4];
-    for (int j = 0; j < Kc - 1; ++j) win[j] = bf16_bits_to_f32(cst[(size_t)j * C + ch]);
-    const uint16_t xn_bits = xin[ch];
-    win[Kc - 1] = bf16_bits_to_f32(xn_bits);
-    float pre = 0.0f;
-    for (int j = 0; j < Kc; ++j) pre = fmaf(bf16_bits_to_f32(a.conv_w[(size_t)ch * Kc + j]), win[j], pre);
-    const float out = siluf_(pre);
-    if (t < D) s_q[t] = out;
-    else if (t < 2 * D) s_k[t - D] = out;
-    else s_v[t - 2 * D] = out;
-    // new state: taps shift by one, newest raw input last
-    if (t < 2 * D) {
-      for (int j = 0; j < Kc - 2; ++j) s_qk_new[j][t] = cst[(size_t)(j + 1) * C + ch];
-      s_qk_new[Kc - 2][t] = xn_bits;
-    } else {  // v channels belong to this CTA alone
-      uint16_t nw[3];
-      for (int j = 0; j < Kc - 2; ++j) nw[j] = cst[(size_t)(j + 1) * C + ch];
-      nw[Kc - 2] = xn_bits;
-      for (int j = 0; j < Kc - 1; ++j) cst[(size_t)j * C + ch] = nw[j];
+#pragma unroll
+  for (int c = 0; c < CPT; ++c) {
+    const int t = tid + c * THREADS;
+    if (t < NCH) {
+      float pre = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < Kc) {
+          const uint16_t bits = j < Kc - 1 ? tap[c][j < 3 ? j : 2] : xn[c];
+          pre = fmaf(cw[c][j], bf16_bits_to_f32(bits), pre);
+        }
+      }
+      const float out = siluf_(pre);
+      if (t < D) s_q[t] = out;
+      else if (t < 2 * D) s_k[t - D] = out;
+      else s_v[t - 2 * D] = out;
+      // new state: taps shift by one, newest raw input last
+      if (t < 2 * D) {
+        for (int j = 0; j < Kc - 2; ++j) s_qk_new[j][t] = tap[c][j + 1 < 3 ? j + 1 : 2];
+        s_qk_new[Kc - 2][t] = xn[c];
+      } else {  // v channels belong to this CTA alone
+        for (int j = 0; j < Kc - 2; ++j) cst[(size_t)j * C + ch[c]] = tap[c][j + 1 < 3 ? j + 1 : 2];
+        cst[(size_t)(Kc - 2) * C + ch[c]] = xn[c];
+      }
     }
   }
   __syncthreads();
@@ -127,28 +181,12 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
     kq = fmaf(kr[e], qr[e], kq);
   }
   kq = warp_sum(kq);
-  const uint16_t *bain = a.ba + (size_t)b * a.ld_ba;
-  const float beta = sigmoidf_(bf16_bits_to_f32(bain[h]));
-  const float g = -expf(a.A_log[h]) * softplusf_(bf16_bits_to_f32(bain[a.Hv + h]) + a.dt_bias[h]);
+  const float beta = sigmoidf_(b_raw);
+  const float g = -expf(A_log) * softplusf_(a_raw + dt_bias);
   const float alpha = expf(g);
 
   // ---- the delta rule on this warp's rows
   {
-    const int lr0 = warp * kRPW;
-    float *S = a.ssm_state + (((size_t)slot * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
-    float st[kRPW][EPL];
-#pragma unroll
-    for (int j = 0; j < kRPW; ++j) {
-      if (EPL == 4) {
-        float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
-        st[j][0] = t4.x; st[j][1] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
-      } else if (EPL == 2) {
-        float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
-        st[j][0] = t2.x; st[j][1 % EPL] = t2.y;
-      } else {
-        st[j][0] = S[(size_t)j * D];
-      }
-    }
     float vals[2 * kRPW];
 #pragma unroll
     for (int j = 0; j < kRPW; ++j) {
@@ -177,7 +215,8 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
 #pragma unroll
     for (int j = 0; j < kRPW; ++j) {
       if (EPL == 4) {
-        *reinterpret_cast<float4 *>(S + (size_t)j * D) = make_float4(st[j][0], st[j][1], st[j][2 % EPL], st[j][3 % EPL]);
+        *reinterpret_cast<float4 *>(S + (size_t)j * D) =
+            make_float4(st[j][0], st[j][1 % EPL], st[j][2 % EPL], st[j][3 % EPL]);
       } else if (EPL == 2) {
         *reinterpret_cast<float2 *>(S + (size_t)j * D) = make_float2(st[j][0], st[j][1 % EPL]);
       } else {
@@ -190,11 +229,12 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   cluster_wait();
   if (qk_writer) {
     for (int t = tid; t < 2 * D; t += blockDim.x) {
-      const int ch = t < D ? kh * D + t : a.Hk * D + kh * D + (t - D);
-      for (int j = 0; j < Kc - 1; ++j) cst[(size_t)j * C + ch] = s_qk_new[j][t];
+      const int q = t < D ? kh * D + t : a.Hk * D + kh * D + (t - D);
+      for (int j = 0; j < Kc - 1; ++j) cst[(size_t)j * C + q] = s_qk_new[j][t];
     }
   }
   __syncthreads();  // s_o complete
+  pdl_launch_dependents();
 
   // ---- sum of o^2 over the head in one fixed order whatever NS is: 16-row group
   // sums (rows in order), then the D/16 group sums in order, read from the
@@ -217,11 +257,10 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   const float rstd = 1.0f / sqrtf(sumsq / (float)D + a.rms_eps);
 
   // ---- gated RMSNorm -> y (FP32), then NVFP4 blocks of 16 rows
-  const uint16_t *zin = xin + 2 * a.Hk * D + vd + h * D + row0;
-  for (int i = tid; i < R; i += blockDim.x) {
-    const float y = s_o[i] * rstd * a.norm_w[row0 + i] * siluf_(bf16_bits_to_f32(zin[i]));
-    s_y[i] = y;
-    if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = y;
+  if (tid < R) {
+    const float y = s_o[tid] * rstd * nw * siluf_(zv);
+    s_y[tid] = y;
+    if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + tid] = y;
   }
   __syncthreads();
   if (a.y_codes && tid < R / 16) {
@@ -245,13 +284,15 @@ cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
   cfg.blockDim = dim3((D / NS / kRPW) * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = G * NS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, mix_kernel<D, NS>, a);
 }
 
