@@ -157,9 +157,12 @@ def time_graph(g, steps, warmup):
 
 def time_gemv(pkg, layers, xcodes, xscales, steps):
     """The dominant kernel alone: the W4A4 projection GEMV over the stack's
-    qkvz weights (1 activation row, N = 12288 + 64 rows, K = 2048), one launch
-    per layer instance, timed with CUDA events on the launching stream."""
+    qkvz+ba weights (1 activation row, N = 12288 + 64 rows, K = 2048), one
+    launch per layer instance, timed with CUDA events on the launching stream.
+    It is the CUDA-core kernel the c1 decode step runs (selected with tuning
+    knob 0 = 1 for this measurement, restored afterwards)."""
     import torch
+    pkg.lib().gdn_set_tuning(0, 1)
     import numpy as np
     from nvfp4_gated_deltanet_gb300 import synth
     w = synth.layer_weights(synth.FULL, 1)
@@ -180,7 +183,61 @@ def time_gemv(pkg, layers, xcodes, xscales, steps):
     with torch.cuda.graph(g):
         one_pass()
     ms = time_graph(g, steps, 3)
+    pkg.lib().gdn_set_tuning(0, 0)
     return ms / len(mats) * 1e3, len(mats)  # us per launch
+
+
+def time_batch(pkg, synth, B, hbm_peak, n_layers=2, steps=10):
+    """Large-batch decode: B sequences per step through n_layers layer instances
+    (each layer-step moves > 300 MB, far beyond L2)."""
+    w, layers, states, xd = make_stack_b(pkg, synth, n_layers, B)
+    g, _ = capture_stack(layers, states, xd, B)
+    ms = time_graph(g, steps, 3)
+    us = ms * 1e3 / n_layers
+    gbs = step_bytes(B) / (us * 1e-6) / 1e9
+    return {"us_per_layer_step": round(us, 2), "tokens_per_s": round(B / (us * 1e-6)), "hbm_gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / hbm_peak, 4)}
+
+
+def make_stack_b(pkg, synth, n_layers, B, device="cuda"):
+    import numpy as np
+    import torch
+    w = synth.layer_weights(synth.FULL, 1)
+    x = np.stack([synth.x_tokens(synth.FULL, synth.slot_seed(s), 1)[0] for s in range(B)])
+    xd = torch.from_numpy(x.view(np.int16)).to(device)
+    layers, states = [], []
+    for _ in range(n_layers):
+        L = pkg.layer_from_synth(w, max_batch=B)
+        conv = torch.empty(B, 3, synth.FULL.conv_channels, dtype=torch.int16, device=device)
+        ssm = torch.empty(B, synth.FULL.n_v_heads, 128, 128, dtype=torch.float32, device=device)
+        conv.copy_(torch.from_numpy(synth.conv_state(synth.FULL, 100).view(np.int16)).to(device).expand_as(conv))
+        ssm.copy_(torch.from_numpy(synth.ssm_state(synth.FULL, 100)).to(device).expand_as(ssm))
+        layers.append(L)
+        states.append((conv, ssm))
+    return w, layers, states, xd
+
+
+def time_prefill(pkg, synth, T, reps=3):
+    """Prefill of one T-token sequence from zero state (weights stay resident
+    in L2 within the call, as they would in a real prompt)."""
+    import numpy as np
+    import torch
+    w = synth.layer_weights(synth.FULL, 1)
+    L = pkg.layer_from_synth(w, max_batch=1, max_prefill_tokens=T)
+    x = torch.from_numpy(synth.x_tokens(synth.FULL, 7, T).view(np.int16)).cuda()
+    conv, ssm = L.new_states(1)
+    out = torch.empty(T, synth.FULL.hidden, dtype=torch.int16, device="cuda")
+    L.prefill(x, 0, True, conv, ssm, out=out)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        L.prefill(x, 0, True, conv, ssm, out=out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    return {"ms": round(ms, 3), "tokens_per_s": round(T / (ms * 1e-3))}
 
 
 def cpu_baseline_leg(seconds_budget=15.0):
@@ -317,6 +374,14 @@ def main():
             del gB
         extra["c1"] = {"us_per_layer_step": round(us_layer, 3), "hbm_gbs": round(gbs_step, 1),
                        "frac_of_peak": round(gbs_step / hbm_peak, 4)}
+        del layers, states
+        torch.cuda.empty_cache()
+        for B in (64, 128, 256):
+            extra[f"batch{B}"] = time_batch(pkg, synth, B, hbm_peak)
+            torch.cuda.empty_cache()
+        for T in (1024, 4096, 16384):
+            extra[f"prefill{T}"] = time_prefill(pkg, synth, T)
+            torch.cuda.empty_cache()
 
     cpu = None if (args.no_cpu or rank != 0) else cpu_baseline_leg()
     line = {
@@ -329,7 +394,7 @@ def main():
                                 f"({l2 / 1e6:.0f} MB)", "graph": "one CUDA graph per bucket over the stack",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs_step": round(gbs_step, 1), "hbm_frac_step": round(gbs_step / hbm_peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1> (W4A4 qkvz+ba projection, M=1)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1,1> (W4A4 qkvz+ba projection on CUDA cores, 1 row)",
                      "achieved": round(gemv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(gemv_gbs / hbm_peak, 4), "peak_kind": peak_kind, "traffic": None,
                      "us_per_launch": round(us_gemv, 3), "bytes_per_launch": GEMV_IN_BYTES},

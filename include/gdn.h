@@ -171,6 +171,18 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
                        uint16_t *out, uint16_t *conv_state, float *ssm_state, int num_slots,
                        void *stream);
 
+/* Process-wide tuning knobs (they change speed, never results beyond FP32
+ * summation order). knob 0: projection kernel of decode and prefill:
+ * 0 = automatic (more than 2 activation rows and a reduction length that is a
+ * multiple of 256: tcgen05 block-scaled MMA; else the CUDA-core kernel),
+ * 1 = CUDA-core kernel (also for nvfp4_gemm with M <= 16), 2 = tensor cores
+ * where the reduction length allows. knob 1 / knob 2: split-K of the in- /
+ * out-projection on tensor cores, 0 = automatic, or 1, 2, 4, 8 (reduced to
+ * the largest power of two that divides the 256-wide K tiles).
+ * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
+ * before launching work. */
+gdn_status gdn_set_tuning(int knob, int value);
+
 /* Synchronise `stream`, read the context's sticky device status word, clear it
  * if `clear`, and return it (GDN_OK when nothing was flagged). A CUDA error seen
  * while synchronising returns GDN_E_CUDA. */

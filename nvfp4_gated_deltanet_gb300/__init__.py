@@ -46,6 +46,7 @@ SIGNATURES = {
     "gdn_mix_step": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp]),
     "gdn_prefill": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _i, _vp]),
     "gdn_check": (_i, [_vp, _i, _vp]),
+    "gdn_set_tuning": (_i, [_i, _i]),
 }
 
 _lib = None

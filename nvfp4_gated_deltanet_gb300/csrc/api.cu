@@ -23,6 +23,9 @@ struct gdn_ctx {
   uint8_t *y_codes, *y_scales;          // [prow][Vd/2], [prow][Vd/16]
   float *qn, *kn, *v, *beta, *alpha, *o;  // prefill intermediates
   uint16_t *conv_tmp;                   // [K-1][C]
+  uint8_t *xq_codes, *xq_scales;        // [prow][H/2], [prow][H/16]: x as NVFP4 for the tensor-core GEMM
+  TcGemm tc_in, tc_out;                 // weight tensor maps of the two projections
+  bool tc_in_ok, tc_out_ok;             // K % 256 == 0: the tcgen05 path applies
   int32_t *status;
   std::vector<void *> allocs;
 };
@@ -35,6 +38,30 @@ gdn_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return GDN_OK;
   if (e == cudaErrorMemoryAllocation) return GDN_E_OOM;
   return GDN_E_CUDA;
+}
+
+// Process-wide tuning knobs (gdn_set_tuning).
+struct Tuning {
+  int decode_gemm = 0;  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
+  int split_in = 0;     // split-K of the in-projection on tensor cores (0 = automatic)
+  int split_out = 0;    // split-K of the out-projection
+};
+Tuning g_tune;
+
+// Automatic choice, measured on GB300 (decode stack, us per layer-step):
+// one row streams the weights faster through the CUDA-core GEMV (c1: 14.9 vs
+// 18.3); from two rows on the tensor cores win (c2: 26.1 on the GEMV, c4: 20.3
+// vs 36.2, c16: 34.8 vs 97.9).
+bool use_tensor_cores(int rows) {
+  if (g_tune.decode_gemm == 1) return false;
+  if (g_tune.decode_gemm == 2) return true;
+  return rows > 1;
+}
+// Split-K for few activation rows: spreads the K loop of the 97 (in) or 16
+// (out) weight tiles over 2 or 4 CTAs of a cluster (measured best at B 1..16).
+int split_for(int knob_value, int rows, int dflt) {
+  if (knob_value > 0) return knob_value;
+  return rows <= 64 ? dflt : 0;
 }
 
 template <typename T>
@@ -114,9 +141,109 @@ MixArgs mix_args(gdn_ctx *c) {
   return m;
 }
 
+// x (BF16 rows, padding rows masked by row_slot) -> the in-projection
+// (q|k|v|z|b|a, BF16, ldc = Nin) on tensor cores, or on the CUDA cores.
+cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t *row_slot, int num_slots,
+                        const LaunchCtx &lc, bool allow_tc) {
+  const gdn_config &c = ctx->cfg;
+  if (allow_tc && ctx->tc_in_ok && use_tensor_cores(rows)) {
+    cudaError_t e = launch_quantize(x, 0, rows, c.hidden, c.act_scale_in, ctx->xq_codes, ctx->xq_scales, ctx->status,
+                                    lc.stream, row_slot, num_slots, lc.pdl);
+    if (e != cudaSuccess) return e;
+    TcGemm t = ctx->tc_in;
+    t.b_codes = ctx->xq_codes;
+    t.b_scales = ctx->xq_scales;
+    t.args.Ma = ctx->Nin;
+    t.args.Nb = rows;
+    t.args.K = c.hidden;
+    t.args.c = ctx->proj;
+    t.args.ldc = ctx->Nin;
+    t.args.c_is_bf16 = 1;
+    t.args.ts_a0 = ctx->ts_qkvz;
+    t.args.ts_a1 = ctx->ts_ba;
+    t.args.a_split = ctx->Nqkvz;
+    t.args.ts_b = c.act_scale_in;
+    t.args.a_const = 1;
+    t.args.status = ctx->status;
+    t.split_k = split_for(g_tune.split_in, rows, 2);
+    return launch_tc_gemm(t, lc);
+  }
+  GemvArgs g{};
+  g.a_bf16 = x;
+  g.ts_a = c.act_scale_in;
+  g.row_slot = row_slot;
+  g.num_slots = num_slots;
+  g.w_codes = ctx->w_in_codes;
+  g.w_scales = ctx->w_in_scales;
+  g.ts_w0 = ctx->ts_qkvz;
+  g.ts_w1 = ctx->ts_ba;
+  g.n_split = ctx->Nqkvz;
+  g.c = ctx->proj;
+  g.c_is_bf16 = 1;
+  g.ldc = ctx->Nin;
+  g.N = ctx->Nin;
+  g.K = c.hidden;
+  g.status = ctx->status;
+  return run_gemv(g, lc, rows);
+}
+
+// y (NVFP4 in the context's workspace) -> out (BF16 [rows][H]).
+cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx &lc, bool allow_tc) {
+  const gdn_config &c = ctx->cfg;
+  if (allow_tc && ctx->tc_out_ok && use_tensor_cores(rows)) {
+    TcGemm t = ctx->tc_out;
+    t.b_codes = ctx->y_codes;
+    t.b_scales = ctx->y_scales;
+    t.args.Ma = c.hidden;
+    t.args.Nb = rows;
+    t.args.K = ctx->Vd;
+    t.args.c = out;
+    t.args.ldc = c.hidden;
+    t.args.c_is_bf16 = 1;
+    t.args.ts_a0 = t.args.ts_a1 = ctx->ts_wout;
+    t.args.a_split = c.hidden;
+    t.args.ts_b = c.act_scale_out;
+    t.args.a_const = 1;
+    t.args.status = ctx->status;
+    t.split_k = split_for(g_tune.split_out, rows, 4);
+    return launch_tc_gemm(t, lc);
+  }
+  GemvArgs o{};
+  o.a_codes = ctx->y_codes;
+  o.a_scales = ctx->y_scales;
+  o.ts_a = c.act_scale_out;
+  o.w_codes = ctx->w_out_codes;
+  o.w_scales = ctx->w_out_scales;
+  o.ts_w0 = o.ts_w1 = ctx->ts_wout;
+  o.n_split = c.hidden;
+  o.c = out;
+  o.c_is_bf16 = 1;
+  o.ldc = c.hidden;
+  o.N = c.hidden;
+  o.K = ctx->Vd;
+  o.status = ctx->status;
+  return run_gemv(o, lc, rows);
+}
+
 }  // namespace
 
 extern "C" {
+
+gdn_status gdn_set_tuning(int knob, int value) {
+  switch (knob) {
+    case 0:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      g_tune.decode_gemm = value;
+      return GDN_OK;
+    case 1:
+    case 2:
+      if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return GDN_E_RANGE;
+      (knob == 1 ? g_tune.split_in : g_tune.split_out) = value;
+      return GDN_OK;
+    default:
+      return GDN_E_RANGE;
+  }
+}
 
 const char *gdn_status_string(int s) {
   static const char *names[] = {"GDN_OK",          "GDN_E_NULL",     "GDN_E_SHAPE",   "GDN_E_ALIGN",
@@ -185,6 +312,8 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_scales, prow * Vd / 16);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->status, 1);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->conv_tmp, (c.conv_kernel - 1) * Cc);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_codes, prow * H / 2);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_scales, prow * H / 16);
   if (T > 0) {
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->qn, T * Hk * D);
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->kn, T * Hk * D);
@@ -222,6 +351,8 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
     delete ctx;
     return r;
   }
+  ctx->tc_in_ok = H % 256 == 0 && tc_make_weight_maps(ctx->tc_in, ctx->w_in_codes, ctx->w_in_scales, (int)Nin, (int)H);
+  ctx->tc_out_ok = Vd % 256 == 0 && tc_make_weight_maps(ctx->tc_out, ctx->w_out_codes, ctx->w_out_scales, (int)H, (int)Vd);
   *out = ctx;
   return GDN_OK;
 }
@@ -260,8 +391,26 @@ gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int 
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_status(e);
-  if ((size_t)16 * (K >> 6) * (4 * 2 * 16 + 16) > 200 * 1024) return GDN_E_SHAPE;
   LaunchCtx lc{static_cast<cudaStream_t>(stream), sms, false};  // B may come from a preceding kernel
+  if (K % 256 == 0 && !(g_tune.decode_gemm == 1 && M <= 16)) {
+    // tensor cores: B (N rows) is the MMA's A operand, A (M rows) its B operand
+    TcGemm t{};
+    if (!tc_make_weight_maps(t, B->codes, B->scales, N, K)) return GDN_E_CUDA;
+    t.b_codes = A->codes;
+    t.b_scales = A->scales;
+    t.args.Ma = N;
+    t.args.Nb = M;
+    t.args.K = K;
+    t.args.c = C;
+    t.args.ldc = N;
+    t.args.c_is_bf16 = c_is_bf16 ? 1 : 0;
+    t.args.ts_a0 = t.args.ts_a1 = B->tensor_scale;
+    t.args.a_split = N;
+    t.args.ts_b = A->tensor_scale;
+    t.args.a_const = 0;
+    return cuda_status(launch_tc_gemm(t, lc));
+  }
+  if ((size_t)16 * (K >> 6) * (4 * 2 * 16 + 16) > 200 * 1024) return GDN_E_SHAPE;
   GemvArgs g{};
   g.a_codes = A->codes;
   g.a_scales = A->scales;
@@ -286,24 +435,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   if (!aligned16(slot_ids)) return GDN_E_ALIGN;
   if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
   LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, true};
-  const int H = ctx->cfg.hidden;
-  GemvArgs g{};
-  g.a_bf16 = x;
-  g.ts_a = ctx->cfg.act_scale_in;
-  g.row_slot = slot_ids;
-  g.num_slots = num_slots;
-  g.w_codes = ctx->w_in_codes;
-  g.w_scales = ctx->w_in_scales;
-  g.ts_w0 = ctx->ts_qkvz;
-  g.ts_w1 = ctx->ts_ba;
-  g.n_split = ctx->Nqkvz;
-  g.c = ctx->proj;
-  g.c_is_bf16 = 1;
-  g.ldc = ctx->Nin;
-  g.N = ctx->Nin;
-  g.K = H;
-  g.status = ctx->status;
-  cudaError_t e = run_gemv(g, lc, B);
+  cudaError_t e = run_in_proj(ctx, x, B, slot_ids, num_slots, lc, true);
   if (e != cudaSuccess) return cuda_status(e);
   MixArgs m = mix_args(ctx);
   m.qkvz = ctx->proj;
@@ -320,21 +452,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   m.y_f32 = nullptr;
   e = launch_mix(m, lc);
   if (e != cudaSuccess) return cuda_status(e);
-  GemvArgs o{};
-  o.a_codes = ctx->y_codes;
-  o.a_scales = ctx->y_scales;
-  o.ts_a = ctx->cfg.act_scale_out;
-  o.w_codes = ctx->w_out_codes;
-  o.w_scales = ctx->w_out_scales;
-  o.ts_w0 = o.ts_w1 = ctx->ts_wout;
-  o.n_split = H;
-  o.c = out;
-  o.c_is_bf16 = 1;
-  o.ldc = H;
-  o.N = H;
-  o.K = ctx->Vd;
-  o.status = ctx->status;
-  return cuda_status(run_gemv(o, lc, B));
+  return cuda_status(run_out_proj(ctx, out, B, lc, true));
 }
 
 gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, const int32_t *slot_ids, int B,
@@ -370,7 +488,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LaunchCtx lc{s, ctx->num_sms, true};
   const gdn_config &c = ctx->cfg;
-  const int H = c.hidden, D = c.d_k;
+  const int D = c.d_k;
   uint16_t *cst = conv_state + (size_t)slot * (c.conv_kernel - 1) * ctx->C;
   float *S = ssm_state + (size_t)slot * c.n_v_heads * D * D;
   cudaError_t e = cudaSuccess;
@@ -379,21 +497,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
     if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, (size_t)c.n_v_heads * D * D * 4, s);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  GemvArgs g{};
-  g.a_bf16 = x;
-  g.ts_a = c.act_scale_in;
-  g.w_codes = ctx->w_in_codes;
-  g.w_scales = ctx->w_in_scales;
-  g.ts_w0 = ctx->ts_qkvz;
-  g.ts_w1 = ctx->ts_ba;
-  g.n_split = ctx->Nqkvz;
-  g.c = ctx->proj;
-  g.c_is_bf16 = 1;
-  g.ldc = ctx->Nin;
-  g.N = ctx->Nin;
-  g.K = H;
-  g.status = ctx->status;
-  e = run_gemv(g, lc, T);
+  e = run_in_proj(ctx, x, T, nullptr, 0, lc, true);
   if (e != cudaSuccess) return cuda_status(e);
   PrefillArgs p{};
   p.proj = ctx->proj;
@@ -424,21 +528,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.status = ctx->status;
   e = launch_prefill_mix(p, ctx->conv_tmp, lc);
   if (e != cudaSuccess) return cuda_status(e);
-  GemvArgs o{};
-  o.a_codes = ctx->y_codes;
-  o.a_scales = ctx->y_scales;
-  o.ts_a = c.act_scale_out;
-  o.w_codes = ctx->w_out_codes;
-  o.w_scales = ctx->w_out_scales;
-  o.ts_w0 = o.ts_w1 = ctx->ts_wout;
-  o.n_split = H;
-  o.c = out;
-  o.c_is_bf16 = 1;
-  o.ldc = H;
-  o.N = H;
-  o.K = ctx->Vd;
-  o.status = ctx->status;
-  return cuda_status(run_gemv(o, lc, T));
+  return cuda_status(run_out_proj(ctx, out, T, lc, true));
 }
 
 gdn_status gdn_check(gdn_ctx *ctx, int clear, void *stream) {

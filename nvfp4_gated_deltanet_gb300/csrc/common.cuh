@@ -1,6 +1,7 @@
 // Shared device helpers of the GDN kernels (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -230,8 +231,11 @@ struct LaunchCtx {
              // constants -- weights -- before griddepcontrol.wait)
 };
 
+// row_slot (optional): row r is quantised as zeros when row_slot[r] is not a
+// valid slot (a padding row of a decode batch).
 cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, float ts, uint8_t *codes,
-                            uint8_t *scales, int32_t *status, cudaStream_t stream);
+                            uint8_t *scales, int32_t *status, cudaStream_t stream, const int32_t *row_slot = nullptr,
+                            int num_slots = 0, bool pdl = false);
 
 // C[M][N] (ldc) = A_hat[M][K] * W_hat[N][K]^T. A is BF16 rows (quantised inside
 // with ts_a; a_rows_valid may mark rows to treat as zero) or NVFP4. Rows of W
@@ -291,6 +295,29 @@ struct PrefillArgs {
   uint8_t *y_scales;     // [T][Hv*D/16]
   int32_t *status;
 };
+// Block-scaled W4A4 GEMM on tcgen05: D[m][n] = W_hat[m][:] . X_hat[n][:],
+// stored C[n][m] (ldc). W = weights (A operand, M = 128 rows per tile), X =
+// activations (B operand). K % 256 == 0; row-major codes and scales.
+struct TcArgs {
+  int Ma, Nb, K;
+  void *c;
+  int ldc;
+  int c_is_bf16;
+  float ts_a0, ts_a1;  // weight tensor scale of rows < a_split, and of the rest
+  int a_split;
+  float ts_b;
+  int a_const;         // weights written by no preceding kernel: stream them before griddepcontrol.wait
+  int32_t *status;
+};
+struct TcGemm {
+  CUtensorMap mapA, mapSA;  // weights: codes [Ma][K/2] (128-byte swizzle), scales [Ma][K/16]
+  const uint8_t *b_codes, *b_scales;
+  TcArgs args;
+  int split_k;  // 0 = automatic
+};
+bool tc_make_weight_maps(TcGemm &g, const uint8_t *w_codes, const uint8_t *w_scales, int rows, int K);
+cudaError_t launch_tc_gemm(const TcGemm &g, const LaunchCtx &lc);
+
 cudaError_t launch_prefill_mix(const PrefillArgs &a, uint16_t *tmp, const LaunchCtx &lc);
 
 }  // namespace gdn

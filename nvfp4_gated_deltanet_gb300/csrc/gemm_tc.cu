@@ -1,0 +1,415 @@
+// Block-scaled W4A4 GEMM on the 5th-generation tensor cores:
+// tcgen05.mma .kind::mxf4nvf4 .scale_vec::4X (E2M1 operands, one UE4M3 scale
+// per 16 elements), FP32 accumulators in tensor memory.
+//
+//   D[m][n] = sum_k W_hat[m][k] * X_hat[n][k],   stored as C[n][m]
+//
+// W (the weights) is the MMA's A operand: 128 rows per CTA tile. X (the
+// activations: decode rows or prompt tokens) is the B operand: BN rows. Both
+// are K-major NVFP4 with row-major codes [rows][K/2] and scales [rows][K/16].
+//
+// Per CTA (6 warps):
+//   warp 0      TMA producer: code tiles (128 B x rows, 128-byte swizzle) and
+//               the row-major scale rows of this K tile, into a ring of S stages
+//   warp 1      tensor-memory allocation, then one thread issues tcgen05.cp
+//               (scales -> TMEM) and tcgen05.mma, committing each stage back
+//               to the producer
+//   warps 2..5  rearrange each stage's scale rows into the 32x16-byte layout
+//               tcgen05.cp reads (row r: byte (r%32)*16 + (r/32)*4 + k-block),
+//               then the epilogue: TMEM -> registers -> scaled BF16/FP32 stores
+// Split-K over a thread-block cluster of KS CTAs: ranks != 0 push their FP32
+// partial tile into rank 0's shared memory before one cluster barrier; rank 0
+// adds them in rank order (deterministic, no atomics).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kATile = 128 * 128;  // 128 rows x 128 bytes (256 E2M1 values)
+constexpr int kSFAtom = 512;       // scales of 128 rows x one K=64 step
+constexpr int kTmemCols = 256;     // accumulator at column 0, scales from column 128
+
+// ---------------------------------------------------------------- PTX wrappers
+GDN_DEV void tmem_alloc(uint32_t *holder, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)), "r"(ncols)
+               : "memory");
+}
+GDN_DEV void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory"); }
+GDN_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+GDN_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+GDN_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+GDN_DEV void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+GDN_DEV void tc_cp_scales(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+GDN_DEV void tc_mma_nvf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+GDN_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+GDN_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+GDN_DEV void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+GDN_DEV void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+GDN_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 bytes,
+// 8-row atoms 1024 bytes apart (stride byte offset); leading offset unused.
+GDN_DEV uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // descriptor version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+// 32 rows x 16 bytes, no swizzle: 8-row core matrices 128 bytes apart.
+GDN_DEV uint64_t desc_scales(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 16;
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+// Instruction descriptor: E2M1 x E2M1, K-major A and B, UE4M3 scales,
+// N = BN, M = 128, dense.
+template <int BN>
+GDN_DEV uint32_t idesc_nvf4() {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | (0u << 23) | ((uint32_t)(128 >> 4) << 24);
+}
+
+template <int BN>
+struct Layout {
+  static constexpr int kB = BN * 128;                 // B codes
+  static constexpr int kSfaRows = 128 * 16;           // row-major scale rows of this K tile
+  static constexpr int kSfbRows = (BN * 16 + 127) / 128 * 128;
+  static constexpr int kAtoms = 4 * kSFAtom;          // 4 K=64 steps
+  static constexpr int kStage = (kATile + kB + kSfaRows + kSfbRows + 2 * kAtoms + 1023) / 1024 * 1024;
+  static_assert(kATile % 1024 == 0 && kB % 1024 == 0, "swizzled tiles stay 1024-byte aligned");
+};
+
+template <int BN, int KS, int S>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, TcArgs a) {
+  using L = Layout<BN>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  unsigned char *stage0 = sm;
+  float *part = reinterpret_cast<float *>(sm + (size_t)S * L::kStage);
+  uint64_t *full = reinterpret_cast<uint64_t *>(part + (KS > 1 ? (KS - 1) * 128 * BN : 0));
+  uint64_t *sfready = full + S;
+  uint64_t *empty = sfready + S;
+  uint64_t *accum = empty + S;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(accum + 1);
+  auto stA = [&](int s) { return stage0 + (size_t)s * L::kStage; };
+  auto stB = [&](int s) { return stA(s) + kATile; };
+  auto stSA = [&](int s) { return stB(s) + L::kB; };
+  auto stSB = [&](int s) { return stSA(s) + L::kSfaRows; };
+  auto stAtA = [&](int s) { return stSB(s) + L::kSfbRows; };
+  auto stAtB = [&](int s) { return stAtA(s) + L::kAtoms; };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x / KS, ks = blockIdx.x % KS;
+  const int nt = blockIdx.y;
+  const int nkt = (a.K >> 8) / KS;
+  const int kt0 = ks * nkt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(sfready + s, 128);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(accum, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint32_t bytes = kATile + L::kB + 128 * 16 + BN * 16;
+      const int pre = a.a_const ? min(S, nkt) : 0;
+      for (int i = 0; i < pre; ++i) {  // weights do not depend on the preceding kernel
+        mbar_arrive_expect_tx(full + i, bytes);
+        tma_load_2d(stA(i), &tmA, (kt0 + i) * 128, mt * 128, full + i);
+        tma_load_2d(stSA(i), &tmSA, (kt0 + i) * 16, mt * 128, full + i);
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      for (int i = 0; i < pre; ++i) {
+        tma_load_2d(stB(i), &tmB, (kt0 + i) * 128, nt * BN, full + i);
+        tma_load_2d(stSB(i), &tmSB, (kt0 + i) * 16, nt * BN, full + i);
+      }
+      for (int i = pre; i < nkt; ++i) {
+        const int s = i % S, u = i / S;
+        if (u > 0 && !mbar_wait(empty + s, (uint32_t)((u - 1) & 1))) { ok = false; break; }
+        mbar_arrive_expect_tx(full + s, bytes);
+        tma_load_2d(stA(s), &tmA, (kt0 + i) * 128, mt * 128, full + s);
+        tma_load_2d(stSA(s), &tmSA, (kt0 + i) * 16, mt * 128, full + s);
+        tma_load_2d(stB(s), &tmB, (kt0 + i) * 128, nt * BN, full + s);
+        tma_load_2d(stSB(s), &tmSB, (kt0 + i) * 16, nt * BN, full + s);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_nvf4<BN>();
+      for (int i = 0; i < nkt; ++i) {
+        const int s = i % S, u = i / S;
+        if (!mbar_wait(full + s, (uint32_t)(u & 1)) || !mbar_wait(sfready + s, (uint32_t)(u & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sfa = tmem + 128 + 32 * s, sfb = sfa + 16;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tc_cp_scales(sfa + 4 * j, desc_scales(smem_u32(stAtA(s)) + j * kSFAtom));
+          tc_cp_scales(sfb + 4 * j, desc_scales(smem_u32(stAtB(s)) + j * kSFAtom));
+        }
+        const uint64_t ad = desc_sw128(smem_u32(stA(s))), bd = desc_sw128(smem_u32(stB(s)));
+#pragma unroll
+        for (int j = 0; j < 4; ++j)  // K = 64 per MMA: 32 bytes further along the swizzled rows
+          tc_mma_nvf4(tmem, ad + 2 * j, bd + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j, (i | j) != 0);
+        tc_commit(empty + s);
+      }
+      tc_commit(accum);
+    }
+  } else {
+    // ------------------------------------------------ scale rearrangement
+    const int t = threadIdx.x - 64;  // 0..127
+    for (int i = 0; i < nkt; ++i) {
+      const int s = i % S, u = i / S;
+      if (!mbar_wait(full + s, (uint32_t)(u & 1))) { ok = false; break; }
+      const uint4 va = *reinterpret_cast<const uint4 *>(stSA(s) + t * 16);
+      uint32_t *atA = reinterpret_cast<uint32_t *>(stAtA(s) + (t & 31) * 16 + (t >> 5) * 4);
+      atA[0 * kSFAtom / 4] = va.x;
+      atA[1 * kSFAtom / 4] = va.y;
+      atA[2 * kSFAtom / 4] = va.z;
+      atA[3 * kSFAtom / 4] = va.w;
+      if (t < BN) {
+        const uint4 vb = *reinterpret_cast<const uint4 *>(stSB(s) + t * 16);
+        uint32_t *atB = reinterpret_cast<uint32_t *>(stAtB(s) + (t & 31) * 16 + (t >> 5) * 4);
+        atB[0 * kSFAtom / 4] = vb.x;
+        atB[1 * kSFAtom / 4] = vb.y;
+        atB[2 * kSFAtom / 4] = vb.z;
+        atB[3 * kSFAtom / 4] = vb.w;
+      }
+      fence_async_shared();  // generic-proxy writes -> visible to tcgen05.cp
+      mbar_arrive(sfready + s);
+    }
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    float acc[BN];
+    if (ok && mbar_wait(accum, 0)) {
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) acc[c0 + c] = __uint_as_float(r[c]);
+      }
+    } else {
+      ok = false;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) acc[c] = 0.0f;
+    }
+    if (KS > 1 && ks != 0) {
+      float *dst = cg::this_cluster().map_shared_rank(part, 0) + (size_t)(ks - 1) * 128 * BN;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) dst[c * 128 + row] = acc[c];
+    }
+    if (KS > 1) cg::this_cluster().sync();  // partials have landed in rank 0
+    if (KS == 1 || ks == 0) {
+      for (int p = 0; p < KS - 1; ++p)
+#pragma unroll
+        for (int c = 0; c < BN; ++c) acc[c] += part[((size_t)p * BN + c) * 128 + row];
+      const int m = mt * 128 + row;
+      if (m < a.Ma) {
+        const float ts = (m < a.a_split ? a.ts_a0 : a.ts_a1) * a.ts_b;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int n = nt * BN + c;
+          if (n < a.Nb) {
+            const float y = acc[c] * ts;
+            if (a.c_is_bf16)
+              static_cast<uint16_t *>(a.c)[(size_t)n * a.ldc + m] = f32_to_bf16_bits(y);
+            else
+              static_cast<float *>(a.c)[(size_t)n * a.ldc + m] = y;
+          }
+        }
+      }
+    }
+  }
+  if (warp < 2 && KS > 1) cg::this_cluster().sync();  // the same cluster barrier, producer/MMA warps
+  if (!ok && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows][row_bytes] (row stride = row_bytes), box [box_rows][box_bytes].
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t row_bytes, uint32_t box_rows,
+              uint32_t box_bytes, bool swizzle128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_bytes, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int KS, int S>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)S * Layout<BN>::kStage + (KS > 1 ? (size_t)(KS - 1) * 128 * BN * 4 : 0) + (3 * S + 1) * 8 + 16;
+}
+
+template <int BN, int KS, int S>
+cudaError_t launch_t(const TcGemm &g, const LaunchCtx &lc) {
+  CUtensorMap mB, mSB;
+  if (!make_map(&mB, g.b_codes, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 2, BN, 128, true) ||
+      !make_map(&mSB, g.b_scales, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 16, BN, 16, false))
+    return cudaErrorInvalidValue;
+  size_t smem = smem_bytes<BN, KS, S>();
+  if (smem < 80 * 1024) smem = 80 * 1024;  // at most two CTAs (2 x 256 TMEM columns) per SM
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_nvf4_kernel<BN, KS, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(((g.args.Ma + 127) / 128) * KS, (g.args.Nb + BN - 1) / BN, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  ++na;
+  if (KS > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = KS;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemm_nvf4_kernel<BN, KS, S>, g.mapA, mB, g.mapSA, mSB, g.args);
+}
+
+constexpr size_t kSmemCap = 227 * 1024;
+
+template <int BN>
+cudaError_t launch_bn(const TcGemm &g, int ks, const LaunchCtx &lc) {
+  // the largest split <= ks whose shared memory fits
+  if (ks >= 8 && smem_bytes<BN, 8, 4>() <= kSmemCap) return launch_t<BN, 8, 4>(g, lc);
+  if (ks >= 4 && smem_bytes<BN, 4, 4>() <= kSmemCap) return launch_t<BN, 4, 4>(g, lc);
+  if (ks >= 2 && smem_bytes<BN, 2, 4>() <= kSmemCap) return launch_t<BN, 2, 4>(g, lc);
+  return launch_t<BN, 1, 4>(g, lc);
+}
+
+}  // namespace
+
+bool tc_make_weight_maps(TcGemm &g, const uint8_t *w_codes, const uint8_t *w_scales, int rows, int K) {
+  return make_map(&g.mapA, w_codes, (uint64_t)rows, (uint64_t)K / 2, 128, 128, true) &&
+         make_map(&g.mapSA, w_scales, (uint64_t)rows, (uint64_t)K / 16, 128, 16, false);
+}
+
+// Split-K so that the grid covers the GPU: tiles x KS >= SMs when K allows.
+int tc_pick_split(int m_tiles, int n_tiles, int K, int num_sms) {
+  const int kt = K / 256;
+  int ks = 1;
+  while (ks < 8 && m_tiles * n_tiles * ks * 2 <= num_sms && kt % (ks * 2) == 0) ks *= 2;
+  return ks;
+}
+
+cudaError_t launch_tc_gemm(const TcGemm &g, const LaunchCtx &lc) {
+  const TcArgs &a = g.args;
+  if (a.Ma <= 0 || a.Nb <= 0) return cudaSuccess;
+  if (a.K % 256) return cudaErrorInvalidValue;
+  const int m_tiles = (a.Ma + 127) / 128;
+  int bn = a.Nb <= 16 ? 16 : a.Nb <= 32 ? 32 : a.Nb <= 64 ? 64 : 128;
+  const int n_tiles = (a.Nb + bn - 1) / bn;
+  int ks = g.split_k > 0 ? g.split_k : tc_pick_split(m_tiles, n_tiles, a.K, lc.num_sms);
+  while (ks > 1 && (a.K / 256) % ks) ks >>= 1;  // the split must divide the K tiles
+  switch (bn) {
+    case 16: return launch_bn<16>(g, ks, lc);
+    case 32: return launch_bn<32>(g, ks, lc);
+    case 64: return launch_bn<64>(g, ks, lc);
+    default: return launch_bn<128>(g, ks, lc);
+  }
+}
+
+}  // namespace gdn

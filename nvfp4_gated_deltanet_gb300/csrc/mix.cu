@@ -30,8 +30,6 @@ namespace {
 
 constexpr int kRPW = 8;  // state rows per warp
 
-GDN_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
-GDN_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 
 template <int D, int NS>
 __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
@@ -45,7 +43,7 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
 
   __shared__ float s_q[D], s_k[D], s_v[R], s_o[R], s_y[R];
   __shared__ uint16_t s_qk_new[3][2 * D];  // new conv state of the q/k channels (K_conv <= 4)
-  __shared__ float s_gsum[R / 16];         // sums of o^2 over 16-row groups, read by the peers
+  __shared__ float s_gsum[D / 16];         // sums of o^2 over the head's 16-row groups
 
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -57,7 +55,11 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   const int vd = a.Hv * D;
   const int C = a.C, Kc = a.Kc;
 
-  // ---- constants first (written by no kernel): conv taps, gate and norm params
+  // ---- loads that do not depend on the preceding kernel come first. With
+  // programmatic dependent launch this kernel starts once the projection
+  // kernel has passed its own griddepcontrol.wait, so everything earlier in
+  // the stream (slot ids, the previous step's state writes) is complete;
+  // only the projections themselves may still be in flight.
   int ch[CPT];
   float cw[CPT][4];
 #pragma unroll
@@ -73,11 +75,52 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   }
   const float A_log = a.A_log[h], dt_bias = a.dt_bias[h];
   const float nw = tid < R ? a.norm_w[row0 + tid] : 0.0f;
-
-  // ---- then what the preceding kernel produced: projections (and slot ids)
-  pdl_wait();
   const int slot = a.slot_ids[b];
+  bool live = slot >= 0 && slot < a.num_slots;
+  bool bad = slot < -1 || slot >= a.num_slots;
+  if (live) {
+    for (int j = 0; j < a.B; ++j)
+      if (j != b && a.slot_ids[j] == slot) { bad = true; live = false; }
+  }
+  // state: conv taps and this warp's rows of S
+  uint16_t *cst = a.conv_state + (size_t)(live ? slot : 0) * (Kc - 1) * C;
+  uint16_t tap[CPT][3];
+  const int lr0 = warp * kRPW;
+  float *S = a.ssm_state + (((size_t)(live ? slot : 0) * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
+  float st[kRPW][EPL];
+  if (live) {
+#pragma unroll
+    for (int c = 0; c < CPT; ++c)
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+        tap[c][j] = (tid + c * THREADS < NCH && j < Kc - 1) ? cst[(size_t)j * C + ch[c]] : uint16_t(0);
+#pragma unroll
+    for (int j = 0; j < kRPW; ++j) {
+      if (EPL == 4) {
+        float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
+        st[j][0] = t4.x; st[j][1 % EPL] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
+      } else if (EPL == 2) {
+        float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
+        st[j][0] = t2.x; st[j][1 % EPL] = t2.y;
+      } else {
+        st[j][0] = S[(size_t)j * D];
+      }
+    }
+  }
+
+  // ---- the projections come from the preceding kernel
+  pdl_wait();
+  pdl_launch_dependents();
   const uint16_t *xin = a.qkvz + (size_t)b * a.ld_qkvz;
+  if (bad && tid == 0 && blockIdx.x == 0) flag_status(a.status, GDN_E_RANGE);
+  if (!live) {  // padding: zero y for this slice, touch no state (whole cluster agrees)
+    for (int i = tid; i < R; i += blockDim.x) {
+      if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = 0.0f;
+      if (a.y_codes && (i & 1) == 0) a.y_codes[((size_t)b * vd + h * D + row0 + i) >> 1] = 0;
+      if (a.y_scales && (i & 15) == 0) a.y_scales[((size_t)b * vd + h * D + row0 + i) >> 4] = 0;
+    }
+    return;
+  }
   uint16_t xn[CPT];
 #pragma unroll
   for (int c = 0; c < CPT; ++c) xn[c] = (tid + c * THREADS < NCH) ? xin[ch[c]] : uint16_t(0);
@@ -86,50 +129,7 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   const float b_raw = bf16_bits_to_f32(bain[h]);
   const float a_raw = bf16_bits_to_f32(bain[a.Hv + h]);
 
-  // ---- which slot, and is it valid (range, no repeats)
-  bool live = slot >= 0 && slot < a.num_slots;
-  bool bad = slot < -1 || slot >= a.num_slots;
-  if (live) {
-    for (int j = 0; j < a.B; ++j)
-      if (j != b && a.slot_ids[j] == slot) { bad = true; live = false; }
-  }
-  if (bad && tid == 0 && blockIdx.x == 0) flag_status(a.status, GDN_E_RANGE);
-  if (!live) {  // padding: zero y for this slice, touch no state (whole cluster agrees)
-    pdl_launch_dependents();
-    for (int i = tid; i < R; i += blockDim.x) {
-      if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = 0.0f;
-      if (a.y_codes && (i & 1) == 0) a.y_codes[((size_t)b * vd + h * D + row0 + i) >> 1] = 0;
-      if (a.y_scales && (i & 15) == 0) a.y_scales[((size_t)b * vd + h * D + row0 + i) >> 4] = 0;
-    }
-    return;
-  }
-
-  // ---- state loads, all issued before any use: conv taps and this warp's rows of S
-  uint16_t *cst = a.conv_state + (size_t)slot * (Kc - 1) * C;
-  uint16_t tap[CPT][3];
-#pragma unroll
-  for (int c = 0; c < CPT; ++c)
-#pragma unroll
-    for (int j = 0; j < 3; ++j)
-      tap[c][j] = (tid + c * THREADS < NCH && j < Kc - 1) ? cst[(size_t)j * C + ch[c]] : uint16_t(0);
-  const int lr0 = warp * kRPW;
-  float *S = a.ssm_state + (((size_t)slot * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
-  float st[kRPW][EPL];
-#pragma unroll
-  for (int j = 0; j < kRPW; ++j) {
-    if (EPL == 4) {
-      float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
-      st[j][0] = t4.x; st[j][1 % EPL] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
-    } else if (EPL == 2) {
-      float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
-      st[j][0] = t2.x; st[j][1 % EPL] = t2.y;
-    } else {
-      st[j][0] = S[(size_t)j * D];
-    }
-  }
-
   // ---- conv + SiLU for q, k (key head kh, all D) and v (this slice)
-  const bool qk_writer = cluster.block_rank() == 0;
 #pragma unroll
   for (int c = 0; c < CPT; ++c) {
     const int t = tid + c * THREADS;
@@ -157,7 +157,6 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
     }
   }
   __syncthreads();
-  cluster_arrive();  // this CTA has read the shared q/k conv state
 
   // ---- per-warp: normalised q, k in registers; k.q; gates
   float kr[EPL], qr[EPL];
@@ -225,35 +224,35 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
     }
   }
 
-  // every CTA of the cluster has read the q/k conv state: rank 0 writes it
-  cluster_wait();
-  if (qk_writer) {
+  __syncthreads();  // s_o complete
+
+  // ---- sum of o^2 over the head in one fixed order whatever NS is: 16-row
+  // group sums (rows in order), then the D/16 group sums in order. Every slice
+  // pushes its group sums into the shared memory of all slices of the head
+  // (remote stores before the one cluster barrier), so after the barrier each
+  // CTA reads only its own shared memory and nobody reads a peer that may have
+  // exited.
+  if (tid < R / 16) {
+    float p = 0.0f;
+    for (int i = 0; i < 16; ++i) p = fmaf(s_o[tid * 16 + i], s_o[tid * 16 + i], p);
+    if (NS > 1) {
+      const int gbase = (h % G) * NS;
+      for (int s2 = 0; s2 < NS; ++s2) *cluster.map_shared_rank(&s_gsum[split * (R / 16) + tid], gbase + s2) = p;
+    } else {
+      s_gsum[tid] = p;
+    }
+  }
+  // One cluster barrier: every slice's group sums have landed, and every CTA
+  // of the key head has read the shared q/k conv state (its reads came first).
+  if (G * NS > 1) cluster.sync(); else __syncthreads();
+  if (cluster.block_rank() == 0) {  // the q/k conv state of this key head
     for (int t = tid; t < 2 * D; t += blockDim.x) {
       const int q = t < D ? kh * D + t : a.Hk * D + kh * D + (t - D);
       for (int j = 0; j < Kc - 1; ++j) cst[(size_t)j * C + q] = s_qk_new[j][t];
     }
   }
-  __syncthreads();  // s_o complete
-  pdl_launch_dependents();
-
-  // ---- sum of o^2 over the head in one fixed order whatever NS is: 16-row group
-  // sums (rows in order), then the D/16 group sums in order, read from the
-  // slice that owns each group through distributed shared memory
-  if (tid < R / 16) {
-    float p = 0.0f;
-    for (int i = 0; i < 16; ++i) p = fmaf(s_o[tid * 16 + i], s_o[tid * 16 + i], p);
-    s_gsum[tid] = p;
-  }
   float sumsq = 0.0f;
-  if (NS > 1) {
-    cluster.sync();  // every slice's group sums are written
-    const int gbase = (h % G) * NS;
-    for (int gi = 0; gi < D / 16; ++gi)
-      sumsq += *cluster.map_shared_rank(&s_gsum[gi % (R / 16)], gbase + gi / (R / 16));
-  } else {
-    __syncthreads();
-    for (int gi = 0; gi < D / 16; ++gi) sumsq += s_gsum[gi];
-  }
+  for (int gi = 0; gi < D / 16; ++gi) sumsq += s_gsum[gi];
   const float rstd = 1.0f / sqrtf(sumsq / (float)D + a.rms_eps);
 
   // ---- gated RMSNorm -> y (FP32), then NVFP4 blocks of 16 rows
@@ -273,7 +272,6 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
     *reinterpret_cast<uint2 *>(a.y_codes + (e0 >> 1)) = make_uint2(lo, hi);
     a.y_scales[e0 >> 4] = uint8_t(s);
   }
-  if (NS > 1) cluster.sync();  // peers may still read this CTA's s_gsum
 }
 
 template <int D, int NS>

@@ -8,7 +8,9 @@ template <bool F32>
 __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ x, int rows, int cols, float ts,
                                                        uint8_t *__restrict__ codes,
                                                        uint8_t *__restrict__ scales,
-                                                       int32_t *status) {
+                                                       int32_t *status, const int32_t *row_slot, int num_slots) {
+  pdl_wait();  // x may come from the preceding kernel
+  pdl_launch_dependents();
   const int nb = cols >> 4;
   const long long total = (long long)rows * nb;
   const float inv6ts = inv6ts_of(ts);
@@ -16,7 +18,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
        blk += (long long)gridDim.x * blockDim.x) {
     const long long r = blk / nb, b = blk % nb;
     float v[16];
-    if (F32) {
+    const bool live = !row_slot || (row_slot[r] >= 0 && row_slot[r] < num_slots);
+    if (!live) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    } else if (F32) {
       const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(x) + r * cols + b * 16);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -44,16 +50,24 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
 }
 
 cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, float ts, uint8_t *codes,
-                            uint8_t *scales, int32_t *status, cudaStream_t stream) {
+                            uint8_t *scales, int32_t *status, cudaStream_t stream, const int32_t *row_slot,
+                            int num_slots, bool pdl) {
   const long long total = (long long)rows * (cols / 16);
   if (total == 0) return cudaSuccess;
   long long blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (x_is_f32)
-    quantize_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(x, rows, cols, ts, codes, scales, status);
-  else
-    quantize_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(x, rows, cols, ts, codes, scales, status);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<true>, x, rows, cols, ts, codes, scales, status, row_slot, num_slots);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<false>, x, rows, cols, ts, codes, scales, status, row_slot, num_slots);
 }
 
 }  // namespace gdn

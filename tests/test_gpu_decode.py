@@ -119,16 +119,30 @@ def test_nonfinite_input_is_flagged(api):
     assert L.check() == 0
 
 
-def test_batch_rows_equal_single_rows(api):
-    """B rows in one call equal B single-row calls (bitwise: no cross-row arithmetic)."""
+@pytest.mark.parametrize("path", [1, 2, 0])
+def test_batch_rows_equal_single_rows(api, path):
+    """B rows in one call equal B single-row calls: bitwise when both run the
+    same projection kernel (knob 0 = 1: CUDA cores, 2: tensor cores; there is
+    no cross-row arithmetic and every reduction has a fixed order), and within
+    the BF16 tolerance when the automatic choice runs B = 1 and B = 5 on
+    different kernels."""
     shape = synth.FULL
     L = _layer(api, "FULL", 1)
-    slots = [0, 1, 2, 3, 4]
-    x, conv0, ssm0 = slot_inputs(shape, slots, 1)
-    cb, sb = to_dev(conv0), to_dev(ssm0)
-    ob = to_host(L.decode_step(to_dev(x[0]), torch.arange(5, dtype=torch.int32, device="cuda"), cb, sb))
-    for i in slots:
-        c1, s1 = to_dev(conv0), to_dev(ssm0)
-        o1 = to_host(L.decode_step(to_dev(x[0][i:i + 1]), torch.tensor([i], dtype=torch.int32, device="cuda"), c1, s1))
-        np.testing.assert_array_equal(o1[0], ob[i])
-        np.testing.assert_array_equal(to_host(s1)[i], to_host(sb)[i])
+    api.lib().gdn_set_tuning(0, path)
+    try:
+        slots = [0, 1, 2, 3, 4]
+        x, conv0, ssm0 = slot_inputs(shape, slots, 1)
+        cb, sb = to_dev(conv0), to_dev(ssm0)
+        ob = to_host(L.decode_step(to_dev(x[0]), torch.arange(5, dtype=torch.int32, device="cuda"), cb, sb))
+        for i in slots:
+            c1, s1 = to_dev(conv0), to_dev(ssm0)
+            o1 = to_host(L.decode_step(to_dev(x[0][i:i + 1]), torch.tensor([i], dtype=torch.int32, device="cuda"),
+                                       c1, s1))
+            if path:
+                np.testing.assert_array_equal(o1[0], ob[i])
+                np.testing.assert_array_equal(to_host(s1)[i], to_host(sb)[i])
+            else:
+                assert rel_l2(_bf16(o1[0]), _bf16(ob[i])) <= 4e-3
+                assert rel_l2(to_host(s1)[i], to_host(sb)[i]) <= 1e-5
+    finally:
+        api.lib().gdn_set_tuning(0, 0)

@@ -73,7 +73,11 @@ def test_quantize_nonfinite_flags_status(g):
     assert (to_host(codes)[1, :8] == 0).all()
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 384, 256), (5, 100, 128), (16, 2048, 4096), (33, 64, 64), (2, 12352, 2048)])
+# K % 256 == 0 runs on the tcgen05 block-scaled kernel (N-tile 16/32/64/128, split-K
+# clusters, ragged M and N); other K on the CUDA-core kernel.
+@pytest.mark.parametrize("M,N,K", [(1, 384, 256), (5, 100, 128), (16, 2048, 4096), (33, 64, 64), (2, 12352, 2048),
+                                   (128, 256, 256), (200, 384, 512), (64, 1024, 2048), (40, 300, 256),
+                                   (256, 12352, 2048), (3, 2048, 4096)])
 def test_gemm_fp32_matches_exact_product(g, M, N, K):
     from oracle import nvfp4
     a = synth.nvfp4_random(M, K, seed=M + 1000, prefix="mat", tensor_scale=2.0 ** -8)
