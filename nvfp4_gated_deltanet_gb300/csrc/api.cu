@@ -21,7 +21,8 @@ struct gdn_ctx {
   float *A_log, *dt_bias, *norm_w;
   uint16_t *proj;                       // [prow][Nin] BF16 projection outputs
   uint8_t *y_codes, *y_scales;          // [prow][Vd/2], [prow][Vd/16]
-  float *qn, *kn, *v, *beta, *alpha, *o;  // prefill intermediates
+  float *qn, *kn, *v, *beta, *gl, *o;     // prefill intermediates (head-major, chunk-padded)
+  float *W, *Ut, *Am, *Gam;               // per (value head, 64-token chunk) products
   uint16_t *conv_tmp;                   // [K-1][C]
   uint8_t *xq_codes, *xq_scales;        // [prow][H/2], [prow][H/16]: x as NVFP4 for the tensor-core GEMM
   TcGemm tc_in, tc_out;                 // weight tensor maps of the two projections
@@ -315,12 +316,17 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_codes, prow * H / 2);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_scales, prow * H / 16);
   if (T > 0) {
-    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->qn, T * Hk * D);
-    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->kn, T * Hk * D);
-    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->v, T * Hv * D);
+    const long long Tp = (T + 63) / 64 * 64;
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->qn, Tp * Hk * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->kn, Tp * Hk * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->v, Tp * Hv * D);
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->o, T * Hv * D);
-    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->beta, T * Hv);
-    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->alpha, T * Hv);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->beta, Tp * Hv);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->gl, Tp * Hv);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->W, Tp * Hv * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Ut, Tp * Hv * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Am, Tp * Hv * 64);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Gam, Tp * Hv);
   }
   // weights into the kernels' layout: [qkvz; ba] as one matrix for one pass over x
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->w_in_codes, w->qkvz.codes, Nqkvz * H / 2, cudaMemcpyDeviceToDevice, s);
@@ -517,11 +523,16 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.l2_eps = c.l2_eps;
   p.rms_eps = c.rms_eps;
   p.ts_out = c.act_scale_out;
+  p.Tp = (T + 63) / 64 * 64;
   p.qn = ctx->qn;
   p.kn = ctx->kn;
   p.v = ctx->v;
   p.beta = ctx->beta;
-  p.alpha = ctx->alpha;
+  p.gl = ctx->gl;
+  p.W = ctx->W;
+  p.Ut = ctx->Ut;
+  p.Am = ctx->Am;
+  p.Gam = ctx->Gam;
   p.o = ctx->o;
   p.y_codes = ctx->y_codes;
   p.y_scales = ctx->y_scales;

@@ -280,16 +280,19 @@ cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc);
 
 struct PrefillArgs {
   const uint16_t *proj;  // [T][ld] BF16: q | k | v | z | b | a
-  int ld, T;
+  int ld, T, Tp;         // Tp = T rounded up to whole 64-token chunks
   uint16_t *conv_state;  // this slot's [K-1][C]
   float *ssm;            // this slot's [Hv][D][D]
   const uint16_t *conv_w;
   const float *A_log, *dt_bias, *norm_w;
   int Hk, Hv, D, C, Kc;
   float l2_eps, rms_eps, ts_out;
-  float *qn, *kn;        // [T][Hk][D]
-  float *v;              // [T][Hv][D]
-  float *beta, *alpha;   // [T][Hv]
+  float *qn, *kn;        // [Hk][Tp][D]: normalised q (times d^-1/2) and k
+  float *v;              // [Hv][Tp][D]
+  float *beta, *gl;      // [Hv][Tp]: beta and the log-decay g
+  float *W, *Ut;         // [Hv][nc][64][D]: per chunk T diag(beta e^Gamma) K and T diag(beta) V
+  float *Am;             // [Hv][nc][64][64]: exp(Gamma_i - Gamma_j) q_i.k_j, j <= i
+  float *Gam;            // [Hv][nc][64]: in-chunk cumulative log-decay
   float *o;              // [T][Hv][D]
   uint8_t *y_codes;      // [T][Hv*D/2]
   uint8_t *y_scales;     // [T][Hv*D/16]

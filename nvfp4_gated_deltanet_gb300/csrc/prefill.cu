@@ -1,17 +1,33 @@
-// Prefill of one sequence: the decode arithmetic applied to T tokens, split
-// into token-parallel stages around the one sequential part, the recurrence.
+// Prefill of one sequence: the decode arithmetic over T tokens, with the gated
+// delta rule in 64-token chunks (the WY / UT form; bloomery issue #565, Round 1,
+// #812: the delta rule of a prompt runs in chunks on tensor cores).
 //
-//   prep      (token, key head)  conv + SiLU of q, k and the group's v channels,
-//                                 q/k L2 norm, beta and alpha = exp(g)
-//   recur     (value head, rows) S kept in registers across all T tokens
-//   gnorm     (token)            z-gated RMSNorm + NVFP4 quantisation of y
-//   conv_tail (channel)          the slot's conv state after the last token
+// Within a chunk with start state S0 and rows i = 1..64 (per value head):
+//   Gamma_i = sum_{j<=i} g_j,  D_ij = exp(Gamma_i - Gamma_j)  (j <= i)
+//   L_ij = beta_i D_ij (k_i . k_j)  (j < i)
+//   (I + L) [W | Ut] = [diag(beta e^Gamma) K | diag(beta) V]
+//   U = Ut - W S0^T
+//   O_i = e^Gamma_i (S0 q_i) + sum_{j<=i} D_ij (q_i . k_j) u_j
+//   S_64 = e^Gamma_64 S0 + sum_j D_64j u_j k_j^T
+// which is the token recurrence S <- a S; u = b (v - S k); S <- S + u k^T;
+// o = S q rewritten over a chunk (u_i = beta_i (v_i - a_i S_{i-1} k_i)).
+// Decays are formed only as exp of non-positive log differences, never as
+// ratios, so decays down to -240 per token cannot overflow.
+//
+//   prep        (token, key head)   conv + SiLU, q/k L2 norm, beta, g
+//   chunk_prep  (chunk, value head) k.k and q.k, the triangular solve, W, Ut
+//   chunk_scan  (value head, 32 rows of d_v), sequential over chunks: U, O,
+//               and the state slice, kept in shared memory across chunks
+//   gnorm       (token)             z-gated RMSNorm + NVFP4 quantisation of y
+//   conv_tail   (channel)           the slot's conv state after the last token
+// This first form does the chunk products in FP32 on the CUDA cores.
 #include "common.cuh"
 
 namespace gdn {
 
-
 namespace {
+
+constexpr int kC = 64;  // chunk length
 
 // raw conv input of channel `ch` at token `tau` (tau < 0 reads the state)
 GDN_DEV float conv_in(const PrefillArgs &a, int tau, int ch) {
@@ -35,8 +51,12 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
     for (int j = 0; j < a.Kc; ++j)
       pre = fmaf(bf16_bits_to_f32(a.conv_w[(size_t)ch * a.Kc + j]), conv_in(a, t - (a.Kc - 1) + j, ch), pre);
     const float y = siluf_(pre);
-    if (i < 2 * D) sm[i] = y;
-    else a.v[((size_t)t * a.Hv + kh * G) * D + (i - 2 * D)] = y;
+    if (i < 2 * D) {
+      sm[i] = y;
+    } else {
+      const int h = kh * G + (i - 2 * D) / D, e = (i - 2 * D) % D;
+      a.v[((size_t)h * a.Tp + t) * D + e] = y;
+    }
   }
   __syncthreads();
   // norms exactly as the decode kernel takes them: lane-local sums over D/32
@@ -55,82 +75,256 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
   const float rq = (1.0f / sqrtf(ss[0] + a.l2_eps)) * (1.0f / sqrtf((float)D));
   const float rk = 1.0f / sqrtf(ss[1] + a.l2_eps);
   for (int i = threadIdx.x; i < D; i += blockDim.x) {
-    a.qn[((size_t)t * a.Hk + kh) * D + i] = sq[i] * rq;
-    a.kn[((size_t)t * a.Hk + kh) * D + i] = sk[i] * rk;
+    a.qn[((size_t)kh * a.Tp + t) * D + i] = sq[i] * rq;
+    a.kn[((size_t)kh * a.Tp + t) * D + i] = sk[i] * rk;
   }
   if (threadIdx.x < G) {
     const int h = kh * G + threadIdx.x;
     const uint16_t *ba = a.proj + (size_t)t * a.ld + 2 * a.Hk * D + 2 * a.Hv * D;
-    const float bt = sigmoidf_(bf16_bits_to_f32(ba[h]));
-    const float g = -expf(a.A_log[h]) * softplusf_(bf16_bits_to_f32(ba[a.Hv + h]) + a.dt_bias[h]);
-    a.beta[(size_t)t * a.Hv + h] = bt;
-    a.alpha[(size_t)t * a.Hv + h] = expf(g);
+    a.beta[(size_t)h * a.Tp + t] = sigmoidf_(bf16_bits_to_f32(ba[h]));
+    a.gl[(size_t)h * a.Tp + t] = -expf(a.A_log[h]) * softplusf_(bf16_bits_to_f32(ba[a.Hv + h]) + a.dt_bias[h]);
   }
 }
 
-constexpr int kRPW = 8;
-
-// one warp owns kRPW rows of one value head's state for the whole sequence
+// ---------------------------------------------------------------- chunk_prep
+// One CTA (256 threads) per (chunk, value head). Tokens past T count as zero
+// (k = q = v = 0, beta = 0, g = 0), which adds nothing to any product.
 template <int D>
-__global__ void __launch_bounds__(128) recur_kernel(PrefillArgs a) {
-  constexpr int EPL = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int wph = D / kRPW;  // warps per head
-  const int h = gw / wph;
-  if (h >= a.Hv) return;
-  const int r0 = (gw % wph) * kRPW;
+__global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
+  constexpr int LD = kC + 4;  // row stride of the transposed tiles (float4 aligned)
+  extern __shared__ __align__(16) float sm[];
+  float *KT = sm;                 // [D][LD]: KT[d][i] = k_i[d]
+  float *QT = KT + D * LD;        // [D][LD]
+  float *Lm = QT + D * LD;        // [kC][kC]
+  float *gam = Lm + kC * kC;      // [kC]
+  float *bet = gam + kC;          // [kC]
+  const int c = blockIdx.x, h = blockIdx.y;
   const int kh = h / (a.Hv / a.Hk);
-  float *S = a.ssm + ((size_t)h * D + r0) * D + lane * EPL;
-  float st[kRPW][EPL];
-#pragma unroll
-  for (int j = 0; j < kRPW; ++j)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) st[j][e] = S[(size_t)j * D + e];
+  const int t0 = c * kC;
+  const int nc = a.Tp / kC;
+  const int tid = threadIdx.x;
 
-  for (int t = 0; t < a.T; ++t) {
-    float kr[EPL], qr[EPL];
-    const float *kp = a.kn + ((size_t)t * a.Hk + kh) * D + lane * EPL;
-    const float *qp = a.qn + ((size_t)t * a.Hk + kh) * D + lane * EPL;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) { kr[e] = kp[e]; qr[e] = qp[e]; }
-    const float beta = a.beta[(size_t)t * a.Hv + h];
-    const float alpha = a.alpha[(size_t)t * a.Hv + h];
-    const float *vp = a.v + ((size_t)t * a.Hv + h) * D + r0;
-    float kq = 0.0f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) kq = fmaf(kr[e], qr[e], kq);
-    float red[2 * kRPW];
-#pragma unroll
-    for (int j = 0; j < kRPW; ++j) {
-      float dk = 0.0f, dq = 0.0f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        dk = fmaf(st[j][e], kr[e], dk);
-        dq = fmaf(st[j][e], qr[e], dq);
-      }
-      red[j] = dk;
-      red[kRPW + j] = dq;
-    }
-    const float tot = warp_transpose_reduce<2 * kRPW>(red, lane);
-    kq = warp_sum(kq);
-    float my_o = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kRPW; ++j) {
-      const float Sk = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(j));
-      const float Sq = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(kRPW + j));
-      const float u = beta * (vp[j] - alpha * Sk);
-      const float o = fmaf(u, kq, alpha * Sq);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) st[j][e] = fmaf(u, kr[e], alpha * st[j][e]);
-      if (lane == j) my_o = o;
-    }
-    if (lane < kRPW) a.o[((size_t)t * a.Hv + h) * D + r0 + lane] = my_o;
+  for (int e = tid; e < kC * D; e += blockDim.x) {
+    const int i = e / D, d = e % D;
+    const bool live = t0 + i < a.T;
+    KT[d * LD + i] = live ? a.kn[((size_t)kh * a.Tp + t0 + i) * D + d] : 0.0f;
+    QT[d * LD + i] = live ? a.qn[((size_t)kh * a.Tp + t0 + i) * D + d] : 0.0f;
   }
+  if (tid < kC) {
+    const bool live = t0 + tid < a.T;
+    bet[tid] = live ? a.beta[(size_t)h * a.Tp + t0 + tid] : 0.0f;
+  }
+  if (tid == 0) {  // cumulative log-decay, in token order
+    float acc = 0.0f;
+    for (int i = 0; i < kC; ++i) {
+      acc += (t0 + i < a.T) ? a.gl[(size_t)h * a.Tp + t0 + i] : 0.0f;
+      gam[i] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < kC) a.Gam[((size_t)h * nc + c) * kC + tid] = gam[tid];
+
+  // k.k and q.k on a 4x4 register tile per thread
+  {
+    const int ti = tid >> 4, tj = tid & 15;
+    float kk[4][4] = {}, qk[4][4] = {};
+    for (int d = 0; d < D; ++d) {
+      const float4 ka = *reinterpret_cast<const float4 *>(KT + d * LD + 4 * ti);
+      const float4 qa = *reinterpret_cast<const float4 *>(QT + d * LD + 4 * ti);
+      const float4 kb = *reinterpret_cast<const float4 *>(KT + d * LD + 4 * tj);
+      const float av[4] = {ka.x, ka.y, ka.z, ka.w}, qv[4] = {qa.x, qa.y, qa.z, qa.w};
+      const float bv[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-  for (int j = 0; j < kRPW; ++j)
+      for (int x = 0; x < 4; ++x)
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) S[(size_t)j * D + e] = st[j][e];
+        for (int y = 0; y < 4; ++y) {
+          kk[x][y] = fmaf(av[x], bv[y], kk[x][y]);
+          qk[x][y] = fmaf(qv[x], bv[y], qk[x][y]);
+        }
+    }
+    float *Ag = a.Am + ((size_t)h * nc + c) * kC * kC;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int i = 4 * ti + x;
+      float lrow[4], arow[4];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int j = 4 * tj + y;
+        const float dec = j <= i ? expf(gam[i] - gam[j]) : 0.0f;
+        lrow[y] = j < i ? bet[i] * dec * kk[x][y] : 0.0f;
+        arow[y] = dec * qk[x][y];
+      }
+      *reinterpret_cast<float4 *>(Lm + i * kC + 4 * tj) = make_float4(lrow[0], lrow[1], lrow[2], lrow[3]);
+      *reinterpret_cast<float4 *>(Ag + (size_t)i * kC + 4 * tj) = make_float4(arow[0], arow[1], arow[2], arow[3]);
+    }
+  }
+  __syncthreads();
+
+  // (I + L) X = R by forward substitution, one column per thread (no barriers):
+  // columns 0..D-1 give W (R = beta e^Gamma k), D..2D-1 give Ut (R = beta v).
+  if (tid < 2 * D) {
+    const int col = tid;
+    float X[kC];
+#pragma unroll
+    for (int i = 0; i < kC; ++i) {
+      float r;
+      if (col < D) {
+        r = bet[i] * expf(gam[i]) * KT[col * LD + i];
+      } else {
+        r = (t0 + i < a.T) ? bet[i] * a.v[((size_t)h * a.Tp + t0 + i) * D + (col - D)] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < i; ++j) r = fmaf(-Lm[i * kC + j], X[j], r);
+      X[i] = r;
+    }
+    float *dst = (col < D ? a.W : a.Ut) + ((size_t)h * nc + c) * kC * D + (col < D ? col : col - D);
+#pragma unroll
+    for (int i = 0; i < kC; ++i) dst[(size_t)i * D] = X[i];
+  }
+}
+
+// ---------------------------------------------------------------- chunk_scan
+GDN_DEV void cp_async16(void *dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+GDN_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+GDN_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// One CTA (256 threads = 8 warps) per (value head, 32 rows of d_v). The state
+// slice S[32][D] stays in shared memory across all chunks; lane = row r of the
+// slice in every product.
+template <int D>
+__global__ void __launch_bounds__(256) chunk_scan_kernel(PrefillArgs a) {
+  constexpr int R = 32;
+  constexpr int NSL = D / R;
+  constexpr int SLD = D + 1;  // padded row stride of S (conflict-free lane = row)
+  constexpr int RLD = R + 1;
+  extern __shared__ __align__(16) float sm[];
+  float *Ws = sm;                    // [kC][D]
+  float *Qs = Ws + kC * D;           // [kC][D]
+  float *Ks = Qs + kC * D;           // [kC][D]
+  float *Us = Ks + kC * D;           // [kC][R]  Ut slice, then U
+  float *As = Us + kC * R;           // [kC][kC]
+  float *Gs = As + kC * kC;          // [kC]
+  float *S = Gs + kC;                // [R][SLD]
+  float *P = S + R * SLD;            // [2 kC][RLD]: W S0^T then Q S0^T
+  float *Cf = P + 2 * kC * RLD;      // [kC][RLD]: e^(Gamma_64 - Gamma_j) u_j
+
+  const int h = blockIdx.x / NSL, r0 = (blockIdx.x % NSL) * R;
+  const int kh = h / (a.Hv / a.Hk);
+  const int nc = a.Tp / kC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int e = tid; e < R * D; e += blockDim.x) {
+    const int r = e / D, d = e % D;
+    S[r * SLD + d] = a.ssm[((size_t)h * D + r0 + r) * D + d];
+  }
+  auto load_wq = [&](int c) {
+    const float *w = a.W + ((size_t)h * nc + c) * kC * D;
+    const float *q = a.qn + ((size_t)kh * a.Tp + (size_t)c * kC) * D;
+    for (int e = tid; e < kC * D / 4; e += blockDim.x) {
+      const int i = (4 * e) / D;
+      cp_async16(Ws + 4 * e, w + 4 * e, true);
+      cp_async16(Qs + 4 * e, q + 4 * e, c * kC + i < a.T);
+    }
+  };
+  auto load_rest = [&](int c) {
+    const float *k = a.kn + ((size_t)kh * a.Tp + (size_t)c * kC) * D;
+    for (int e = tid; e < kC * D / 4; e += blockDim.x) {
+      const int i = (4 * e) / D;
+      cp_async16(Ks + 4 * e, k + 4 * e, c * kC + i < a.T);
+    }
+    const float *u = a.Ut + ((size_t)h * nc + c) * kC * D + r0;
+    for (int e = tid; e < kC * R / 4; e += blockDim.x) {
+      const int i = (4 * e) / R, r = (4 * e) % R;
+      cp_async16(Us + 4 * e, u + (size_t)i * D + r, true);
+    }
+    const float *am = a.Am + ((size_t)h * nc + c) * kC * kC;
+    for (int e = tid; e < kC * kC / 4; e += blockDim.x) cp_async16(As + 4 * e, am + 4 * e, true);
+    if (tid < kC / 4) cp_async16(Gs + 4 * tid, a.Gam + ((size_t)h * nc + c) * kC + 4 * tid, true);
+  };
+  load_wq(0);
+  load_rest(0);
+  cp_async_commit();
+
+  for (int c = 0; c < nc; ++c) {
+    cp_async_wait_all();
+    __syncthreads();
+    // P = [W; Q] S0^T: warp w -> rows 16w..16w+15 of [W; Q], lane -> slice row r
+    {
+      const float *X = warp < 4 ? Ws + (16 * warp) * D : Qs + (16 * (warp - 4)) * D;
+      float acc[16];
+#pragma unroll
+      for (int x = 0; x < 16; ++x) acc[x] = 0.0f;
+      for (int d = 0; d < D; d += 4) {
+        const float s0 = S[lane * SLD + d], s1 = S[lane * SLD + d + 1];
+        const float s2 = S[lane * SLD + d + 2], s3 = S[lane * SLD + d + 3];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const float4 xv = *reinterpret_cast<const float4 *>(X + x * D + d);
+          acc[x] = fmaf(xv.x, s0, fmaf(xv.y, s1, fmaf(xv.z, s2, fmaf(xv.w, s3, acc[x]))));
+        }
+      }
+#pragma unroll
+      for (int x = 0; x < 16; ++x) P[(16 * warp + x) * RLD + lane] = acc[x];
+    }
+    __syncthreads();
+    if (c + 1 < nc) {  // W and Q of this chunk are consumed
+      load_wq(c + 1);
+      cp_async_commit();
+    }
+    // U = Ut - W S0^T (in place in Us), and the state-update coefficients
+    const float gC = Gs[kC - 1];
+    for (int e = tid; e < kC * R; e += blockDim.x) {
+      const int i = e / R, r = e % R;
+      const float u = Us[i * R + r] - P[i * RLD + r];
+      Us[i * R + r] = u;
+      Cf[i * RLD + r] = expf(gC - Gs[i]) * u;
+    }
+    __syncthreads();
+    // O_i = e^Gamma_i (Q S0^T)_i + sum_{j<=i} A_ij u_j : warps 0..3, 16 rows each
+    if (warp < 4) {
+      for (int x = 0; x < 16; ++x) {
+        const int i = 16 * warp + x;
+        float acc = expf(Gs[i]) * P[(kC + i) * RLD + lane];
+        for (int j = 0; j <= i; ++j) acc = fmaf(As[i * kC + j], Us[j * R + lane], acc);
+        const int t = c * kC + i;
+        if (t < a.T) a.o[((size_t)t * a.Hv + h) * D + r0 + lane] = acc;
+      }
+    }
+    // S <- e^Gamma_64 S + sum_j coef_j[r] k_j : warp w -> columns 16w..16w+15
+    if (warp < D / 16) {
+      const float dC = expf(gC);
+      float sv[16];
+#pragma unroll
+      for (int y = 0; y < 16; ++y) sv[y] = dC * S[lane * SLD + 16 * warp + y];
+      for (int j = 0; j < kC; ++j) {
+        const float cf = Cf[j * RLD + lane];
+#pragma unroll
+        for (int y = 0; y < 16; y += 4) {
+          const float4 kv = *reinterpret_cast<const float4 *>(Ks + j * D + 16 * warp + y);
+          sv[y] = fmaf(cf, kv.x, sv[y]);
+          sv[y + 1] = fmaf(cf, kv.y, sv[y + 1]);
+          sv[y + 2] = fmaf(cf, kv.z, sv[y + 2]);
+          sv[y + 3] = fmaf(cf, kv.w, sv[y + 3]);
+        }
+      }
+#pragma unroll
+      for (int y = 0; y < 16; ++y) S[lane * SLD + 16 * warp + y] = sv[y];
+    }
+    __syncthreads();
+    if (c + 1 < nc) {  // K, U, A and Gamma of this chunk are consumed
+      load_rest(c + 1);
+      cp_async_commit();
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  for (int e = tid; e < R * D; e += blockDim.x) {
+    const int r = e / D, d = e % D;
+    a.ssm[((size_t)h * D + r0 + r) * D + d] = S[r * SLD + d];
+  }
 }
 
 // one CTA per token; thread i owns 16-block i of y (head i / (D/16))
@@ -183,6 +377,26 @@ __global__ void copy_u16_kernel(uint16_t *dst, const uint16_t *src, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) dst[i] = src[i];
 }
 
+template <int D>
+cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
+  constexpr int LD = kC + 4;
+  const size_t sm_prep = (size_t)(2 * D * LD + kC * kC + 2 * kC) * sizeof(float);
+  const size_t sm_scan =
+      (size_t)(3 * kC * D + kC * 32 + kC * kC + kC + 32 * (D + 1) + 2 * kC * 33 + kC * 33) * sizeof(float);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_prep);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(chunk_scan_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_scan);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int nc = a.Tp / kC;
+  chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
+  chunk_scan_kernel<D><<<a.Hv * (D / 32), 256, sm_scan, lc.stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 // The stages between the projections (run by the caller) and the out
@@ -194,14 +408,13 @@ cudaError_t launch_prefill_mix(const PrefillArgs &a, uint16_t *tmp, const Launch
   // conv state tail is computed from the old state before anything overwrites it
   const int n = (a.Kc - 1) * a.C;
   conv_tail_kernel<<<(n + 255) / 256, 256, 0, lc.stream>>>(a, tmp);
-  const int warps = a.Hv * (a.D / kRPW);
-  const int ctas = (warps + 3) / 4;
   switch (a.D) {
-    case 128: recur_kernel<128><<<ctas, 128, 0, lc.stream>>>(a); break;
-    case 64: recur_kernel<64><<<ctas, 128, 0, lc.stream>>>(a); break;
-    case 32: recur_kernel<32><<<ctas, 128, 0, lc.stream>>>(a); break;
+    case 128: e = launch_chunks<128>(a, lc); break;
+    case 64: e = launch_chunks<64>(a, lc); break;
+    case 32: e = launch_chunks<32>(a, lc); break;
     default: return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   const int gthreads = ((a.Hv * a.D / 16) + 31) / 32 * 32;
   gnorm_kernel<<<a.T, gthreads, 0, lc.stream>>>(a);
   copy_u16_kernel<<<(n + 255) / 256, 256, 0, lc.stream>>>(a.conv_state, tmp, n);

@@ -128,3 +128,26 @@ def test_prefill_long_vs_decode_and_sampled_heads(api, T):
     want = _oracle_heads_final_state(x, heads)
     for h in heads:
         assert rel_l2(ssm_p[h], want[h]) <= 2e-3, h
+
+
+@pytest.mark.parametrize("shape_name,seed,T", [("TINY", 0, 150), ("TINY", 0, 64), ("TINY", 0, 1), ("FULL", 1, 200)])
+def test_prefill_ragged_and_continued_matches_oracle(api, shape_name, seed, T):
+    """Ragged last chunk, a single token, and a prompt split in two calls (the
+    second continues from the slot's state) against the oracle's recurrence."""
+    shape = getattr(synth, shape_name)
+    layer = api.layer_from_synth(weights(shape_name, seed), max_batch=1, max_prefill_tokens=T)
+    O = oracle_layer(shape_name, seed)
+    x = synth.x_tokens(shape, 7, T)
+    conv_d, ssm_d = layer.new_states(3)
+    split = max(1, T // 3)
+    out1 = to_host(layer.prefill(to_dev(x[:split]), 2, True, conv_d, ssm_d))
+    out2 = to_host(layer.prefill(to_dev(x[split:]), 2, False, conv_d, ssm_d)) if split < T else np.zeros((0, shape.hidden), np.uint16)
+    assert layer.check() == 0
+    got = np.concatenate([out1, out2])
+    c = synth.conv_state(shape, 7, True)
+    s = synth.ssm_state(shape, 7, True)
+    want = O.prefill(x, c, s, init_zero=True)
+    assert rel_l2(_bf(got), _bf(want)) <= 2e-3
+    assert rel_l2(to_host(ssm_d)[2], s) <= 2e-3
+    np.testing.assert_array_equal(to_host(ssm_d)[0], 0)          # other slots untouched
+    assert rel_l2(_bf(to_host(conv_d)[2]), _bf(c)) <= 4e-3
