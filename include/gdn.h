@@ -171,6 +171,26 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
                        uint16_t *out, uint16_t *conv_state, float *ssm_state, int num_slots,
                        void *stream);
 
+/* The decode step of gdn_decode_step for callers that cannot allocate device
+ * memory or keep a context: runtimes that fix all device memory at start-up,
+ * work issued while a CUDA graph is captured, hosts that pass only tensors.
+ * (It has no counterpart on the pages the library follows: it is an interface
+ * choice of this library.) The caller passes the config and the weights
+ * exactly as for gdn_create (device pointers, read on every call), and x,
+ * slot_ids, out, conv_state, ssm_state as for gdn_decode_step. The call
+ * allocates nothing: its intermediates live in one fixed device array of
+ * 450,560 bytes inside the library, which bounds the shape: B <= 16,
+ * hidden <= 2048, 2*Hk*d_k + 2*Hv*d_v + 2*Hv <= 12352, Hv*d_v <= 4096
+ * (else GDN_E_SHAPE). The first call on a device looks up that array's
+ * address (make it before any stream capture). All calls on a device share the
+ * array: calls that overlap on the GPU race, so serialise them. Weight scale
+ * bytes are not scanned for NaN (gdn_create does that). Device-detected errors
+ * go to *dev_status (device int32, may be NULL) as in nvfp4_quantize.
+ * Errors: as gdn_create's checks and gdn_decode_step's, plus GDN_E_CUDA. */
+gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, const uint16_t *x,
+                                  const int32_t *slot_ids, int B, uint16_t *out, uint16_t *conv_state,
+                                  float *ssm_state, int num_slots, int32_t *dev_status, void *stream);
+
 /* Process-wide tuning knobs (they change speed, never results beyond FP32
  * summation order). knob 0: projection kernel of decode and prefill:
  * 0 = automatic (more than 2 activation rows and a reduction length that is a

@@ -47,6 +47,8 @@ SIGNATURES = {
     "gdn_prefill": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp, _vp, _i, _vp]),
     "gdn_check": (_i, [_vp, _i, _vp]),
     "gdn_set_tuning": (_i, [_i, _i]),
+    "gdn_decode_step_static": (_i, [ctypes.POINTER(GdnConfig), ctypes.POINTER(GdnWeights), _vp, _vp, _i, _vp, _vp,
+                                    _vp, _i, _vp, _vp]),
 }
 
 _lib = None
