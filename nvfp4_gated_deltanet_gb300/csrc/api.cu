@@ -24,7 +24,8 @@ struct gdn_ctx {
   float *qn, *kn, *v, *beta, *gl, *o;     // prefill intermediates (head-major, chunk-padded)
   float *W, *Ut, *Am, *Gam;               // per (value head, 64-token chunk) products
   uint16_t *conv_tmp;                   // [K-1][C]
-  uint8_t *xq_codes, *xq_scales;        // [prow][H/2], [prow][H/16]: x as NVFP4 for the tensor-core GEMM
+  uint8_t *xq_codes, *xq_scales;        // [prow][H/2] and tiled scales: x as NVFP4 for the tensor-core GEMM
+  uint8_t *w_in_sf_t, *w_out_sf_t;      // the weights' scales in the tiled layout tcgen05.cp reads
   TcGemm tc_in, tc_out;                 // weight tensor maps of the two projections
   bool tc_in_ok, tc_out_ok;             // K % 256 == 0: the tcgen05 path applies
   int32_t *status;
@@ -149,7 +150,7 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
   const gdn_config &c = ctx->cfg;
   if (allow_tc && ctx->tc_in_ok && use_tensor_cores(rows)) {
     cudaError_t e = launch_quantize(x, 0, rows, c.hidden, c.act_scale_in, ctx->xq_codes, ctx->xq_scales, ctx->status,
-                                    lc.stream, row_slot, num_slots, lc.pdl);
+                                    lc.stream, row_slot, num_slots, lc.pdl, true);
     if (e != cudaSuccess) return e;
     TcGemm t = ctx->tc_in;
     t.b_codes = ctx->xq_codes;
@@ -165,6 +166,8 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
     t.args.a_split = ctx->Nqkvz;
     t.args.ts_b = c.act_scale_in;
     t.args.a_const = 1;
+    t.args.sfa_tiled = ctx->w_in_sf_t;
+    t.args.sfb_tiled = ctx->xq_scales;
     t.args.status = ctx->status;
     t.split_k = split_for(g_tune.split_in, rows, 2);
     return launch_tc_gemm(t, lc);
@@ -188,6 +191,10 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
   return run_gemv(g, lc, rows);
 }
 
+// Whether the out-projection of `rows` rows runs on tensor cores, so the
+// mixing stage must write y's scales in the tiled layout.
+bool out_proj_tiled(const gdn_ctx *ctx, int rows) { return ctx->tc_out_ok && use_tensor_cores(rows); }
+
 // y (NVFP4 in the context's workspace) -> out (BF16 [rows][H]).
 cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx &lc, bool allow_tc) {
   const gdn_config &c = ctx->cfg;
@@ -205,6 +212,8 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
     t.args.a_split = c.hidden;
     t.args.ts_b = c.act_scale_out;
     t.args.a_const = 1;
+    t.args.sfa_tiled = ctx->w_out_sf_t;
+    t.args.sfb_tiled = ctx->y_scales;  // written tiled by the mixing stage (out_proj_tiled)
     t.args.status = ctx->status;
     t.split_k = split_for(g_tune.split_out, rows, 4);
     return launch_tc_gemm(t, lc);
@@ -310,11 +319,14 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->norm_w, D);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->proj, prow * Nin);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_codes, prow * Vd / 2);
-  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_scales, prow * Vd / 16);
+  // scales sized for both layouts: row-major, or tiled (rows padded to 128)
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_scales, sf_tiled_bytes((int)prow, (int)Vd));
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_in_sf_t, sf_tiled_bytes((int)Nin, (int)H));
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_out_sf_t, sf_tiled_bytes((int)H, (int)Vd));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->status, 1);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->conv_tmp, (c.conv_kernel - 1) * Cc);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_codes, prow * H / 2);
-  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_scales, prow * H / 16);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_scales, sf_tiled_bytes((int)prow, (int)H));
   if (T > 0) {
     const long long Tp = (T + 63) / 64 * 64;
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->qn, Tp * Hk * D);
@@ -342,6 +354,8 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->A_log, w->A_log, Hv * 4, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->dt_bias, w->dt_bias, Hv * 4, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->norm_w, w->norm_w, D * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && H % 64 == 0) e = launch_tile_scales(ctx->w_in_scales, (int)Nin, (int)H, ctx->w_in_sf_t, s);
+  if (e == cudaSuccess && Vd % 64 == 0) e = launch_tile_scales(ctx->w_out_scales, (int)H, (int)Vd, ctx->w_out_sf_t, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->status, 0, 4, s);
   if (e == cudaSuccess) {
     scan_nan_scales<<<256, 256, 0, s>>>(ctx->w_in_scales, (size_t)(Nin * H / 16), ctx->status);
@@ -455,6 +469,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   m.ssm_state = ssm_state;
   m.y_codes = ctx->y_codes;
   m.y_scales = ctx->y_scales;
+  m.y_sf_tiled = out_proj_tiled(ctx, B) ? 1 : 0;
   m.y_f32 = nullptr;
   e = launch_mix(m, lc);
   if (e != cudaSuccess) return cuda_status(e);
@@ -536,6 +551,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.o = ctx->o;
   p.y_codes = ctx->y_codes;
   p.y_scales = ctx->y_scales;
+  p.y_sf_tiled = out_proj_tiled(ctx, T) ? 1 : 0;
   p.status = ctx->status;
   e = launch_prefill_mix(p, ctx->conv_tmp, lc);
   if (e != cudaSuccess) return cuda_status(e);

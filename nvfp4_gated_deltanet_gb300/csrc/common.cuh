@@ -99,6 +99,16 @@ GDN_DEV bool quant_block16(const float (&v)[16], float ts, float inv6ts, uint32_
 
 GDN_DEV float inv6ts_of(float ts) { return __frcp_rn(__fmul_rn(6.0f, ts)); }
 
+// Tiled scale layout read by tcgen05.cp .32x128b.warpx4 for one operand of the
+// block-scaled MMA: the scales of 128 rows x one 64-wide K step form a 512-byte
+// atom, row r at byte (r % 32) * 16 + ((r % 128) / 32) * 4 + k-block; atoms are
+// ordered [row tile][K step]. `blk` is the 16-element block index along K,
+// `nblk` = K / 16 (a multiple of 4). Rows are padded to whole 128-row tiles.
+__host__ __device__ __forceinline__ size_t sf_tiled_offset(int r, int blk, int nblk) {
+  return ((size_t)(r >> 7) * (nblk >> 2) + (blk >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (blk & 3);
+}
+inline size_t sf_tiled_bytes(int rows, int K) { return (size_t)((rows + 127) / 128) * 128 * (K / 16); }
+
 // ---------------------------------------------------------------- reductions
 // xor butterfly: partners add the same two values in either order, so every
 // lane ends with the bit-identical total.
@@ -233,9 +243,13 @@ struct LaunchCtx {
 
 // row_slot (optional): row r is quantised as zeros when row_slot[r] is not a
 // valid slot (a padding row of a decode batch).
+// sf_tiled: write the scales in the tiled layout (sf_tiled_offset) instead of
+// row-major [rows][cols/16]; needs cols % 64 == 0.
 cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, float ts, uint8_t *codes,
                             uint8_t *scales, int32_t *status, cudaStream_t stream, const int32_t *row_slot = nullptr,
-                            int num_slots = 0, bool pdl = false);
+                            int num_slots = 0, bool pdl = false, bool sf_tiled = false);
+// Repack row-major scales [rows][K/16] into the tiled layout (padding rows 0).
+cudaError_t launch_tile_scales(const uint8_t *src, int rows, int K, uint8_t *dst, cudaStream_t stream);
 
 // C[M][N] (ldc) = A_hat[M][K] * W_hat[N][K]^T. A is BF16 rows (quantised inside
 // with ts_a; a_rows_valid may mark rows to treat as zero) or NVFP4. Rows of W
@@ -272,7 +286,8 @@ struct MixArgs {
   int Hk, Hv, D, C, Kc;
   float l2_eps, rms_eps, ts_out;
   uint8_t *y_codes;   // [B][Hv*dv/2] or null
-  uint8_t *y_scales;  // [B][Hv*dv/16]
+  uint8_t *y_scales;  // [B][Hv*dv/16] row-major, or tiled when y_sf_tiled
+  int y_sf_tiled;
   float *y_f32;       // [B][Hv*dv] or null
   int32_t *status;
 };
@@ -295,7 +310,8 @@ struct PrefillArgs {
   float *Gam;            // [Hv][nc][64]: in-chunk cumulative log-decay
   float *o;              // [T][Hv][D]
   uint8_t *y_codes;      // [T][Hv*D/2]
-  uint8_t *y_scales;     // [T][Hv*D/16]
+  uint8_t *y_scales;     // [T][Hv*D/16] row-major, or tiled when y_sf_tiled
+  int y_sf_tiled;
   int32_t *status;
 };
 // Block-scaled W4A4 GEMM on tcgen05: D[m][n] = W_hat[m][:] . X_hat[n][:],
@@ -310,6 +326,9 @@ struct TcArgs {
   int a_split;
   float ts_b;
   int a_const;         // weights written by no preceding kernel: stream them before griddepcontrol.wait
+  // Optional: both operands' scales already in the tiled layout tcgen05.cp
+  // reads (sf_tiled_offset); then they are bulk-copied straight into place.
+  const uint8_t *sfa_tiled, *sfb_tiled;
   int32_t *status;
 };
 struct TcGemm {

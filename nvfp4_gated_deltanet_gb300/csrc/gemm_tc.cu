@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nt = blockIdx.y;
   const int nkt = (a.K >> 8) / KS;
   const int kt0 = ks * nkt;
+  const bool tiled = a.sfa_tiled != nullptr && a.sfb_tiled != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -171,27 +172,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t bytes = kATile + L::kB + 128 * 16 + BN * 16;
+      const uint32_t bytes = tiled ? kATile + L::kB + 2 * 4 * kSFAtom : kATile + L::kB + 128 * 16 + BN * 16;
+      const int ksteps = a.K >> 6;
+      const int nsf = (nt * BN) >> 7;  // 128-row tile of the activation scales (BN < 128: one N tile)
+      auto load_a = [&](int i, int s) {
+        tma_load_2d(stA(s), &tmA, (kt0 + i) * 128, mt * 128, full + s);
+        if (tiled)
+          bulk_g2s(stAtA(s), a.sfa_tiled + ((size_t)mt * ksteps + (size_t)(kt0 + i) * 4) * kSFAtom, 4 * kSFAtom, full + s);
+        else
+          tma_load_2d(stSA(s), &tmSA, (kt0 + i) * 16, mt * 128, full + s);
+      };
+      auto load_b = [&](int i, int s) {
+        tma_load_2d(stB(s), &tmB, (kt0 + i) * 128, nt * BN, full + s);
+        if (tiled)
+          bulk_g2s(stAtB(s), a.sfb_tiled + ((size_t)nsf * ksteps + (size_t)(kt0 + i) * 4) * kSFAtom, 4 * kSFAtom, full + s);
+        else
+          tma_load_2d(stSB(s), &tmSB, (kt0 + i) * 16, nt * BN, full + s);
+      };
       const int pre = a.a_const ? min(S, nkt) : 0;
       for (int i = 0; i < pre; ++i) {  // weights do not depend on the preceding kernel
         mbar_arrive_expect_tx(full + i, bytes);
-        tma_load_2d(stA(i), &tmA, (kt0 + i) * 128, mt * 128, full + i);
-        tma_load_2d(stSA(i), &tmSA, (kt0 + i) * 16, mt * 128, full + i);
+        load_a(i, i);
       }
       pdl_wait();
       pdl_launch_dependents();
-      for (int i = 0; i < pre; ++i) {
-        tma_load_2d(stB(i), &tmB, (kt0 + i) * 128, nt * BN, full + i);
-        tma_load_2d(stSB(i), &tmSB, (kt0 + i) * 16, nt * BN, full + i);
-      }
+      for (int i = 0; i < pre; ++i) load_b(i, i);
       for (int i = pre; i < nkt; ++i) {
         const int s = i % S, u = i / S;
         if (u > 0 && !mbar_wait(empty + s, (uint32_t)((u - 1) & 1))) { ok = false; break; }
         mbar_arrive_expect_tx(full + s, bytes);
-        tma_load_2d(stA(s), &tmA, (kt0 + i) * 128, mt * 128, full + s);
-        tma_load_2d(stSA(s), &tmSA, (kt0 + i) * 16, mt * 128, full + s);
-        tma_load_2d(stB(s), &tmB, (kt0 + i) * 128, nt * BN, full + s);
-        tma_load_2d(stSB(s), &tmSB, (kt0 + i) * 16, nt * BN, full + s);
+        load_a(i, s);
+        load_b(i, s);
       }
     }
   } else if (warp == 1) {
@@ -200,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_nvf4<BN>();
       for (int i = 0; i < nkt; ++i) {
         const int s = i % S, u = i / S;
-        if (!mbar_wait(full + s, (uint32_t)(u & 1)) || !mbar_wait(sfready + s, (uint32_t)(u & 1))) {
+        if (!mbar_wait(full + s, (uint32_t)(u & 1)) || (!tiled && !mbar_wait(sfready + s, (uint32_t)(u & 1)))) {
           ok = false;
           break;
         }
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ scale rearrangement
     const int t = threadIdx.x - 64;  // 0..127
-    for (int i = 0; i < nkt; ++i) {
+    for (int i = 0; i < (tiled ? 0 : nkt); ++i) {
       const int s = i % S, u = i / S;
       if (!mbar_wait(full + s, (uint32_t)(u & 1))) { ok = false; break; }
       const uint4 va = *reinterpret_cast<const uint4 *>(stSA(s) + t * 16);
@@ -272,8 +283,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < BN; ++c) acc[c] += part[((size_t)p * BN + c) * 128 + row];
       const int m = mt * 128 + row;
-      if (m < a.Ma) {
-        const float ts = (m < a.a_split ? a.ts_a0 : a.ts_a1) * a.ts_b;
+      const float ts = (m < a.a_split ? a.ts_a0 : a.ts_a1) * a.ts_b;
+      // Stage the tile as [BN][128] in shared memory (the pipeline stages are
+      // idle once the accumulator is complete), then write whole rows of C
+      // with 16-byte stores.
+      const int esz = a.c_is_bf16 ? 2 : 4;
+      const bool vec = (a.ldc * esz) % 16 == 0 && (a.Ma % 8) == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.c) & 15u) == 0;
+      if (vec) {
+        unsigned char *tile = stage0;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const float y = acc[c] * ts;
+          if (a.c_is_bf16)
+            reinterpret_cast<uint16_t *>(tile)[c * 128 + row] = f32_to_bf16_bits(y);
+          else
+            reinterpret_cast<float *>(tile)[c * 128 + row] = y;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+        const int t = threadIdx.x - 64;
+        const int per_row = 128 * esz / 16;  // 16-byte chunks per tile row
+        for (int idx = t; idx < BN * per_row; idx += 128) {
+          const int cl = idx / per_row, ch = idx % per_row;
+          const int n = nt * BN + cl, m0 = mt * 128 + ch * (16 / esz);
+          if (n < a.Nb && m0 < a.Ma)
+            *reinterpret_cast<uint4 *>(static_cast<unsigned char *>(a.c) + ((size_t)n * a.ldc + m0) * esz) =
+                *reinterpret_cast<const uint4 *>(tile + ((size_t)cl * 128 + ch * (16 / esz)) * esz);
+        }
+      } else if (m < a.Ma) {
 #pragma unroll
         for (int c = 0; c < BN; ++c) {
           const int n = nt * BN + c;

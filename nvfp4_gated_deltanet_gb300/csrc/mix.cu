@@ -117,7 +117,10 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
     for (int i = tid; i < R; i += blockDim.x) {
       if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = 0.0f;
       if (a.y_codes && (i & 1) == 0) a.y_codes[((size_t)b * vd + h * D + row0 + i) >> 1] = 0;
-      if (a.y_scales && (i & 15) == 0) a.y_scales[((size_t)b * vd + h * D + row0 + i) >> 4] = 0;
+      if (a.y_scales && (i & 15) == 0) {
+        const int blk = (h * D + row0 + i) >> 4;
+        a.y_scales[a.y_sf_tiled ? sf_tiled_offset(b, blk, vd >> 4) : ((size_t)b * vd >> 4) + blk] = 0;
+      }
     }
     return;
   }
@@ -270,7 +273,8 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
     if (!quant_block16(v, a.ts_out, inv6ts_of(a.ts_out), lo, hi, s)) flag_status(a.status, GDN_E_NONFINITE);
     const size_t e0 = (size_t)b * vd + h * D + row0 + tid * 16;
     *reinterpret_cast<uint2 *>(a.y_codes + (e0 >> 1)) = make_uint2(lo, hi);
-    a.y_scales[e0 >> 4] = uint8_t(s);
+    const int blk = (h * D + row0 + tid * 16) >> 4;
+    a.y_scales[a.y_sf_tiled ? sf_tiled_offset(b, blk, vd >> 4) : (e0 >> 4)] = uint8_t(s);
   }
 }
 

@@ -20,7 +20,7 @@
 //               and the state slice, kept in shared memory across chunks
 //   gnorm       (token)             z-gated RMSNorm + NVFP4 quantisation of y
 //   conv_tail   (channel)           the slot's conv state after the last token
-// This first form does the chunk products in FP32 on the CUDA cores.
+// The chunk products run in FP32 on the CUDA cores.
 #include "common.cuh"
 
 namespace gdn {
@@ -29,17 +29,12 @@ namespace {
 
 constexpr int kC = 64;  // chunk length
 
-// raw conv input of channel `ch` at token `tau` (tau < 0 reads the state)
-GDN_DEV float conv_in(const PrefillArgs &a, int tau, int ch) {
-  if (tau >= 0) return bf16_bits_to_f32(a.proj[(size_t)tau * a.ld + ch]);
-  return bf16_bits_to_f32(a.conv_state[(size_t)(a.Kc - 1 + tau) * a.C + ch]);
-}
-
 // one CTA per (token, key head); blockDim = 128
+template <int D>
 __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
-  extern __shared__ float sm[];
+  __shared__ float sm[2 * D];
   const int t = blockIdx.x, kh = blockIdx.y;
-  const int D = a.D, G = a.Hv / a.Hk;
+  const int G = a.Hv / a.Hk;
   float *sq = sm, *sk = sm + D;
   const int nch = 2 * D + G * D;
   for (int i = threadIdx.x; i < nch; i += blockDim.x) {
@@ -48,13 +43,20 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
     else if (i < 2 * D) ch = a.Hk * D + kh * D + (i - D);
     else ch = 2 * a.Hk * D + kh * G * D + (i - 2 * D);
     float pre = 0.0f;
-    for (int j = 0; j < a.Kc; ++j)
-      pre = fmaf(bf16_bits_to_f32(a.conv_w[(size_t)ch * a.Kc + j]), conv_in(a, t - (a.Kc - 1) + j, ch), pre);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < a.Kc) {
+        const int tau = t - (a.Kc - 1) + j;
+        const uint16_t bits = tau >= 0 ? a.proj[(size_t)tau * a.ld + ch]
+                                       : a.conv_state[(size_t)(a.Kc - 1 + tau) * a.C + ch];
+        pre = fmaf(bf16_bits_to_f32(a.conv_w[(size_t)ch * a.Kc + j]), bf16_bits_to_f32(bits), pre);
+      }
+    }
     const float y = siluf_(pre);
     if (i < 2 * D) {
       sm[i] = y;
     } else {
-      const int h = kh * G + (i - 2 * D) / D, e = (i - 2 * D) % D;
+      const int h = kh * G + (i - 2 * D) / D, e = (i - 2 * D) % D;  // D is a power of two
       a.v[((size_t)h * a.Tp + t) * D + e] = y;
     }
   }
@@ -65,7 +67,7 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp < 2) {
     const float *src = warp == 0 ? sq : sk;
-    const int epl = D / 32;
+    constexpr int epl = D / 32;
     float p = 0.0f;
     for (int e = 0; e < epl; ++e) p = fmaf(src[lane * epl + e], src[lane * epl + e], p);
     p = warp_sum(p);
@@ -173,9 +175,18 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
       } else {
         r = (t0 + i < a.T) ? bet[i] * a.v[((size_t)h * a.Tp + t0 + i) * D + (col - D)] : 0.0f;
       }
+      // four independent partial sums shorten the dependent FMA chain 4x
+      float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
 #pragma unroll
-      for (int j = 0; j < i; ++j) r = fmaf(-Lm[i * kC + j], X[j], r);
-      X[i] = r;
+      for (int j = 0; j + 3 < i; j += 4) {
+        p0 = fmaf(Lm[i * kC + j], X[j], p0);
+        p1 = fmaf(Lm[i * kC + j + 1], X[j + 1], p1);
+        p2 = fmaf(Lm[i * kC + j + 2], X[j + 2], p2);
+        p3 = fmaf(Lm[i * kC + j + 3], X[j + 3], p3);
+      }
+#pragma unroll
+      for (int j = i & ~3; j < i; ++j) p0 = fmaf(Lm[i * kC + j], X[j], p0);
+      X[i] = r - ((p0 + p1) + (p2 + p3));
     }
     float *dst = (col < D ? a.W : a.Ut) + ((size_t)h * nc + c) * kC * D + (col < D ? col : col - D);
 #pragma unroll
@@ -191,11 +202,11 @@ GDN_DEV void cp_async16(void *dst, const void *src, bool valid) {
 GDN_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 GDN_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// One CTA (256 threads = 8 warps) per (value head, 32 rows of d_v). The state
+// One CTA (512 threads = 16 warps) per (value head, 32 rows of d_v). The state
 // slice S[32][D] stays in shared memory across all chunks; lane = row r of the
 // slice in every product.
 template <int D>
-__global__ void __launch_bounds__(256) chunk_scan_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
   constexpr int R = 32;
   constexpr int NSL = D / R;
   constexpr int SLD = D + 1;  // padded row stride of S (conflict-free lane = row)
@@ -251,23 +262,24 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(PrefillArgs a) {
   for (int c = 0; c < nc; ++c) {
     cp_async_wait_all();
     __syncthreads();
-    // P = [W; Q] S0^T: warp w -> rows 16w..16w+15 of [W; Q], lane -> slice row r
+    // P = [W; Q] S0^T: warp w -> rows 8w..8w+7 of [W; Q], lane -> slice row r
     {
-      const float *X = warp < 4 ? Ws + (16 * warp) * D : Qs + (16 * (warp - 4)) * D;
-      float acc[16];
+      const float *X = warp < 8 ? Ws + (8 * warp) * D : Qs + (8 * (warp - 8)) * D;
+      float acc[8];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) acc[x] = 0.0f;
+      for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+#pragma unroll 4
       for (int d = 0; d < D; d += 4) {
         const float s0 = S[lane * SLD + d], s1 = S[lane * SLD + d + 1];
         const float s2 = S[lane * SLD + d + 2], s3 = S[lane * SLD + d + 3];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
+        for (int x = 0; x < 8; ++x) {
           const float4 xv = *reinterpret_cast<const float4 *>(X + x * D + d);
           acc[x] = fmaf(xv.x, s0, fmaf(xv.y, s1, fmaf(xv.z, s2, fmaf(xv.w, s3, acc[x]))));
         }
       }
 #pragma unroll
-      for (int x = 0; x < 16; ++x) P[(16 * warp + x) * RLD + lane] = acc[x];
+      for (int x = 0; x < 8; ++x) P[(8 * warp + x) * RLD + lane] = acc[x];
     }
     __syncthreads();
     if (c + 1 < nc) {  // W and Q of this chunk are consumed
@@ -283,35 +295,44 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(PrefillArgs a) {
       Cf[i * RLD + r] = expf(gC - Gs[i]) * u;
     }
     __syncthreads();
-    // O_i = e^Gamma_i (Q S0^T)_i + sum_{j<=i} A_ij u_j : warps 0..3, 16 rows each
-    if (warp < 4) {
-      for (int x = 0; x < 16; ++x) {
-        const int i = 16 * warp + x;
-        float acc = expf(Gs[i]) * P[(kC + i) * RLD + lane];
-        for (int j = 0; j <= i; ++j) acc = fmaf(As[i * kC + j], Us[j * R + lane], acc);
+    // O_i = e^Gamma_i (Q S0^T)_i + sum_{j<=i} A_ij u_j : warp w -> rows 4w..4w+3
+    {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int i = 4 * warp + x;
+        float acc0 = expf(Gs[i]) * P[(kC + i) * RLD + lane], acc1 = 0.0f;
+        int j = 0;
+        for (; j + 1 <= i; j += 2) {
+          acc0 = fmaf(As[i * kC + j], Us[j * R + lane], acc0);
+          acc1 = fmaf(As[i * kC + j + 1], Us[(j + 1) * R + lane], acc1);
+        }
+        if (j == i) acc0 = fmaf(As[i * kC + j], Us[j * R + lane], acc0);
         const int t = c * kC + i;
-        if (t < a.T) a.o[((size_t)t * a.Hv + h) * D + r0 + lane] = acc;
+        if (t < a.T) a.o[((size_t)t * a.Hv + h) * D + r0 + lane] = acc0 + acc1;
       }
     }
-    // S <- e^Gamma_64 S + sum_j coef_j[r] k_j : warp w -> columns 16w..16w+15
-    if (warp < D / 16) {
+    // S <- e^Gamma_64 S + sum_j coef_j[r] k_j : warp w -> columns 8w..8w+7
+    if (warp < D / 8) {
       const float dC = expf(gC);
-      float sv[16];
+      float sv[8];
 #pragma unroll
-      for (int y = 0; y < 16; ++y) sv[y] = dC * S[lane * SLD + 16 * warp + y];
+      for (int y = 0; y < 8; ++y) sv[y] = dC * S[lane * SLD + 8 * warp + y];
+#pragma unroll 4
       for (int j = 0; j < kC; ++j) {
         const float cf = Cf[j * RLD + lane];
-#pragma unroll
-        for (int y = 0; y < 16; y += 4) {
-          const float4 kv = *reinterpret_cast<const float4 *>(Ks + j * D + 16 * warp + y);
-          sv[y] = fmaf(cf, kv.x, sv[y]);
-          sv[y + 1] = fmaf(cf, kv.y, sv[y + 1]);
-          sv[y + 2] = fmaf(cf, kv.z, sv[y + 2]);
-          sv[y + 3] = fmaf(cf, kv.w, sv[y + 3]);
-        }
+        const float4 k0 = *reinterpret_cast<const float4 *>(Ks + j * D + 8 * warp);
+        const float4 k1 = *reinterpret_cast<const float4 *>(Ks + j * D + 8 * warp + 4);
+        sv[0] = fmaf(cf, k0.x, sv[0]);
+        sv[1] = fmaf(cf, k0.y, sv[1]);
+        sv[2] = fmaf(cf, k0.z, sv[2]);
+        sv[3] = fmaf(cf, k0.w, sv[3]);
+        sv[4] = fmaf(cf, k1.x, sv[4]);
+        sv[5] = fmaf(cf, k1.y, sv[5]);
+        sv[6] = fmaf(cf, k1.z, sv[6]);
+        sv[7] = fmaf(cf, k1.w, sv[7]);
       }
 #pragma unroll
-      for (int y = 0; y < 16; ++y) S[lane * SLD + 16 * warp + y] = sv[y];
+      for (int y = 0; y < 8; ++y) S[lane * SLD + 8 * warp + y] = sv[y];
     }
     __syncthreads();
     if (c + 1 < nc) {  // K, U, A and Gamma of this chunk are consumed
@@ -360,7 +381,7 @@ __global__ void gnorm_kernel(PrefillArgs a) {
   if (!ok) flag_status(a.status, GDN_E_NONFINITE);
   const size_t b0 = (size_t)t * vd + h * D + e0;
   *reinterpret_cast<uint2 *>(a.y_codes + (b0 >> 1)) = make_uint2(lo, hi);
-  a.y_scales[b0 >> 4] = uint8_t(s);
+  a.y_scales[a.y_sf_tiled ? sf_tiled_offset(t, (h * D + e0) >> 4, vd >> 4) : (b0 >> 4)] = uint8_t(s);
 }
 
 // the slot's conv state after the last token: taps hold inputs T-K+1 .. T-1
@@ -393,7 +414,7 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
   }
   const int nc = a.Tp / kC;
   chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
-  chunk_scan_kernel<D><<<a.Hv * (D / 32), 256, sm_scan, lc.stream>>>(a);
+  chunk_scan_kernel<D><<<a.Hv * (D / 32), 512, sm_scan, lc.stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -402,7 +423,12 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
 // The stages between the projections (run by the caller) and the out
 // projection. `tmp` holds (K-1)*C BF16 values.
 cudaError_t launch_prefill_mix(const PrefillArgs &a, uint16_t *tmp, const LaunchCtx &lc) {
-  prep_kernel<<<dim3(a.T, a.Hk), 128, 2 * a.D * sizeof(float), lc.stream>>>(a);
+  switch (a.D) {
+    case 128: prep_kernel<128><<<dim3(a.T, a.Hk), 128, 0, lc.stream>>>(a); break;
+    case 64: prep_kernel<64><<<dim3(a.T, a.Hk), 128, 0, lc.stream>>>(a); break;
+    case 32: prep_kernel<32><<<dim3(a.T, a.Hk), 128, 0, lc.stream>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // conv state tail is computed from the old state before anything overwrites it

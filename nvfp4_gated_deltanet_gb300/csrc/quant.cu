@@ -8,7 +8,8 @@ template <bool F32>
 __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ x, int rows, int cols, float ts,
                                                        uint8_t *__restrict__ codes,
                                                        uint8_t *__restrict__ scales,
-                                                       int32_t *status, const int32_t *row_slot, int num_slots) {
+                                                       int32_t *status, const int32_t *row_slot, int num_slots,
+                                                       int sf_tiled) {
   pdl_wait();  // x may come from the preceding kernel
   pdl_launch_dependents();
   const int nb = cols >> 4;
@@ -45,13 +46,16 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void *__restrict__ 
     uint32_t lo, hi, s;
     if (!quant_block16(v, ts, inv6ts, lo, hi, s)) flag_status(status, GDN_E_NONFINITE);
     *reinterpret_cast<uint2 *>(codes + r * (cols >> 1) + b * 8) = make_uint2(lo, hi);
-    scales[r * nb + b] = uint8_t(s);
+    if (sf_tiled)
+      scales[sf_tiled_offset((int)r, (int)b, nb)] = uint8_t(s);
+    else
+      scales[r * nb + b] = uint8_t(s);
   }
 }
 
 cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, float ts, uint8_t *codes,
                             uint8_t *scales, int32_t *status, cudaStream_t stream, const int32_t *row_slot,
-                            int num_slots, bool pdl) {
+                            int num_slots, bool pdl, bool sf_tiled) {
   const long long total = (long long)rows * (cols / 16);
   if (total == 0) return cudaSuccess;
   long long blocks = (total + 255) / 256;
@@ -66,8 +70,24 @@ cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, flo
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (x_is_f32)
-    return cudaLaunchKernelEx(&cfg, quantize_kernel<true>, x, rows, cols, ts, codes, scales, status, row_slot, num_slots);
-  return cudaLaunchKernelEx(&cfg, quantize_kernel<false>, x, rows, cols, ts, codes, scales, status, row_slot, num_slots);
+    return cudaLaunchKernelEx(&cfg, quantize_kernel<true>, x, rows, cols, ts, codes, scales, status, row_slot, num_slots,
+                              (int)sf_tiled);
+  return cudaLaunchKernelEx(&cfg, quantize_kernel<false>, x, rows, cols, ts, codes, scales, status, row_slot, num_slots,
+                            (int)sf_tiled);
+}
+
+__global__ void tile_scales_kernel(const uint8_t *src, int rows, int K, uint8_t *dst) {
+  const int nb = K / 16;
+  const int prow = (rows + 127) / 128 * 128;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < (size_t)prow * nb; i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / nb), b = (int)(i % nb);
+    dst[sf_tiled_offset(r, b, nb)] = r < rows ? src[(size_t)r * nb + b] : uint8_t(0);
+  }
+}
+
+cudaError_t launch_tile_scales(const uint8_t *src, int rows, int K, uint8_t *dst, cudaStream_t stream) {
+  tile_scales_kernel<<<304, 256, 0, stream>>>(src, rows, K, dst);
+  return cudaGetLastError();
 }
 
 }  // namespace gdn
