@@ -198,7 +198,11 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * 1 = CUDA-core kernel (also for nvfp4_gemm with M <= 16), 2 = tensor cores
  * where the reduction length allows. knob 1 / knob 2: split-K of the in- /
  * out-projection on tensor cores, 0 = automatic, or 1, 2, 4, 8 (reduced to
- * the largest power of two that divides the 256-wide K tiles).
+ * the largest power of two that divides the 256-wide K tiles). knob 3: decode
+ * of one or two rows as one persistent cooperative kernel (weights and state
+ * prefetched into shared memory, grid barriers between the stages): 0 and 1 =
+ * never (the default: it measured slower than the three-kernel step on
+ * GB300), 2 = when the shape allows (d_k = 128, B <= 2, knob 0 is not 2).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

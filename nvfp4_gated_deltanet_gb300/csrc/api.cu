@@ -29,6 +29,7 @@ struct gdn_ctx {
   TcGemm tc_in, tc_out;                 // weight tensor maps of the two projections
   bool tc_in_ok, tc_out_ok;             // K % 256 == 0: the tcgen05 path applies
   int32_t *status;
+  unsigned int *grid_bar;               // the fused decode kernel's grid barrier words
   std::vector<void *> allocs;
 };
 
@@ -47,6 +48,7 @@ struct Tuning {
   int decode_gemm = 0;  // 0 auto, 1 CUDA-core GEMV, 2 tcgen05
   int split_in = 0;     // split-K of the in-projection on tensor cores (0 = automatic)
   int split_out = 0;    // split-K of the out-projection
+  int fused = 0;        // one- and two-row decode as one persistent kernel: 0 auto (off), 1 off, 2 on
 };
 Tuning g_tune;
 
@@ -235,6 +237,49 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
   return run_gemv(o, lc, rows);
 }
 
+FusedArgs fused_args(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *out,
+                     uint16_t *conv_state, float *ssm_state, int num_slots) {
+  const gdn_config &c = ctx->cfg;
+  FusedArgs f{};
+  f.w_in_codes = ctx->w_in_codes;
+  f.w_in_scales = ctx->w_in_scales;
+  f.w_out_codes = ctx->w_out_codes;
+  f.w_out_scales = ctx->w_out_scales;
+  f.ts_qkvz = ctx->ts_qkvz;
+  f.ts_ba = ctx->ts_ba;
+  f.ts_wout = ctx->ts_wout;
+  f.Nqkvz = ctx->Nqkvz;
+  f.Nin = ctx->Nin;
+  f.conv_w = ctx->conv_w;
+  f.A_log = ctx->A_log;
+  f.dt_bias = ctx->dt_bias;
+  f.norm_w = ctx->norm_w;
+  f.H = c.hidden;
+  f.Hk = c.n_k_heads;
+  f.Hv = c.n_v_heads;
+  f.D = c.d_k;
+  f.C = ctx->C;
+  f.Kc = c.conv_kernel;
+  f.Vd = ctx->Vd;
+  f.l2_eps = c.l2_eps;
+  f.rms_eps = c.rms_eps;
+  f.ts_in = c.act_scale_in;
+  f.ts_out = c.act_scale_out;
+  f.x = x;
+  f.slot_ids = slot_ids;
+  f.B = B;
+  f.num_slots = num_slots;
+  f.out = out;
+  f.conv_state = conv_state;
+  f.ssm_state = ssm_state;
+  f.proj = ctx->proj;
+  f.y_codes = ctx->y_codes;
+  f.y_scales = ctx->y_scales;
+  f.bar = ctx->grid_bar;
+  f.status = ctx->status;
+  return f;
+}
+
 }  // namespace
 
 extern "C" {
@@ -249,6 +294,10 @@ gdn_status gdn_set_tuning(int knob, int value) {
     case 2:
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return GDN_E_RANGE;
       (knob == 1 ? g_tune.split_in : g_tune.split_out) = value;
+      return GDN_OK;
+    case 3:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      g_tune.fused = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;
@@ -324,6 +373,7 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_in_sf_t, sf_tiled_bytes((int)Nin, (int)H));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_out_sf_t, sf_tiled_bytes((int)H, (int)Vd));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->status, 1);
+  if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->grid_bar, 4);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->conv_tmp, (c.conv_kernel - 1) * Cc);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_codes, prow * H / 2);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->xq_scales, sf_tiled_bytes((int)prow, (int)H));
@@ -357,6 +407,7 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess && H % 64 == 0) e = launch_tile_scales(ctx->w_in_scales, (int)Nin, (int)H, ctx->w_in_sf_t, s);
   if (e == cudaSuccess && Vd % 64 == 0) e = launch_tile_scales(ctx->w_out_scales, (int)H, (int)Vd, ctx->w_out_sf_t, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->status, 0, 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->grid_bar, 0, 16, s);
   if (e == cudaSuccess) {
     scan_nan_scales<<<256, 256, 0, s>>>(ctx->w_in_scales, (size_t)(Nin * H / 16), ctx->status);
     scan_nan_scales<<<256, 256, 0, s>>>(ctx->w_out_scales, (size_t)(H * Vd / 16), ctx->status);
@@ -455,6 +506,13 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   if (!aligned16(slot_ids)) return GDN_E_ALIGN;
   if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
   LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, true};
+  // The persistent single-kernel step (fused.cu) is correct but measured slower
+  // on GB300 (c1 20.8 vs 14.6 us per layer-step: each grid barrier costs
+  // ~2.5 us, more than a PDL kernel boundary), so it runs only on request.
+  if (g_tune.fused == 2 && g_tune.decode_gemm != 2 && B <= 2) {
+    FusedArgs f = fused_args(ctx, x, slot_ids, B, out, conv_state, ssm_state, num_slots);
+    if (fused_plan(f, ctx->num_sms)) return cuda_status(launch_fused(f, lc));
+  }
   cudaError_t e = run_in_proj(ctx, x, B, slot_ids, num_slots, lc, true);
   if (e != cudaSuccess) return cuda_status(e);
   MixArgs m = mix_args(ctx);

@@ -340,6 +340,31 @@ struct TcGemm {
 bool tc_make_weight_maps(TcGemm &g, const uint8_t *w_codes, const uint8_t *w_scales, int rows, int K);
 cudaError_t launch_tc_gemm(const TcGemm &g, const LaunchCtx &lc);
 
+// The whole decode layer-step for one or two rows in one cooperative launch
+// (fused.cu).
+struct FusedArgs {
+  const uint8_t *w_in_codes, *w_in_scales;    // [Nin][H/2], [Nin][H/16]: qkvz rows then ba rows
+  const uint8_t *w_out_codes, *w_out_scales;  // [H][Vd/2], [H][Vd/16]
+  float ts_qkvz, ts_ba, ts_wout;
+  int Nqkvz, Nin;
+  const uint16_t *conv_w;
+  const float *A_log, *dt_bias, *norm_w;
+  int H, Hk, Hv, D, C, Kc, Vd;
+  float l2_eps, rms_eps, ts_in, ts_out;
+  const uint16_t *x;
+  const int32_t *slot_ids;
+  int B, num_slots;
+  uint16_t *out, *conv_state;
+  float *ssm_state;
+  uint16_t *proj;                 // scratch [B][Nin]
+  uint8_t *y_codes, *y_scales;    // scratch [B][Vd/2], [B][Vd/16] row-major
+  unsigned int *bar;              // grid barrier words (2), zero before the first launch
+  int32_t *status;
+  int rows_in, rows_out;          // weight rows per CTA (set by fused_plan)
+};
+bool fused_plan(FusedArgs &a, int num_sms);
+cudaError_t launch_fused(const FusedArgs &a, const LaunchCtx &lc);
+
 cudaError_t launch_prefill_mix(const PrefillArgs &a, uint16_t *tmp, const LaunchCtx &lc);
 
 }  // namespace gdn

@@ -146,3 +146,25 @@ def test_batch_rows_equal_single_rows(api, path):
                 assert rel_l2(to_host(s1)[i], to_host(sb)[i]) <= 1e-5
     finally:
         api.lib().gdn_set_tuning(0, 0)
+
+
+def test_fused_single_kernel_step_matches_oracle(api):
+    """The one-launch decode step (tuning knob 3 = 2) for one and two rows."""
+    shape = synth.FULL
+    L = _layer(api, "FULL", 1)
+    O = oracle_layer("FULL", 1)
+    api.lib().gdn_set_tuning(3, 2)
+    try:
+        for B in (1, 2):
+            x, conv0, ssm0 = slot_inputs(shape, list(range(B)), 3)
+            conv_d, ssm_d = to_dev(conv0), to_dev(ssm0)
+            ids = torch.arange(B, dtype=torch.int32, device="cuda")
+            got = np.stack([to_host(L.decode_step(to_dev(x[t]), ids, conv_d, ssm_d)) for t in range(3)])
+            assert L.check() == 0
+            c, s = conv0.copy(), ssm0.copy()
+            want = np.stack([O.decode_step(x[t], list(range(B)), c, s) for t in range(3)])
+            assert rel_l2(_bf16(got), _bf16(want)) <= 4e-3
+            assert rel_l2(to_host(ssm_d), s) <= 1e-4
+            np.testing.assert_array_equal(to_host(conv_d), c)
+    finally:
+        api.lib().gdn_set_tuning(3, 0)
