@@ -14,7 +14,7 @@
 // Decays are formed only as exp of non-positive log differences, never as
 // ratios, so decays down to -240 per token cannot overflow.
 //
-//   prep        (token, key head)   conv + SiLU, q/k L2 norm, beta, g
+//   prep        (32 tokens, head)   conv + SiLU, q/k L2 norm, beta, g
 //   chunk_prep  (chunk, value head) k.k and q.k, the triangular solve, W, Ut
 //   chunk_scan  (value head, 32 rows of d_v), sequential over chunks: U, O,
 //               and the state slice, kept in shared memory across chunks
@@ -29,62 +29,96 @@ namespace {
 
 constexpr int kC = 64;  // chunk length
 
-// one CTA per (token, key head); blockDim = 128
+// prep: one CTA (128 threads) per (32-token tile, group of D channels): the
+// group is the q or k channels of one key head, or the v channels of one value
+// head; group index 2*Hk + Hv .. handles beta and g. The conv window (tile +
+// K-1 earlier tokens) is read once with 16-byte loads; q and k rows are
+// L2-normalised by one warp per token with lane-local sums over D/32
+// consecutive elements and the warp butterfly -- the decode kernel's order.
+constexpr int kPrepTT = 32;
+
 template <int D>
 __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
-  __shared__ float sm[2 * D];
-  const int t = blockIdx.x, kh = blockIdx.y;
-  const int G = a.Hv / a.Hk;
-  float *sq = sm, *sk = sm + D;
-  const int nch = 2 * D + G * D;
-  for (int i = threadIdx.x; i < nch; i += blockDim.x) {
-    int ch;
-    if (i < D) ch = kh * D + i;
-    else if (i < 2 * D) ch = a.Hk * D + kh * D + (i - D);
-    else ch = 2 * a.Hk * D + kh * G * D + (i - 2 * D);
-    float pre = 0.0f;
+  __shared__ __align__(16) uint16_t win[kPrepTT + 3][D];
+  __shared__ float outv[kPrepTT][D + 1];
+  const int t0 = blockIdx.x * kPrepTT, grp = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ngrp = 2 * a.Hk + a.Hv;
+  if (grp == ngrp) {  // gates: beta and g for the tile's tokens and every value head
+    for (int e = tid; e < kPrepTT * a.Hv; e += blockDim.x) {
+      const int t = t0 + e / a.Hv, h = e % a.Hv;
+      if (t >= a.T) continue;
+      const uint16_t *ba = a.proj + (size_t)t * a.ld + 2 * a.Hk * D + 2 * a.Hv * D;
+      a.beta[(size_t)h * a.Tp + t] = sigmoidf_(bf16_bits_to_f32(ba[h]));
+      a.gl[(size_t)h * a.Tp + t] = -expf(a.A_log[h]) * softplusf_(bf16_bits_to_f32(ba[a.Hv + h]) + a.dt_bias[h]);
+    }
+    return;
+  }
+  const int ch0 = grp * D;  // q heads, then k heads, then v heads: the conv channel order
+  const int Kc = a.Kc;
+  // window rows r = 0 .. TT+Kc-2 hold tokens t0 - (Kc-1) + r (state rows for t < 0)
+  constexpr int VPR = D / 8;  // 16-byte vectors per row
+  if (a.ld % 8 == 0 && a.C % 8 == 0) {  // every row starts 16-byte aligned
+    for (int e = tid; e < (kPrepTT + Kc - 1) * VPR; e += blockDim.x) {
+      const int r = e / VPR, v = e % VPR;
+      const int tau = t0 - (Kc - 1) + r;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (tau >= 0 && tau < a.T)
+        val = *reinterpret_cast<const uint4 *>(a.proj + (size_t)tau * a.ld + ch0 + v * 8);
+      else if (tau < 0)
+        val = *reinterpret_cast<const uint4 *>(a.conv_state + (size_t)(Kc - 1 + tau) * a.C + ch0 + v * 8);
+      *reinterpret_cast<uint4 *>(&win[r][v * 8]) = val;
+    }
+  } else {
+    for (int e = tid; e < (kPrepTT + Kc - 1) * D; e += blockDim.x) {
+      const int r = e / D, c = e % D;
+      const int tau = t0 - (Kc - 1) + r;
+      uint16_t val = 0;
+      if (tau >= 0 && tau < a.T)
+        val = a.proj[(size_t)tau * a.ld + ch0 + c];
+      else if (tau < 0)
+        val = a.conv_state[(size_t)(Kc - 1 + tau) * a.C + ch0 + c];
+      win[r][c] = val;
+    }
+  }
+  __syncthreads();
+  // conv + SiLU: thread -> channel, loop over the tile's tokens
+  for (int c = tid; c < D; c += blockDim.x) {
+    float w[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (j < a.Kc) {
-        const int tau = t - (a.Kc - 1) + j;
-        const uint16_t bits = tau >= 0 ? a.proj[(size_t)tau * a.ld + ch]
-                                       : a.conv_state[(size_t)(a.Kc - 1 + tau) * a.C + ch];
-        pre = fmaf(bf16_bits_to_f32(a.conv_w[(size_t)ch * a.Kc + j]), bf16_bits_to_f32(bits), pre);
-      }
-    }
-    const float y = siluf_(pre);
-    if (i < 2 * D) {
-      sm[i] = y;
-    } else {
-      const int h = kh * G + (i - 2 * D) / D, e = (i - 2 * D) % D;  // D is a power of two
-      a.v[((size_t)h * a.Tp + t) * D + e] = y;
+    for (int j = 0; j < 4; ++j) w[j] = j < Kc ? bf16_bits_to_f32(a.conv_w[(size_t)(ch0 + c) * Kc + j]) : 0.0f;
+    for (int i = 0; i < kPrepTT; ++i) {
+      float pre = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < Kc) pre = fmaf(w[j], bf16_bits_to_f32(win[i + j][c]), pre);
+      outv[i][c] = siluf_(pre);
     }
   }
   __syncthreads();
-  // norms exactly as the decode kernel takes them: lane-local sums over D/32
-  // consecutive elements, then the warp butterfly (warp 0: q, warp 1: k)
-  __shared__ float ss[2];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp < 2) {
-    const float *src = warp == 0 ? sq : sk;
-    constexpr int epl = D / 32;
-    float p = 0.0f;
-    for (int e = 0; e < epl; ++e) p = fmaf(src[lane * epl + e], src[lane * epl + e], p);
-    p = warp_sum(p);
-    if (lane == 0) ss[warp] = p;
-  }
-  __syncthreads();
-  const float rq = (1.0f / sqrtf(ss[0] + a.l2_eps)) * (1.0f / sqrtf((float)D));
-  const float rk = 1.0f / sqrtf(ss[1] + a.l2_eps);
-  for (int i = threadIdx.x; i < D; i += blockDim.x) {
-    a.qn[((size_t)kh * a.Tp + t) * D + i] = sq[i] * rq;
-    a.kn[((size_t)kh * a.Tp + t) * D + i] = sk[i] * rk;
-  }
-  if (threadIdx.x < G) {
-    const int h = kh * G + threadIdx.x;
-    const uint16_t *ba = a.proj + (size_t)t * a.ld + 2 * a.Hk * D + 2 * a.Hv * D;
-    a.beta[(size_t)h * a.Tp + t] = sigmoidf_(bf16_bits_to_f32(ba[h]));
-    a.gl[(size_t)h * a.Tp + t] = -expf(a.A_log[h]) * softplusf_(bf16_bits_to_f32(ba[a.Hv + h]) + a.dt_bias[h]);
+  const int nq = a.Hk;  // groups 0..Hk-1: q, Hk..2Hk-1: k, then v
+  if (grp < 2 * nq) {
+    const bool isq = grp < nq;
+    const int kh = isq ? grp : grp - nq;
+    float *dst = (isq ? a.qn : a.kn) + ((size_t)kh * a.Tp) * D;
+    constexpr int EPL = D / 32;
+    for (int i = warp; i < kPrepTT; i += blockDim.x / 32) {
+      const int t = t0 + i;
+      float p = 0.0f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) p = fmaf(outv[i][lane * EPL + e], outv[i][lane * EPL + e], p);
+      p = warp_sum(p);
+      const float r = isq ? (1.0f / sqrtf(p + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(p + a.l2_eps);
+      if (t < a.T)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dst[(size_t)t * D + lane * EPL + e] = outv[i][lane * EPL + e] * r;
+    }
+  } else {
+    const int h = grp - 2 * nq;
+    for (int e = tid; e < kPrepTT * D; e += blockDim.x) {
+      const int i = e / D, c = e % D;
+      if (t0 + i < a.T) a.v[((size_t)h * a.Tp + t0 + i) * D + c] = outv[i][c];
+    }
   }
 }
 
@@ -106,11 +140,15 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
   const int nc = a.Tp / kC;
   const int tid = threadIdx.x;
 
-  for (int e = tid; e < kC * D; e += blockDim.x) {
-    const int i = e / D, d = e % D;
+  for (int e = tid; e < kC * D / 4; e += blockDim.x) {
+    const int i = (4 * e) / D, d = (4 * e) % D;
     const bool live = t0 + i < a.T;
-    KT[d * LD + i] = live ? a.kn[((size_t)kh * a.Tp + t0 + i) * D + d] : 0.0f;
-    QT[d * LD + i] = live ? a.qn[((size_t)kh * a.Tp + t0 + i) * D + d] : 0.0f;
+    const float4 kv = live ? *reinterpret_cast<const float4 *>(a.kn + ((size_t)kh * a.Tp + t0 + i) * D + d)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 qv = live ? *reinterpret_cast<const float4 *>(a.qn + ((size_t)kh * a.Tp + t0 + i) * D + d)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    KT[d * LD + i] = kv.x; KT[(d + 1) * LD + i] = kv.y; KT[(d + 2) * LD + i] = kv.z; KT[(d + 3) * LD + i] = kv.w;
+    QT[d * LD + i] = qv.x; QT[(d + 1) * LD + i] = qv.y; QT[(d + 2) * LD + i] = qv.z; QT[(d + 3) * LD + i] = qv.w;
   }
   if (tid < kC) {
     const bool live = t0 + tid < a.T;
@@ -164,29 +202,32 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
 
   // (I + L) X = R by forward substitution, one column per thread (no barriers):
   // columns 0..D-1 give W (R = beta e^Gamma k), D..2D-1 give Ut (R = beta v).
+  // All right-hand sides are loaded first; rows of L are read 4 at a time.
   if (tid < 2 * D) {
     const int col = tid;
     float X[kC];
 #pragma unroll
     for (int i = 0; i < kC; ++i) {
-      float r;
-      if (col < D) {
-        r = bet[i] * expf(gam[i]) * KT[col * LD + i];
-      } else {
-        r = (t0 + i < a.T) ? bet[i] * a.v[((size_t)h * a.Tp + t0 + i) * D + (col - D)] : 0.0f;
-      }
+      if (col < D)
+        X[i] = bet[i] * expf(gam[i]) * KT[col * LD + i];
+      else
+        X[i] = (t0 + i < a.T) ? bet[i] * a.v[((size_t)h * a.Tp + t0 + i) * D + (col - D)] : 0.0f;
+    }
+#pragma unroll
+    for (int i = 1; i < kC; ++i) {
       // four independent partial sums shorten the dependent FMA chain 4x
       float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
 #pragma unroll
       for (int j = 0; j + 3 < i; j += 4) {
-        p0 = fmaf(Lm[i * kC + j], X[j], p0);
-        p1 = fmaf(Lm[i * kC + j + 1], X[j + 1], p1);
-        p2 = fmaf(Lm[i * kC + j + 2], X[j + 2], p2);
-        p3 = fmaf(Lm[i * kC + j + 3], X[j + 3], p3);
+        const float4 l = *reinterpret_cast<const float4 *>(Lm + i * kC + j);
+        p0 = fmaf(l.x, X[j], p0);
+        p1 = fmaf(l.y, X[j + 1], p1);
+        p2 = fmaf(l.z, X[j + 2], p2);
+        p3 = fmaf(l.w, X[j + 3], p3);
       }
 #pragma unroll
       for (int j = i & ~3; j < i; ++j) p0 = fmaf(Lm[i * kC + j], X[j], p0);
-      X[i] = r - ((p0 + p1) + (p2 + p3));
+      X[i] = X[i] - ((p0 + p1) + (p2 + p3));
     }
     float *dst = (col < D ? a.W : a.Ut) + ((size_t)h * nc + c) * kC * D + (col < D ? col : col - D);
 #pragma unroll
@@ -423,10 +464,11 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
 // The stages between the projections (run by the caller) and the out
 // projection. `tmp` holds (K-1)*C BF16 values.
 cudaError_t launch_prefill_mix(const PrefillArgs &a, uint16_t *tmp, const LaunchCtx &lc) {
+  const dim3 pg((a.T + kPrepTT - 1) / kPrepTT, 2 * a.Hk + a.Hv + 1);
   switch (a.D) {
-    case 128: prep_kernel<128><<<dim3(a.T, a.Hk), 128, 0, lc.stream>>>(a); break;
-    case 64: prep_kernel<64><<<dim3(a.T, a.Hk), 128, 0, lc.stream>>>(a); break;
-    case 32: prep_kernel<32><<<dim3(a.T, a.Hk), 128, 0, lc.stream>>>(a); break;
+    case 128: prep_kernel<128><<<pg, 128, 0, lc.stream>>>(a); break;
+    case 64: prep_kernel<64><<<pg, 128, 0, lc.stream>>>(a); break;
+    case 32: prep_kernel<32><<<pg, 128, 0, lc.stream>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaGetLastError();

