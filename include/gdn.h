@@ -203,6 +203,17 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * prefetched into shared memory, grid barriers between the stages): 0 and 1 =
  * never (the default: it measured slower than the three-kernel step on
  * GB300), 2 = when the shape allows (d_k = 128, B <= 2, knob 0 is not 2).
+ * knob 4: a decode in-projection on tensor cores with at most 16 rows
+ * quantises x inside the GEMM (0 and 2 = yes, the default; 1 = a separate
+ * quantisation kernel first). knob 5: the out-projection of gdn_decode_step
+ * lets the next kernel in the stream launch before it waits on the mixing
+ * kernel (0 = on the tensor-core out-projection only, the default; 1 = never;
+ * 2 = also on the CUDA-core one); every kernel of this library that may follow
+ * it reads only weights until its own dependency wait.
+ * knob 6: tensor-core projections of a context stream the weight codes from a
+ * pre-swizzled copy made at gdn_create, one contiguous 16 KB bulk copy per
+ * 128 x 256 tile (0 and 2 = yes, the default; 1 = tensor-map copies from the
+ * row-major codes).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

@@ -26,6 +26,7 @@ struct gdn_ctx {
   uint16_t *conv_tmp;                   // [K-1][C]
   uint8_t *xq_codes, *xq_scales;        // [prow][H/2] and tiled scales: x as NVFP4 for the tensor-core GEMM
   uint8_t *w_in_sf_t, *w_out_sf_t;      // the weights' scales in the tiled layout tcgen05.cp reads
+  uint8_t *w_in_tiles, *w_out_tiles;    // the weights' codes as pre-swizzled 16 KB MMA tiles
   TcGemm tc_in, tc_out;                 // weight tensor maps of the two projections
   bool tc_in_ok, tc_out_ok;             // K % 256 == 0: the tcgen05 path applies
   int32_t *status;
@@ -49,6 +50,10 @@ struct Tuning {
   int split_in = 0;     // split-K of the in-projection on tensor cores (0 = automatic)
   int split_out = 0;    // split-K of the out-projection
   int fused = 0;        // one- and two-row decode as one persistent kernel: 0 auto (off), 1 off, 2 on
+  int in_quant_fused = 0;  // decode in-projection on tensor cores quantises x itself: 0 auto (on), 1 off, 2 on
+  int early_trigger = 0;   // out-projection of a decode step signals the next kernel early: 0 auto (tensor-core
+                           // out-projection only), 1 off, 2 on
+  int swizzled_tiles = 0;  // tensor-core weights from the pre-swizzled tile copy: 0 auto (on), 1 off, 2 on
 };
 Tuning g_tune;
 
@@ -151,10 +156,18 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
                         const LaunchCtx &lc, bool allow_tc) {
   const gdn_config &c = ctx->cfg;
   if (allow_tc && ctx->tc_in_ok && use_tensor_cores(rows)) {
-    cudaError_t e = launch_quantize(x, 0, rows, c.hidden, c.act_scale_in, ctx->xq_codes, ctx->xq_scales, ctx->status,
-                                    lc.stream, row_slot, num_slots, lc.pdl, true);
-    if (e != cudaSuccess) return e;
     TcGemm t = ctx->tc_in;
+    // up to 16 rows: the GEMM quantises x itself; more: a quantisation kernel first
+    const bool fused_q = rows <= 16 && g_tune.in_quant_fused != 1;
+    if (!fused_q) {
+      cudaError_t e = launch_quantize(x, 0, rows, c.hidden, c.act_scale_in, ctx->xq_codes, ctx->xq_scales, ctx->status,
+                                      lc.stream, row_slot, num_slots, lc.pdl, true);
+      if (e != cudaSuccess) return e;
+    } else {
+      t.args.b_bf16 = x;
+      t.args.b_row_slot = row_slot;
+      t.args.b_num_slots = num_slots;
+    }
     t.b_codes = ctx->xq_codes;
     t.b_scales = ctx->xq_scales;
     t.args.Ma = ctx->Nin;
@@ -169,6 +182,7 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
     t.args.ts_b = c.act_scale_in;
     t.args.a_const = 1;
     t.args.sfa_tiled = ctx->w_in_sf_t;
+    t.args.a_tiles = g_tune.swizzled_tiles != 1 ? ctx->w_in_tiles : nullptr;
     t.args.sfb_tiled = ctx->xq_scales;
     t.args.status = ctx->status;
     t.split_k = split_for(g_tune.split_in, rows, 2);
@@ -198,7 +212,10 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
 bool out_proj_tiled(const gdn_ctx *ctx, int rows) { return ctx->tc_out_ok && use_tensor_cores(rows); }
 
 // y (NVFP4 in the context's workspace) -> out (BF16 [rows][H]).
-cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx &lc, bool allow_tc) {
+// early: the out-projection is the last kernel of a decode step and lets the
+// next kernel in the stream launch before it waits (TcArgs::early_trigger).
+cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx &lc, bool allow_tc,
+                         bool early = false) {
   const gdn_config &c = ctx->cfg;
   if (allow_tc && ctx->tc_out_ok && use_tensor_cores(rows)) {
     TcGemm t = ctx->tc_out;
@@ -215,9 +232,11 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
     t.args.ts_b = c.act_scale_out;
     t.args.a_const = 1;
     t.args.sfa_tiled = ctx->w_out_sf_t;
+    t.args.a_tiles = g_tune.swizzled_tiles != 1 ? ctx->w_out_tiles : nullptr;
     t.args.sfb_tiled = ctx->y_scales;  // written tiled by the mixing stage (out_proj_tiled)
     t.args.status = ctx->status;
     t.split_k = split_for(g_tune.split_out, rows, 4);
+    t.args.early_trigger = early && g_tune.early_trigger != 1;
     return launch_tc_gemm(t, lc);
   }
   GemvArgs o{};
@@ -234,6 +253,9 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
   o.N = c.hidden;
   o.K = ctx->Vd;
   o.status = ctx->status;
+  // measured slower for the one-row GEMV chain (its weight prefetch then
+  // competes with the mixing kernel), so only on request
+  o.early_trigger = early && g_tune.early_trigger == 2 && rows <= 16;  // one launch, the step's last
   return run_gemv(o, lc, rows);
 }
 
@@ -298,6 +320,12 @@ gdn_status gdn_set_tuning(int knob, int value) {
     case 3:
       if (value < 0 || value > 2) return GDN_E_RANGE;
       g_tune.fused = value;
+      return GDN_OK;
+    case 4:
+    case 5:
+    case 6:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      (knob == 4 ? g_tune.in_quant_fused : knob == 5 ? g_tune.early_trigger : g_tune.swizzled_tiles) = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;
@@ -372,6 +400,8 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_scales, sf_tiled_bytes((int)prow, (int)Vd));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_in_sf_t, sf_tiled_bytes((int)Nin, (int)H));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_out_sf_t, sf_tiled_bytes((int)H, (int)Vd));
+  if (e == cudaSuccess && H % 256 == 0) e = ctx_alloc(ctx, &ctx->w_in_tiles, swizzled_tiles_bytes((int)Nin, (int)H));
+  if (e == cudaSuccess && Vd % 256 == 0) e = ctx_alloc(ctx, &ctx->w_out_tiles, swizzled_tiles_bytes((int)H, (int)Vd));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->status, 1);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->grid_bar, 4);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->conv_tmp, (c.conv_kernel - 1) * Cc);
@@ -406,6 +436,8 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->norm_w, w->norm_w, D * 4, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && H % 64 == 0) e = launch_tile_scales(ctx->w_in_scales, (int)Nin, (int)H, ctx->w_in_sf_t, s);
   if (e == cudaSuccess && Vd % 64 == 0) e = launch_tile_scales(ctx->w_out_scales, (int)H, (int)Vd, ctx->w_out_sf_t, s);
+  if (e == cudaSuccess && H % 256 == 0) e = launch_swizzle_tiles(ctx->w_in_codes, (int)Nin, (int)H, ctx->w_in_tiles, s);
+  if (e == cudaSuccess && Vd % 256 == 0) e = launch_swizzle_tiles(ctx->w_out_codes, (int)H, (int)Vd, ctx->w_out_tiles, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->status, 0, 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->grid_bar, 0, 16, s);
   if (e == cudaSuccess) {
@@ -531,7 +563,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   m.y_f32 = nullptr;
   e = launch_mix(m, lc);
   if (e != cudaSuccess) return cuda_status(e);
-  return cuda_status(run_out_proj(ctx, out, B, lc, true));
+  return cuda_status(run_out_proj(ctx, out, B, lc, true, true));
 }
 
 gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, const int32_t *slot_ids, int B,
@@ -541,7 +573,9 @@ gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, 
   if (!ba || !slot_ids) return GDN_E_NULL;
   if (!aligned16(ba) || !aligned16(slot_ids)) return GDN_E_ALIGN;
   if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
-  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, true};
+  // no programmatic launch: the mixing kernel reads the state before its
+  // griddepcontrol.wait, so it must not overlap a preceding decode step
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, false};
   MixArgs m = mix_args(ctx);
   m.qkvz = qkvz;
   m.ld_qkvz = ctx->Nqkvz;

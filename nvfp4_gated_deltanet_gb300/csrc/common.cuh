@@ -250,6 +250,10 @@ cudaError_t launch_quantize(const void *x, int x_is_f32, int rows, int cols, flo
                             int num_slots = 0, bool pdl = false, bool sf_tiled = false);
 // Repack row-major scales [rows][K/16] into the tiled layout (padding rows 0).
 cudaError_t launch_tile_scales(const uint8_t *src, int rows, int K, uint8_t *dst, cudaStream_t stream);
+// Repack row-major codes [rows][K/2] (K % 256 == 0) into pre-swizzled 16 KB
+// MMA tiles (TcArgs::a_tiles); swizzled_tiles_bytes gives the size.
+cudaError_t launch_swizzle_tiles(const uint8_t *src, int rows, int K, uint8_t *dst, cudaStream_t stream);
+inline size_t swizzled_tiles_bytes(int rows, int K) { return (size_t)((rows + 127) / 128) * (K / 256) * 16384; }
 
 // C[M][N] (ldc) = A_hat[M][K] * W_hat[N][K]^T. A is BF16 rows (quantised inside
 // with ts_a; a_rows_valid may mark rows to treat as zero) or NVFP4. Rows of W
@@ -269,6 +273,7 @@ struct GemvArgs {
   int ldc;
   int M, N, K;
   int32_t *status;
+  int early_trigger;  // as TcArgs::early_trigger
 };
 cudaError_t launch_gemv(const GemvArgs &a, const LaunchCtx &lc);
 
@@ -329,7 +334,24 @@ struct TcArgs {
   // Optional: both operands' scales already in the tiled layout tcgen05.cp
   // reads (sf_tiled_offset); then they are bulk-copied straight into place.
   const uint8_t *sfa_tiled, *sfb_tiled;
+  // Optional: the weight codes as pre-swizzled 16 KB tiles (launch_swizzle_tiles),
+  // streamed with one contiguous bulk copy per K tile instead of a tensor-map
+  // copy of 128 rows 1 KB apart.
+  const uint8_t *a_tiles;
   int32_t *status;
+  // Optional (decode rows, Nb <= 16): the B operand as BF16 rows [Nb][K],
+  // quantised to NVFP4 (tensor scale ts_b) inside the kernel straight into the
+  // MMA's shared-memory layout. Rows whose b_row_slot entry is not a valid slot
+  // (-1 = padding) read as zero. Needs a_const and sfa_tiled, and every K tile
+  // of a CTA resident at once (K / 256 / split <= the pipeline depth).
+  const uint16_t *b_bf16;
+  const int32_t *b_row_slot;
+  int b_num_slots;
+  // Signal dependents before waiting on the preceding kernel. Only for the last
+  // kernel of a decode step: the next step's first kernel reads nothing but
+  // weights until its own griddepcontrol.wait, which returns after this kernel
+  // (and so everything before it) has completed.
+  int early_trigger;
 };
 struct TcGemm {
   CUtensorMap mapA, mapSA;  // weights: codes [Ma][K/2] (128-byte swizzle), scales [Ma][K/16]

@@ -20,6 +20,11 @@
 // Split-K over a thread-block cluster of KS CTAs: ranks != 0 push their FP32
 // partial tile into rank 0's shared memory before one cluster barrier; rank 0
 // adds them in rank order (deterministic, no atomics).
+//
+// Decode form (b_bf16 set): the weight tiles of every K step of the CTA are
+// requested before griddepcontrol.wait, and warps 2..5 quantise the BF16
+// activation rows themselves, after the wait, into the swizzled B tiles and
+// the tiled scale atoms -- no separate quantisation kernel, no B loads.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cooperative_groups.h>
@@ -126,6 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB, TcArgs a) {
   using L = Layout<BN>;
+  // accumulators in tensor memory: one, or four for narrow tiles (columns
+  // 0 .. 4*BN-1; the scales start at column 128)
+  constexpr int kAcc = BN <= 32 ? 4 : 1;
+  static_assert(kAcc * BN <= 128, "accumulators overlap the scale columns");
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -135,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *sfready = full + S;
   uint64_t *empty = sfready + S;
   uint64_t *accum = empty + S;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(accum + 1);
+  uint64_t *bready = accum + 1;  // decode form: the quantised B tiles are in place
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bready + 1);
   auto stA = [&](int s) { return stage0 + (size_t)s * L::kStage; };
   auto stB = [&](int s) { return stA(s) + kATile; };
   auto stSA = [&](int s) { return stB(s) + L::kB; };
@@ -148,7 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nt = blockIdx.y;
   const int nkt = (a.K >> 8) / KS;
   const int kt0 = ks * nkt;
-  const bool tiled = a.sfa_tiled != nullptr && a.sfb_tiled != nullptr;
+  const bool bq = a.b_bf16 != nullptr;
+  const bool tiled = a.sfa_tiled != nullptr && (a.sfb_tiled != nullptr || bq);
+  if (a.early_trigger) pdl_launch_dependents();
+  if (bq && (BN != 16 || nkt > S || !a.sfa_tiled || !a.a_const)) {  // host-side contract broken: refuse, uniformly
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) flag_status(a.status, GDN_E_SHAPE);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -157,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty + s, 1);
     }
     mbar_init(accum, 1);
+    mbar_init(bready, 128);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -172,11 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint32_t bytes = tiled ? kATile + L::kB + 2 * 4 * kSFAtom : kATile + L::kB + 128 * 16 + BN * 16;
+      const uint32_t bytes = bq ? kATile + 4 * kSFAtom
+                           : tiled ? kATile + L::kB + 2 * 4 * kSFAtom : kATile + L::kB + 128 * 16 + BN * 16;
       const int ksteps = a.K >> 6;
       const int nsf = (nt * BN) >> 7;  // 128-row tile of the activation scales (BN < 128: one N tile)
       auto load_a = [&](int i, int s) {
-        tma_load_2d(stA(s), &tmA, (kt0 + i) * 128, mt * 128, full + s);
+        if (a.a_tiles)
+          bulk_g2s(stA(s), a.a_tiles + ((size_t)mt * (a.K >> 8) + kt0 + i) * kATile, kATile, full + s);
+        else
+          tma_load_2d(stA(s), &tmA, (kt0 + i) * 128, mt * 128, full + s);
         if (tiled)
           bulk_g2s(stAtA(s), a.sfa_tiled + ((size_t)mt * ksteps + (size_t)(kt0 + i) * 4) * kSFAtom, 4 * kSFAtom, full + s);
         else
@@ -194,9 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(full + i, bytes);
         load_a(i, i);
       }
-      pdl_wait();
-      pdl_launch_dependents();
-      for (int i = 0; i < pre; ++i) load_b(i, i);
+      if (!bq) {
+        pdl_wait();
+        if (!a.early_trigger) pdl_launch_dependents();
+      }
+      for (int i = 0; i < (bq ? 0 : pre); ++i) load_b(i, i);
       for (int i = pre; i < nkt; ++i) {
         const int s = i % S, u = i / S;
         if (u > 0 && !mbar_wait(empty + s, (uint32_t)((u - 1) & 1))) { ok = false; break; }
@@ -209,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_nvf4<BN>();
-      for (int i = 0; i < nkt; ++i) {
+      if (bq && !mbar_wait(bready, 0)) ok = false;
+      for (int i = 0; i < (ok ? nkt : 0); ++i) {
         const int s = i % S, u = i / S;
         if (!mbar_wait(full + s, (uint32_t)(u & 1)) || (!tiled && !mbar_wait(sfready + s, (uint32_t)(u & 1)))) {
           ok = false;
@@ -224,15 +248,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint64_t ad = desc_sw128(smem_u32(stA(s))), bd = desc_sw128(smem_u32(stB(s)));
 #pragma unroll
-        for (int j = 0; j < 4; ++j)  // K = 64 per MMA: 32 bytes further along the swizzled rows
-          tc_mma_nvf4(tmem, ad + 2 * j, bd + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j, (i | j) != 0);
+        for (int j = 0; j < 4; ++j) {  // K = 64 per MMA: 32 bytes further along the swizzled rows
+          // narrow tiles rotate over kAcc accumulators so consecutive MMAs do
+          // not wait on each other's result; the epilogue adds them in order
+          const int step = i * 4 + j, acc = step % kAcc;
+          tc_mma_nvf4(tmem + acc * BN, ad + 2 * j, bd + 2 * j, idesc, sfa + 4 * j, sfb + 4 * j, step >= kAcc);
+        }
         tc_commit(empty + s);
       }
       tc_commit(accum);
     }
   } else {
-    // ------------------------------------------------ scale rearrangement
     const int t = threadIdx.x - 64;  // 0..127
+    // ------------------------------------------------ decode form: quantise B
+    if constexpr (BN == 16) if (bq) {
+      pdl_wait();  // the activation rows come from the preceding kernel
+      if (t == 0 && !a.early_trigger) pdl_launch_dependents();
+      const float inv6ts = inv6ts_of(a.ts_b);
+      bool finite = true;
+      // one 32-element piece (two 16-blocks, 16 code bytes) per item: 8 per
+      // row of a 256-wide K tile; consecutive threads walk along a row. All
+      // of a thread's loads are issued before any quantisation (no load waits
+      // behind another), rows' liveness comes from one slot lookup per row.
+      // (x rows of padding slots exist in memory: they are read, then dropped)
+      constexpr int kMaxItems = (4 * BN * 8 + 127) / 128;
+      const int nitems = nkt * BN * 8;
+      uint4 xv[kMaxItems][4];
+      int slot[kMaxItems];
+#pragma unroll
+      for (int j = 0; j < kMaxItems; ++j) {
+        const int idx = t + j * 128;
+        const int i = idx / (BN * 8), r = (idx >> 3) % BN, c = idx & 7;
+        const int n = nt * BN + r;
+        const bool in = idx < nitems && n < a.Nb;
+        slot[j] = in ? (a.b_row_slot ? a.b_row_slot[n] : 0) : -1;
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.b_bf16 + (size_t)n * a.K + (size_t)(kt0 + i) * 256 + c * 32);
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) xv[j][q2] = in ? src[q2] : make_uint4(0, 0, 0, 0);
+      }
+      bool live[kMaxItems];
+#pragma unroll
+      for (int j = 0; j < kMaxItems; ++j)
+        live[j] = slot[j] >= 0 && (a.b_row_slot == nullptr || slot[j] < a.b_num_slots);
+#pragma unroll
+      for (int j = 0; j < kMaxItems; ++j) {
+        const int idx = t + j * 128;
+        if (idx >= nitems) break;
+        const int i = idx / (BN * 8), r = (idx >> 3) % BN, c = idx & 7;
+        uint32_t lo[2] = {0, 0}, hi[2] = {0, 0}, sc[2] = {0, 0};
+        if (live[j]) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float v[16];
+#pragma unroll
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const uint4 w4 = xv[j][half * 2 + q2];
+              const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                v[8 * q2 + 2 * k] = __uint_as_float(w[k] << 16);
+                v[8 * q2 + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+              }
+            }
+            finite &= quant_block16(v, a.ts_b, inv6ts, lo[half], hi[half], sc[half]);
+          }
+        }
+        // codes: row r of the tile is 128 bytes, its 16-byte chunks swizzled by r % 8
+        *reinterpret_cast<uint4 *>(stB(i) + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(lo[0], hi[0], lo[1], hi[1]);
+        // scales: blocks 2c, 2c+1 of the tile = K step c/2, blocks (2c)%4, (2c)%4+1
+        *reinterpret_cast<uint16_t *>(stAtB(i) + (c >> 1) * kSFAtom + (r & 31) * 16 + ((r & 127) >> 5) * 4 + ((2 * c) & 3)) =
+            (uint16_t)(sc[0] | (sc[1] << 8));
+      }
+      if (!finite && blockIdx.x == 0) flag_status(a.status, GDN_E_NONFINITE);
+      fence_async_shared();  // generic-proxy writes -> visible to tcgen05.mma / tcgen05.cp
+      mbar_arrive(bready);
+    }
+    // ------------------------------------------------ scale rearrangement
     for (int i = 0; i < (tiled ? 0 : nkt); ++i) {
       const int s = i % S, u = i / S;
       if (!mbar_wait(full + s, (uint32_t)(u & 1))) { ok = false; break; }
@@ -261,11 +352,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + c0, r);
-        tmem_ld_wait();
+        float part4[kAcc][16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) acc[c0 + c] = __uint_as_float(r[c]);
+        for (int p = 0; p < kAcc; ++p) {
+          uint32_t r[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + p * BN + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) part4[p][c] = __uint_as_float(r[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float v = part4[0][c];
+          if (kAcc == 4) v = (part4[0][c] + part4[1][c]) + (part4[2][c] + part4[3][c]);
+          acc[c0 + c] = v;
+        }
       }
     } else {
       ok = false;
@@ -365,14 +466,15 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t row_bytes
 
 template <int BN, int KS, int S>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)S * Layout<BN>::kStage + (KS > 1 ? (size_t)(KS - 1) * 128 * BN * 4 : 0) + (3 * S + 1) * 8 + 16;
+  return 1024 + (size_t)S * Layout<BN>::kStage + (KS > 1 ? (size_t)(KS - 1) * 128 * BN * 4 : 0) + (3 * S + 2) * 8 + 16;
 }
 
 template <int BN, int KS, int S>
 cudaError_t launch_t(const TcGemm &g, const LaunchCtx &lc) {
-  CUtensorMap mB, mSB;
-  if (!make_map(&mB, g.b_codes, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 2, BN, 128, true) ||
-      !make_map(&mSB, g.b_scales, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 16, BN, 16, false))
+  CUtensorMap mB = g.mapA, mSB = g.mapSA;  // decode form: never read
+  if (!g.args.b_bf16 &&
+      (!make_map(&mB, g.b_codes, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 2, BN, 128, true) ||
+       !make_map(&mSB, g.b_scales, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 16, BN, 16, false)))
     return cudaErrorInvalidValue;
   size_t smem = smem_bytes<BN, KS, S>();
   if (smem < 80 * 1024) smem = 80 * 1024;  // at most two CTAs (2 x 256 TMEM columns) per SM
@@ -441,6 +543,11 @@ cudaError_t launch_tc_gemm(const TcGemm &g, const LaunchCtx &lc) {
   const int n_tiles = (a.Nb + bn - 1) / bn;
   int ks = g.split_k > 0 ? g.split_k : tc_pick_split(m_tiles, n_tiles, a.K, lc.num_sms);
   while (ks > 1 && (a.K / 256) % ks) ks >>= 1;  // the split must divide the K tiles
+  if (a.b_bf16) {  // decode form: at most 16 rows, every K tile of a CTA in its own stage
+    if (bn != 16 || !a.a_const || !a.sfa_tiled) return cudaErrorInvalidValue;
+    while (ks < 8 && (a.K / 256) / ks > 4) ks *= 2;
+    if ((a.K / 256) % ks || (a.K / 256) / ks > 4) return cudaErrorInvalidValue;
+  }
   switch (bn) {
     case 16: return launch_bn<16>(g, ks, lc);
     case 32: return launch_bn<32>(g, ks, lc);

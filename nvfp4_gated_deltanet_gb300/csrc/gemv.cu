@@ -29,6 +29,7 @@ constexpr int kBarBytes = kWarps * kMaxStages * 8;  // mbarriers, 256 bytes
 template <int MB, bool TMA>
 __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a, int rows_per_warp, int stages) {
   extern __shared__ __align__(128) unsigned char smem[];
+  if (a.early_trigger) pdl_launch_dependents();
   const int K = a.K, npiece = K >> 5;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t cbytes = (size_t)K >> 1, sbytes = (size_t)K >> 4;  // per weight row
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a, int rows_
     }
   }
   __syncthreads();
-  pdl_launch_dependents();
+  if (!a.early_trigger) pdl_launch_dependents();
 
   constexpr int NV = 2 * MB;
   bool ok = true;

@@ -90,4 +90,28 @@ cudaError_t launch_tile_scales(const uint8_t *src, int rows, int K, uint8_t *dst
   return cudaGetLastError();
 }
 
+// Codes [rows][K/2] -> 16 KB tiles of 128 rows x 128 bytes (256 values),
+// tile (mt, kt) at ((mt * K/256) + kt) * 16 KB, each already in the 128-byte
+// swizzled order the MMA's shared-memory descriptor expects: row r's 16-byte
+// chunk c sits at r * 128 + ((c ^ (r % 8)) * 16). Rows past the end are zero.
+__global__ void swizzle_tiles_kernel(const uint8_t *src, int rows, int K, uint8_t *dst) {
+  const int nkt = K / 256;
+  const size_t nchunks = (size_t)(rows + 127) / 128 * nkt * 1024;  // 16-byte chunks
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nchunks; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t tile = i >> 10;
+    const int within = (int)(i & 1023), r = within >> 3, pos = within & 7;
+    const int mt = (int)(tile / nkt), kt = (int)(tile % nkt);
+    const int row = mt * 128 + r, c = pos ^ (r & 7);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row < rows) v = *reinterpret_cast<const uint4 *>(src + (size_t)row * (K / 2) + kt * 128 + c * 16);
+    *reinterpret_cast<uint4 *>(dst + i * 16) = v;
+  }
+}
+
+cudaError_t launch_swizzle_tiles(const uint8_t *src, int rows, int K, uint8_t *dst, cudaStream_t stream) {
+  if (K % 256) return cudaErrorInvalidValue;
+  swizzle_tiles_kernel<<<304, 256, 0, stream>>>(src, rows, K, dst);
+  return cudaGetLastError();
+}
+
 }  // namespace gdn

@@ -168,3 +168,47 @@ def test_fused_single_kernel_step_matches_oracle(api):
             assert rel_l2(_bf16(to_host(conv_d)), _bf16(c)) <= 4e-3
     finally:
         api.lib().gdn_set_tuning(3, 0)
+
+
+@pytest.mark.parametrize("shape_name,B", [("TINY", 3), ("FULL", 1), ("FULL", 7), ("FULL", 16)])
+def test_in_projection_quantising_inside_the_gemm(api, shape_name, B):
+    """Tensor-core decode (knob 0 = 2): the in-projection GEMM that quantises
+    x itself (knob 4 = 2) gives bit-identical outputs and states to a separate
+    quantisation kernel followed by the GEMM (knob 4 = 1) -- the same block
+    quantiser, the same MMA order -- and so do weights streamed from the
+    pre-swizzled tile copy (knob 6 = 2) or by tensor-map copies (knob 6 = 1);
+    with one padding row, and matching the oracle."""
+    shape = getattr(synth, shape_name)
+    seed = 0 if shape_name == "TINY" else 1
+    L = _layer(api, shape_name, seed)
+    O = oracle_layer(shape_name, seed)
+    slots = list(range(B))
+    if B > 1:
+        slots[1] = -1                                   # a padding row
+    x, conv0, ssm0 = slot_inputs(shape, list(range(B)), 2)
+    ids = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    res = {}
+    api.lib().gdn_set_tuning(0, 2)
+    try:
+        for knob in ((1, 1), (2, 1), (1, 2), (2, 2)):
+            api.lib().gdn_set_tuning(4, knob[0])
+            api.lib().gdn_set_tuning(6, knob[1])
+            c, s = to_dev(conv0), to_dev(ssm0)
+            outs = [to_host(L.decode_step(to_dev(x[t]), ids, c, s)) for t in range(2)]
+            assert L.check() == 0
+            res[knob] = (np.stack(outs), to_host(c), to_host(s))
+    finally:
+        for k in (0, 4, 6):
+            api.lib().gdn_set_tuning(k, 0)
+    for knob in ((2, 1), (1, 2), (2, 2)):
+        for a, b in zip(res[(1, 1)], res[knob]):
+            np.testing.assert_array_equal(a, b)
+    got, conv_g, ssm_g = res[(2, 2)]
+    c, s = conv0.copy(), ssm0.copy()
+    want = np.stack([O.decode_step(x[t], slots, c, s) for t in range(2)])
+    assert rel_l2(_bf16(got), _bf16(want)) <= 4e-3
+    assert rel_l2(ssm_g, s) <= 1e-4
+    assert rel_l2(_bf16(conv_g), _bf16(c)) <= 4e-3
+    if B > 1:
+        assert not got[:, 1].any()                      # padding row: zero output
+        np.testing.assert_array_equal(ssm_g[1], ssm0[1])  # and its slot untouched
