@@ -213,7 +213,9 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * knob 6: tensor-core projections of a context stream the weight codes from a
  * pre-swizzled copy made at gdn_create, one contiguous 16 KB bulk copy per
  * 128 x 256 tile (0 and 2 = yes, the default; 1 = tensor-map copies from the
- * row-major codes).
+ * row-major codes). knob 7: d_v slices per head in the decode mixing kernel
+ * (0 = chosen from the batch, the default; 1, 2 or 4, reduced while the
+ * cluster of a key head would exceed 8 CTAs).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

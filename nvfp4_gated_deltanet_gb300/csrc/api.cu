@@ -54,6 +54,7 @@ struct Tuning {
   int early_trigger = 0;   // out-projection of a decode step signals the next kernel early: 0 auto (tensor-core
                            // out-projection only), 1 off, 2 on
   int swizzled_tiles = 0;  // tensor-core weights from the pre-swizzled tile copy: 0 auto (on), 1 off, 2 on
+  int mix_slices = 0;      // d_v slices per head in the mixing kernel: 0 auto, 1, 2, 4
 };
 Tuning g_tune;
 
@@ -147,6 +148,7 @@ MixArgs mix_args(gdn_ctx *c) {
   m.rms_eps = c->cfg.rms_eps;
   m.ts_out = c->cfg.act_scale_out;
   m.status = c->status;
+  m.slices = g_tune.mix_slices;
   return m;
 }
 
@@ -326,6 +328,10 @@ gdn_status gdn_set_tuning(int knob, int value) {
     case 6:
       if (value < 0 || value > 2) return GDN_E_RANGE;
       (knob == 4 ? g_tune.in_quant_fused : knob == 5 ? g_tune.early_trigger : g_tune.swizzled_tiles) = value;
+      return GDN_OK;
+    case 7:
+      if (value != 0 && value != 1 && value != 2 && value != 4) return GDN_E_RANGE;
+      g_tune.mix_slices = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;

@@ -295,6 +295,7 @@ struct MixArgs {
   int y_sf_tiled;
   float *y_f32;       // [B][Hv*dv] or null
   int32_t *status;
+  int slices;         // d_v slices per head (1, 2, 4), 0 = chosen from B
 };
 cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc);
 

@@ -28,11 +28,18 @@ namespace gdn {
 
 namespace {
 
-constexpr int kRPW = 8;  // state rows per warp
+// State rows per warp: 8, or 16 when one CTA holds a whole head (the
+// per-warp work that does not scale with rows -- q/k norms, gates, the conv
+// share -- is then spread over twice the state). The row dot products reduce
+// over the lanes in the same butterfly order either way, so the results do
+// not depend on it.
+template <int NS>
+__host__ __device__ constexpr int rows_per_warp() { return NS == 1 ? 16 : 8; }
 
 
 template <int D, int NS>
-__global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
+__global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ? 2 : 1) mix_kernel(MixArgs a) {
+  constexpr int kRPW = rows_per_warp<NS>();
   constexpr int R = D / NS;
   constexpr int WARPS = R / kRPW;
   constexpr int THREADS = WARPS * 32;
@@ -78,9 +85,10 @@ __global__ void __launch_bounds__((D / NS / kRPW) * 32) mix_kernel(MixArgs a) {
   const int slot = a.slot_ids[b];
   bool live = slot >= 0 && slot < a.num_slots;
   bool bad = slot < -1 || slot >= a.num_slots;
-  if (live) {
-    for (int j = 0; j < a.B; ++j)
-      if (j != b && a.slot_ids[j] == slot) { bad = true; live = false; }
+  if (live) {  // a slot used by two rows: refuse both (each warp checks, B/32 loads per lane)
+    bool dup = false;
+    for (int j = lane; j < a.B; j += 32) dup |= (j != b && a.slot_ids[j] == slot);
+    if (__any_sync(0xffffffffu, dup)) { bad = true; live = false; }
   }
   // state: conv taps and this warp's rows of S
   uint16_t *cst = a.conv_state + (size_t)(live ? slot : 0) * (Kc - 1) * C;
@@ -283,7 +291,7 @@ cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
   const int G = a.Hv / a.Hk;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.Hv * NS, a.B, 1);
-  cfg.blockDim = dim3((D / NS / kRPW) * 32, 1, 1);
+  cfg.blockDim = dim3((D / NS / rows_per_warp<NS>()) * 32, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = lc.stream;
   cudaLaunchAttribute attr[2];
@@ -302,10 +310,12 @@ cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
 
 // Slices per head: more CTAs when the batch is small (the state traffic of one
 // row is spread over more SMs), bounded by the portable cluster size 8.
+// Measured on GB300 (us per layer-step): c4 20.5 with 2 slices vs 22.4 with
+// one; c8 24.5 with one vs 26.1 with two; batch 64 and 256 best with one.
 cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc) {
   if (a.B <= 0) return cudaSuccess;
   const int G = a.Hv / a.Hk;
-  int ns = a.B <= 2 ? 4 : (a.B <= 8 ? 2 : 1);
+  int ns = a.slices > 0 ? a.slices : (a.B <= 2 ? 4 : (a.B <= 4 ? 2 : 1));
   while (ns > 1 && G * ns > 8) ns >>= 1;
   if (G > 8) return cudaErrorInvalidValue;
   switch (a.D) {
