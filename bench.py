@@ -37,8 +37,24 @@ SEQ_BYTES = 4_194_304 + 98_304 + 4_096 + 4_096                       # 4,300,800
 GEMV_IN_BYTES = 12352 * (1024 + 128)                                  # qkvz+ba codes+scales
 
 
-def step_bytes(B: int) -> int:
-    return W_BYTES + B * SEQ_BYTES
+def layer_bytes(sh):
+    """(weight bytes, bytes per active sequence) of one decode layer-step of shape sh:
+    NVFP4 codes + E4M3 scales of the three projections, conv taps (BF16), A_log and
+    dt_bias, the norm weight; per sequence the FP32 state and BF16 conv state read
+    and written, x in and out."""
+    nvfp4 = lambda rows, k: rows * (k // 2 + k // 16)
+    w = (nvfp4(sh.qkvz_out, sh.hidden) + nvfp4(sh.ba_out, sh.hidden) + nvfp4(sh.hidden, sh.value_dim)
+         + sh.conv_channels * sh.conv_kernel * 2 + sh.n_v_heads * 8 + sh.d_v * 4)
+    seq = (2 * sh.n_v_heads * sh.d_v * sh.d_k * 4 + 2 * (sh.conv_kernel - 1) * sh.conv_channels * 2
+           + 2 * sh.hidden * 2)
+    return w, seq
+
+
+def step_bytes(B: int, sh=None) -> int:
+    if sh is None:
+        return W_BYTES + B * SEQ_BYTES
+    w, seq = layer_bytes(sh)
+    return w + B * seq
 
 
 def peaks():
@@ -103,16 +119,17 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def make_stack(pkg, synth, n_layers, B, max_batch, device="cuda"):
+def make_stack(pkg, synth, n_layers, B, max_batch, device="cuda", shape=None):
     """n_layers layer contexts sharing one synthetic weight set (uploaded once
     per context, so each has its own copy in HBM), each with B slots of state."""
     import numpy as np
     import torch
-    w = synth.layer_weights(synth.FULL, 1)
+    sh = shape or synth.FULL
+    w = synth.layer_weights(sh, 1)
     layers, states = [], []
-    conv0 = np.stack([synth.conv_state(synth.FULL, synth.slot_seed(s)) for s in range(B)])
-    ssm0 = np.stack([synth.ssm_state(synth.FULL, synth.slot_seed(s)) for s in range(B)])
-    x = np.stack([synth.x_tokens(synth.FULL, synth.slot_seed(s), 1)[0] for s in range(B)])
+    conv0 = np.stack([synth.conv_state(sh, synth.slot_seed(s)) for s in range(B)])
+    ssm0 = np.stack([synth.ssm_state(sh, synth.slot_seed(s)) for s in range(B)])
+    x = np.stack([synth.x_tokens(sh, synth.slot_seed(s), 1)[0] for s in range(B)])
     xd = torch.from_numpy(x.view(np.int16)).to(device)
     for _ in range(n_layers):
         L = pkg.layer_from_synth(w, max_batch=max_batch)
@@ -375,6 +392,20 @@ def main():
         extra["c1"] = {"us_per_layer_step": round(us_layer, 3), "hbm_gbs": round(gbs_step, 1),
                        "frac_of_peak": round(gbs_step / hbm_peak, 4)}
         del layers, states
+        torch.cuda.empty_cache()
+        # the two-way head-parallel slice (8 key / 16 value heads), benched the same way
+        tp = synth.TP2
+        n_tp = max(4, -(-4 * l2 // step_bytes(1, tp)) + 1)
+        _, tl, ts, tx = make_stack(pkg, synth, n_tp, 16, 16, shape=tp)
+        for B in (1, 2, 4, 8, 16):
+            gB, _ = capture_stack(tl, ts, tx, B)
+            usB = time_graph(gB, max(10, args.steps // 4), 3) * 1e3 / n_tp
+            gbsB = step_bytes(B, tp) / (usB * 1e-6) / 1e9
+            extra[f"tp2_c{B}"] = {"us_per_layer_step": round(usB, 3), "hbm_gbs": round(gbsB, 1),
+                                  "frac_of_peak": round(gbsB / hbm_peak, 4), "layers": n_tp,
+                                  "shape": "H2048 Hk8 Hv16 d128 K4 (one rank of two-way head parallelism)"}
+            del gB
+        del tl, ts
         torch.cuda.empty_cache()
         for B in (64, 128, 256):
             extra[f"batch{B}"] = time_batch(pkg, synth, B, hbm_peak)

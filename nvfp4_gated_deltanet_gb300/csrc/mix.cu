@@ -38,7 +38,7 @@ __host__ __device__ constexpr int rows_per_warp() { return NS == 1 ? 16 : 8; }
 
 
 template <int D, int NS>
-__global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ? 2 : 1) mix_kernel(MixArgs a) {
+__global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ? 2 : 0) mix_kernel(MixArgs a) {
   constexpr int kRPW = rows_per_warp<NS>();
   constexpr int R = D / NS;
   constexpr int WARPS = R / kRPW;

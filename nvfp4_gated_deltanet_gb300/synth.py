@@ -75,6 +75,10 @@ class LayerShape:
 
 TINY = LayerShape(hidden=256, n_k_heads=2, n_v_heads=4, d_k=32, d_v=32)
 FULL = LayerShape(hidden=2048, n_k_heads=16, n_v_heads=32, d_k=128, d_v=128)
+# One rank's slice of the full layer under two-way head-parallel serving
+# (half the key and value heads; hidden unchanged, out_proj keeps half its
+# input columns): the shape the pages' GB10 decode table was measured on.
+TP2 = LayerShape(hidden=2048, n_k_heads=8, n_v_heads=16, d_k=128, d_v=128)
 
 
 def rng(seed: int, name: str) -> np.random.Generator:
