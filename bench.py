@@ -306,6 +306,24 @@ def reference_arm(args):
     return 0
 
 
+def single_case(args):
+    """One workload alone (prefill of T tokens, or one large-batch decode
+    layer-step), for profiling runs: a JSON line with its time."""
+    import torch
+    import nvfp4_gated_deltanet_gb300 as pkg
+    from nvfp4_gated_deltanet_gb300 import synth
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    hbm_peak, _ = peaks()
+    if args.case == "prefill":
+        r = time_prefill(pkg, synth, args.T, reps=args.steps)
+        line = {"case": f"prefill{args.T}", **r}
+    else:
+        r = time_batch(pkg, synth, args.batch, hbm_peak, steps=args.steps)
+        line = {"case": f"batch{args.batch}", **r}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -315,10 +333,17 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="layer instances in the stack (0: > 4x L2)")
     ap.add_argument("--no-extra", action="store_true", help="skip the c2..c16 / batch / prefill extras")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--case", default="decode", choices=["decode", "prefill", "batch"],
+                    help="decode: the headline (default); prefill / batch: only that workload, one JSON line "
+                         "(for profiling)")
+    ap.add_argument("--T", type=int, default=4096, help="prompt length for --case prefill")
+    ap.add_argument("--batch", type=int, default=256, help="rows for --case batch")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return reference_arm(args)
+    if args.case != "decode":
+        return single_case(args)
 
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
