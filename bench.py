@@ -35,6 +35,9 @@ UNIT = "us/step"
 W_BYTES = 14_155_776 + 73_728 + 4_718_592 + 65_536 + 256 + 512      # 19,014,400
 SEQ_BYTES = 4_194_304 + 98_304 + 4_096 + 4_096                       # 4,300,800
 GEMV_IN_BYTES = 12352 * (1024 + 128)                                  # qkvz+ba codes+scales
+# dram__bytes_read.sum + dram__bytes_write.sum of one in-projection GEMV launch
+# (ncu --set full capture of the decode c1 stack; summary in profiles/)
+GEMV_IN_TRAFFIC = 14_260_480
 
 
 def layer_bytes(sh):
@@ -452,7 +455,7 @@ def main():
         "hbm_gbs_step": round(gbs_step, 1), "hbm_frac_step": round(gbs_step / hbm_peak, 4),
         "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1,1> (W4A4 qkvz+ba projection on CUDA cores, 1 row)",
                      "achieved": round(gemv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gemv_gbs / hbm_peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "frac": round(gemv_gbs / hbm_peak, 4), "peak_kind": peak_kind, "traffic": GEMV_IN_TRAFFIC,
                      "us_per_launch": round(us_gemv, 3), "bytes_per_launch": GEMV_IN_BYTES},
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(xh.numel() * 2),
                 "d2h_bytes_per_step": int(oh.numel() * 2),
