@@ -40,7 +40,7 @@ GEMV_IN_BYTES = 12352 * (1024 + 128)                                  # qkvz+ba 
 GEMV_IN_TRAFFIC = 14_260_480
 
 
-def layer_bytes(sh):
+def layer_bytes(sh, state_bf16=False):
     """(weight bytes, bytes per active sequence) of one decode layer-step of shape sh:
     NVFP4 codes + E4M3 scales of the three projections, conv taps (BF16), A_log and
     dt_bias, the norm weight; per sequence the FP32 state and BF16 conv state read
@@ -48,15 +48,16 @@ def layer_bytes(sh):
     nvfp4 = lambda rows, k: rows * (k // 2 + k // 16)
     w = (nvfp4(sh.qkvz_out, sh.hidden) + nvfp4(sh.ba_out, sh.hidden) + nvfp4(sh.hidden, sh.value_dim)
          + sh.conv_channels * sh.conv_kernel * 2 + sh.n_v_heads * 8 + sh.d_v * 4)
-    seq = (2 * sh.n_v_heads * sh.d_v * sh.d_k * 4 + 2 * (sh.conv_kernel - 1) * sh.conv_channels * 2
+    seq = (2 * sh.n_v_heads * sh.d_v * sh.d_k * (2 if state_bf16 else 4) + 2 * (sh.conv_kernel - 1) * sh.conv_channels * 2
            + 2 * sh.hidden * 2)
     return w, seq
 
 
-def step_bytes(B: int, sh=None) -> int:
-    if sh is None:
+def step_bytes(B: int, sh=None, state_bf16=False) -> int:
+    if sh is None and not state_bf16:
         return W_BYTES + B * SEQ_BYTES
-    w, seq = layer_bytes(sh)
+    from nvfp4_gated_deltanet_gb300 import synth
+    w, seq = layer_bytes(sh or synth.FULL, state_bf16)
     return w + B * seq
 
 
@@ -122,7 +123,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def make_stack(pkg, synth, n_layers, B, max_batch, device="cuda", shape=None):
+def make_stack(pkg, synth, n_layers, B, max_batch, device="cuda", shape=None, state_bf16=False):
     """n_layers layer contexts sharing one synthetic weight set (uploaded once
     per context, so each has its own copy in HBM), each with B slots of state."""
     import numpy as np
@@ -135,9 +136,12 @@ def make_stack(pkg, synth, n_layers, B, max_batch, device="cuda", shape=None):
     x = np.stack([synth.x_tokens(sh, synth.slot_seed(s), 1)[0] for s in range(B)])
     xd = torch.from_numpy(x.view(np.int16)).to(device)
     for _ in range(n_layers):
-        L = pkg.layer_from_synth(w, max_batch=max_batch)
+        L = pkg.layer_from_synth(w, max_batch=max_batch, state_bf16=state_bf16)
         layers.append(L)
-        states.append((torch.from_numpy(conv0.view(np.int16)).to(device), torch.from_numpy(ssm0).to(device)))
+        ssm = torch.from_numpy(ssm0).to(device)
+        if state_bf16:   # the same values stored as BF16 bits (round to nearest even)
+            ssm = ssm.to(torch.bfloat16).view(torch.int16)
+        states.append((torch.from_numpy(conv0.view(np.int16)).to(device), ssm))
     return w, layers, states, xd
 
 
@@ -207,19 +211,19 @@ def time_gemv(pkg, layers, xcodes, xscales, steps):
     return ms / len(mats) * 1e3, len(mats)  # us per launch
 
 
-def time_batch(pkg, synth, B, hbm_peak, n_layers=2, steps=10):
+def time_batch(pkg, synth, B, hbm_peak, n_layers=2, steps=10, state_bf16=False):
     """Large-batch decode: B sequences per step through n_layers layer instances
     (each layer-step moves > 300 MB, far beyond L2)."""
-    w, layers, states, xd = make_stack_b(pkg, synth, n_layers, B)
+    w, layers, states, xd = make_stack_b(pkg, synth, n_layers, B, state_bf16=state_bf16)
     g, _ = capture_stack(layers, states, xd, B)
     ms = time_graph(g, steps, 3)
     us = ms * 1e3 / n_layers
-    gbs = step_bytes(B) / (us * 1e-6) / 1e9
+    gbs = step_bytes(B, state_bf16=state_bf16) / (us * 1e-6) / 1e9
     return {"us_per_layer_step": round(us, 2), "tokens_per_s": round(B / (us * 1e-6)), "hbm_gbs": round(gbs, 1),
             "frac_of_peak": round(gbs / hbm_peak, 4)}
 
 
-def make_stack_b(pkg, synth, n_layers, B, device="cuda"):
+def make_stack_b(pkg, synth, n_layers, B, device="cuda", state_bf16=False):
     import numpy as np
     import torch
     w = synth.layer_weights(synth.FULL, 1)
@@ -227,11 +231,13 @@ def make_stack_b(pkg, synth, n_layers, B, device="cuda"):
     xd = torch.from_numpy(x.view(np.int16)).to(device)
     layers, states = [], []
     for _ in range(n_layers):
-        L = pkg.layer_from_synth(w, max_batch=B)
+        L = pkg.layer_from_synth(w, max_batch=B, state_bf16=state_bf16)
         conv = torch.empty(B, 3, synth.FULL.conv_channels, dtype=torch.int16, device=device)
         ssm = torch.empty(B, synth.FULL.n_v_heads, 128, 128, dtype=torch.float32, device=device)
         conv.copy_(torch.from_numpy(synth.conv_state(synth.FULL, 100).view(np.int16)).to(device).expand_as(conv))
         ssm.copy_(torch.from_numpy(synth.ssm_state(synth.FULL, 100)).to(device).expand_as(ssm))
+        if state_bf16:
+            ssm = ssm.to(torch.bfloat16).view(torch.int16)
         layers.append(L)
         states.append((conv, ssm))
     return w, layers, states, xd
@@ -435,9 +441,22 @@ def main():
             del gB
         del tl, ts
         torch.cuda.empty_cache()
+        # BF16-stored recurrent state: same kernels, half the state bytes
+        _, bl, bs, bx = make_stack(pkg, synth, n_layers, 16, 16, state_bf16=True)
+        for B in (1, 4, 16):
+            gB, _ = capture_stack(bl, bs, bx, B)
+            usB = time_graph(gB, max(10, args.steps // 4), 3) * 1e3 / n_layers
+            gbsB = step_bytes(B, state_bf16=True) / (usB * 1e-6) / 1e9
+            extra[f"bf16state_c{B}"] = {"us_per_layer_step": round(usB, 3), "hbm_gbs": round(gbsB, 1),
+                                        "frac_of_peak": round(gbsB / hbm_peak, 4)}
+            del gB
+        del bl, bs
+        torch.cuda.empty_cache()
         for B in (64, 128, 256):
             extra[f"batch{B}"] = time_batch(pkg, synth, B, hbm_peak)
             torch.cuda.empty_cache()
+        extra["bf16state_batch256"] = time_batch(pkg, synth, 256, hbm_peak, state_bf16=True)
+        torch.cuda.empty_cache()
         for T in (1024, 4096, 16384):
             extra[f"prefill{T}"] = time_prefill(pkg, synth, T)
             torch.cuda.empty_cache()

@@ -70,6 +70,13 @@ typedef struct {
   float l2_eps;           /* q/k L2-norm epsilon (inside the square root) */
   float act_scale_in;     /* FP32 tensor scale of the x quantiser, > 0 */
   float act_scale_out;    /* FP32 tensor scale of the gated-norm output quantiser, > 0 */
+  int state_bf16;         /* recurrent state storage: 0 = FP32; 1 = BF16 (same layout, 2-byte
+                             elements). The arithmetic stays FP32: a decode step loads the
+                             BF16 state, updates it in FP32 and stores it rounded to nearest
+                             even; a prefill call carries it in FP32 from its first token to
+                             its last and rounds once at the end. Halves the dominant
+                             per-sequence bytes (Rocket blog, "KDA state tile": BF16 state
+                             storage measured beside FP32). */
 } gdn_config;
 
 /* One NVFP4 matrix W[rows][cols]: codes [rows][cols/2], scales [rows][cols/16]
@@ -139,7 +146,8 @@ gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int 
  *   out:        BF16 [B][H]
  *   conv_state: BF16 [num_slots][conv_kernel-1][C], the last conv_kernel-1 raw
  *               inputs of every channel, oldest first; updated in place
- *   ssm_state:  FP32 [num_slots][Hv][d_v][d_k]; updated in place
+ *   ssm_state:  FP32 [num_slots][Hv][d_v][d_k], or BF16 bits of the same shape when
+ *               the config's state_bf16 is set; updated in place
  * Per active row: x -> NVFP4(act_scale_in) -> W4A4 qkvz/ba -> BF16; conv + SiLU;
  * q,k L2-normalised (q also scaled by d_k^-1/2); beta = sigmoid(b),
  * g = -exp(A_log) * softplus(a + dt_bias); per value head S <- exp(g) S,
@@ -148,7 +156,7 @@ gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int 
  * Errors: GDN_E_NULL, GDN_E_SHAPE (B < 1 or > max_batch, num_slots < 1),
  * GDN_E_ALIGN, GDN_E_OVERFLOW, GDN_E_CUDA. */
 gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B,
-                           uint16_t *out, uint16_t *conv_state, float *ssm_state, int num_slots,
+                           uint16_t *out, uint16_t *conv_state, void *ssm_state, int num_slots,
                            void *stream);
 
 /* The token-mixing stage of gdn_decode_step alone, for stage-wise checks and
@@ -158,7 +166,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
  * ssm_state as in gdn_decode_step, updated in place. Same errors. */
 gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba,
                         const int32_t *slot_ids, int B, float *y, uint16_t *conv_state,
-                        float *ssm_state, int num_slots, void *stream);
+                        void *ssm_state, int num_slots, void *stream);
 
 /* Prefill of T tokens of one sequence held in slot `slot` (host int): the same
  * arithmetic as T successive decode steps of that sequence (bloomery issue #565,
@@ -168,7 +176,7 @@ gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba,
  * state. The slot's state is left as after the last token. Errors: GDN_E_NULL,
  * GDN_E_SHAPE (T < 1 or > max_prefill_tokens), GDN_E_RANGE (slot), GDN_E_ALIGN. */
 gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int init_zero,
-                       uint16_t *out, uint16_t *conv_state, float *ssm_state, int num_slots,
+                       uint16_t *out, uint16_t *conv_state, void *ssm_state, int num_slots,
                        void *stream);
 
 /* The decode step of gdn_decode_step for callers that cannot allocate device
@@ -189,7 +197,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
  * Errors: as gdn_create's checks and gdn_decode_step's, plus GDN_E_CUDA. */
 gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, const uint16_t *x,
                                   const int32_t *slot_ids, int B, uint16_t *out, uint16_t *conv_state,
-                                  float *ssm_state, int num_slots, int32_t *dev_status, void *stream);
+                                  void *ssm_state, int num_slots, int32_t *dev_status, void *stream);
 
 /* Process-wide tuning knobs (they change speed, never results beyond FP32
  * summation order). knob 0: projection kernel of decode and prefill:

@@ -24,7 +24,8 @@ _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 class GdnConfig(ctypes.Structure):
     _fields_ = [("hidden", _i), ("n_k_heads", _i), ("n_v_heads", _i), ("d_k", _i), ("d_v", _i),
                 ("conv_kernel", _i), ("max_batch", _i), ("max_prefill_tokens", _i),
-                ("rms_eps", _f), ("l2_eps", _f), ("act_scale_in", _f), ("act_scale_out", _f)]
+                ("rms_eps", _f), ("l2_eps", _f), ("act_scale_in", _f), ("act_scale_out", _f),
+                ("state_bf16", _i)]
 
 
 class GdnNVFP4(ctypes.Structure):

@@ -61,9 +61,10 @@ class GatedDeltaNetLayer:
 
     def __init__(self, hidden, n_k_heads, n_v_heads, d_k, d_v, conv_kernel, weights: dict, max_batch=16,
                  max_prefill_tokens=0, rms_eps=1e-6, l2_eps=1e-6, act_scale_in=2.0 ** -8, act_scale_out=2.0 ** -4,
-                 stream=None):
+                 stream=None, state_bf16=False):
         self.cfg = GdnConfig(hidden, n_k_heads, n_v_heads, d_k, d_v, conv_kernel, max_batch, max_prefill_tokens,
-                             rms_eps, l2_eps, act_scale_in, act_scale_out)
+                             rms_eps, l2_eps, act_scale_in, act_scale_out, int(bool(state_bf16)))
+        self.state_bf16 = bool(state_bf16)
         w = weights
         self._w = GdnWeights(_nv(*w["qkvz"]), _nv(*w["ba"]), _nv(*w["out"]), _ptr(_dev(w["conv_w"])),
                              _ptr(_dev(w["A_log"])), _ptr(_dev(w["dt_bias"])), _ptr(_dev(w["norm_w"])))
@@ -89,17 +90,25 @@ class GatedDeltaNetLayer:
         return self._ctx.value
 
     def new_states(self, num_slots: int, device="cuda"):
-        """Zeroed conv state BF16 bits [S][K-1][C] and recurrent state FP32 [S][Hv][dv][dk]."""
+        """Zeroed conv state BF16 bits [S][K-1][C] and recurrent state [S][Hv][dv][dk]:
+        FP32, or BF16 bits (int16) for a layer created with state_bf16."""
         conv = torch.zeros(num_slots, self.Kc - 1, self.C, dtype=torch.int16, device=device)
-        ssm = torch.zeros(num_slots, self.Hv, self.D, self.D, dtype=torch.float32, device=device)
+        ssm = torch.zeros(num_slots, self.Hv, self.D, self.D,
+                          dtype=torch.int16 if self.state_bf16 else torch.float32, device=device)
         return conv, ssm
+
+    def _state(self, ssm_state):
+        want = (torch.int16, torch.bfloat16) if self.state_bf16 else (torch.float32,)
+        if ssm_state.dtype not in want:
+            raise ValueError(f"recurrent state must be {want[0]} for this layer, got {ssm_state.dtype}")
+        return _dev(ssm_state)
 
     def decode_step(self, x, slot_ids, conv_state, ssm_state, out=None, stream=None):
         B = x.shape[0]
         if out is None:
             out = torch.empty(B, self.H, dtype=torch.int16, device=x.device)
         st = lib().gdn_decode_step(self._ctx, _ptr(_dev(x)), _ptr(_dev(slot_ids)), B, _ptr(out),
-                                   _ptr(_dev(conv_state)), _ptr(_dev(ssm_state)), conv_state.shape[0],
+                                   _ptr(_dev(conv_state)), _ptr(self._state(ssm_state)), conv_state.shape[0],
                                    _stream(stream))
         _check(st, "gdn_decode_step")
         return out
@@ -109,7 +118,7 @@ class GatedDeltaNetLayer:
         if y is None:
             y = torch.empty(B, self.Hv * self.D, dtype=torch.float32, device=qkvz.device)
         st = lib().gdn_mix_step(self._ctx, _ptr(_dev(qkvz)), _ptr(_dev(ba)), _ptr(_dev(slot_ids)), B, _ptr(y),
-                                _ptr(_dev(conv_state)), _ptr(_dev(ssm_state)), conv_state.shape[0], _stream(stream))
+                                _ptr(_dev(conv_state)), _ptr(self._state(ssm_state)), conv_state.shape[0], _stream(stream))
         _check(st, "gdn_mix_step")
         return y
 
@@ -118,7 +127,7 @@ class GatedDeltaNetLayer:
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.int16, device=x.device)
         st = lib().gdn_prefill(self._ctx, _ptr(_dev(x)), T, int(slot), int(bool(init_zero)), _ptr(out),
-                               _ptr(_dev(conv_state)), _ptr(_dev(ssm_state)), conv_state.shape[0], _stream(stream))
+                               _ptr(_dev(conv_state)), _ptr(self._state(ssm_state)), conv_state.shape[0], _stream(stream))
         _check(st, "gdn_prefill")
         return out
 
@@ -134,7 +143,8 @@ def _t(a: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(a).to(device)
 
 
-def layer_from_synth(w, max_batch=16, max_prefill_tokens=0, device="cuda", stream=None) -> GatedDeltaNetLayer:
+def layer_from_synth(w, max_batch=16, max_prefill_tokens=0, device="cuda", stream=None,
+                     state_bf16=False) -> GatedDeltaNetLayer:
     """Upload ``synth.LayerWeights`` and create the layer context."""
     sh = w.shape
     dw = {
@@ -147,6 +157,6 @@ def layer_from_synth(w, max_batch=16, max_prefill_tokens=0, device="cuda", strea
     layer = GatedDeltaNetLayer(sh.hidden, sh.n_k_heads, sh.n_v_heads, sh.d_k, sh.d_v, sh.conv_kernel, dw,
                                max_batch=max_batch, max_prefill_tokens=max_prefill_tokens, rms_eps=w.rms_eps,
                                l2_eps=w.l2_eps, act_scale_in=w.act_scale_in, act_scale_out=w.act_scale_out,
-                               stream=stream)
+                               stream=stream, state_bf16=state_bf16)
     torch.cuda.synchronize()
     return layer

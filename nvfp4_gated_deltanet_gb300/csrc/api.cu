@@ -124,7 +124,7 @@ cudaError_t run_gemv(GemvArgs g, const LaunchCtx &lc, int M) {
 }
 
 gdn_status check_state_args(gdn_ctx *ctx, const void *x, const void *out, const uint16_t *conv_state,
-                            const float *ssm_state, int num_slots) {
+                            const void *ssm_state, int num_slots) {
   if (!ctx || !x || !out || !conv_state || !ssm_state) return GDN_E_NULL;
   if (!aligned16(x) || !aligned16(out) || !aligned16(conv_state) || !aligned16(ssm_state)) return GDN_E_ALIGN;
   if (num_slots < 1) return GDN_E_SHAPE;
@@ -149,6 +149,7 @@ MixArgs mix_args(gdn_ctx *c) {
   m.ts_out = c->cfg.act_scale_out;
   m.status = c->status;
   m.slices = g_tune.mix_slices;
+  m.state_bf16 = c->cfg.state_bf16;
   return m;
 }
 
@@ -357,6 +358,7 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (c.hidden % 64 || c.n_v_heads % c.n_k_heads || c.n_v_heads / c.n_k_heads > 8) return GDN_E_SHAPE;
   if (c.d_k != c.d_v || (c.d_k != 32 && c.d_k != 64 && c.d_k != 128)) return GDN_E_SHAPE;
   if (c.conv_kernel < 2 || c.conv_kernel > 4) return GDN_E_SHAPE;
+  if (c.state_bf16 != 0 && c.state_bf16 != 1) return GDN_E_SHAPE;
   if ((c.n_v_heads * c.d_v) % 64) return GDN_E_SHAPE;
   if (!std::isfinite(c.rms_eps) || !std::isfinite(c.l2_eps) || !std::isfinite(c.act_scale_in) ||
       !std::isfinite(c.act_scale_out))
@@ -537,7 +539,7 @@ gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int 
 }
 
 gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *out,
-                           uint16_t *conv_state, float *ssm_state, int num_slots, void *stream) {
+                           uint16_t *conv_state, void *ssm_state, int num_slots, void *stream) {
   gdn_status st = check_state_args(ctx, x, out, conv_state, ssm_state, num_slots);
   if (st != GDN_OK) return st;
   if (!slot_ids) return GDN_E_NULL;
@@ -547,8 +549,8 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   // The persistent single-kernel step (fused.cu) is correct but measured slower
   // on GB300 (c1 20.8 vs 14.6 us per layer-step: each grid barrier costs
   // ~2.5 us, more than a PDL kernel boundary), so it runs only on request.
-  if (g_tune.fused == 2 && g_tune.decode_gemm != 2 && B <= 2) {
-    FusedArgs f = fused_args(ctx, x, slot_ids, B, out, conv_state, ssm_state, num_slots);
+  if (g_tune.fused == 2 && g_tune.decode_gemm != 2 && B <= 2 && !ctx->cfg.state_bf16) {
+    FusedArgs f = fused_args(ctx, x, slot_ids, B, out, conv_state, static_cast<float *>(ssm_state), num_slots);
     if (fused_plan(f, ctx->num_sms)) return cuda_status(launch_fused(f, lc));
   }
   cudaError_t e = run_in_proj(ctx, x, B, slot_ids, num_slots, lc, true);
@@ -573,7 +575,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
 }
 
 gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, const int32_t *slot_ids, int B,
-                        float *y, uint16_t *conv_state, float *ssm_state, int num_slots, void *stream) {
+                        float *y, uint16_t *conv_state, void *ssm_state, int num_slots, void *stream) {
   gdn_status st = check_state_args(ctx, qkvz, y, conv_state, ssm_state, num_slots);
   if (st != GDN_OK) return st;
   if (!ba || !slot_ids) return GDN_E_NULL;
@@ -599,7 +601,7 @@ gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, 
 }
 
 gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int init_zero, uint16_t *out,
-                       uint16_t *conv_state, float *ssm_state, int num_slots, void *stream) {
+                       uint16_t *conv_state, void *ssm_state, int num_slots, void *stream) {
   gdn_status st = check_state_args(ctx, x, out, conv_state, ssm_state, num_slots);
   if (st != GDN_OK) return st;
   if (T < 1 || T > ctx->cfg.max_prefill_tokens) return GDN_E_SHAPE;
@@ -609,11 +611,12 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   const gdn_config &c = ctx->cfg;
   const int D = c.d_k;
   uint16_t *cst = conv_state + (size_t)slot * (c.conv_kernel - 1) * ctx->C;
-  float *S = ssm_state + (size_t)slot * c.n_v_heads * D * D;
+  const size_t s_elem = c.state_bf16 ? 2 : 4;
+  void *S = static_cast<char *>(ssm_state) + (size_t)slot * c.n_v_heads * D * D * s_elem;
   cudaError_t e = cudaSuccess;
   if (init_zero) {
     e = cudaMemsetAsync(cst, 0, (size_t)(c.conv_kernel - 1) * ctx->C * 2, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, (size_t)c.n_v_heads * D * D * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, (size_t)c.n_v_heads * D * D * s_elem, s);
     if (e != cudaSuccess) return cuda_status(e);
   }
   e = run_in_proj(ctx, x, T, nullptr, 0, lc, true);
@@ -624,6 +627,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.T = T;
   p.conv_state = cst;
   p.ssm = S;
+  p.state_bf16 = c.state_bf16;
   p.conv_w = ctx->conv_w;
   p.A_log = ctx->A_log;
   p.dt_bias = ctx->dt_bias;

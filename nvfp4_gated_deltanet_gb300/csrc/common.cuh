@@ -27,6 +27,17 @@ GDN_DEV uint16_t f32_to_bf16_bits(float f) {
   return *reinterpret_cast<uint16_t *>(&h);
 }
 
+// One element of a recurrent state stored as FP32 or as BF16 bits.
+GDN_DEV float state_load(const void *S, int bf16, size_t i) {
+  return bf16 ? bf16_bits_to_f32(static_cast<const uint16_t *>(S)[i]) : static_cast<const float *>(S)[i];
+}
+GDN_DEV void state_store(void *S, int bf16, size_t i, float v) {
+  if (bf16)
+    static_cast<uint16_t *>(S)[i] = f32_to_bf16_bits(v);
+  else
+    static_cast<float *>(S)[i] = v;
+}
+
 // E4M3 (OCP e4m3fn), round to nearest even, saturate finite values to 448.
 // Returns the byte of `v` (v finite).
 GDN_DEV uint32_t e4m3_from_f32(float v) {
@@ -285,7 +296,7 @@ struct MixArgs {
   const int32_t *slot_ids;
   int B, num_slots;
   uint16_t *conv_state;       // [S][K-1][C]
-  float *ssm_state;           // [S][Hv][dv][dk]
+  void *ssm_state;            // [S][Hv][dv][dk], FP32 or BF16 bits (state_bf16)
   const uint16_t *conv_w;     // [C][K]
   const float *A_log, *dt_bias, *norm_w;
   int Hk, Hv, D, C, Kc;
@@ -296,6 +307,7 @@ struct MixArgs {
   float *y_f32;       // [B][Hv*dv] or null
   int32_t *status;
   int slices;         // d_v slices per head (1, 2, 4), 0 = chosen from B
+  int state_bf16;     // recurrent state stored as BF16 (loaded to FP32, stored rounded)
 };
 cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc);
 
@@ -303,7 +315,8 @@ struct PrefillArgs {
   const uint16_t *proj;  // [T][ld] BF16: q | k | v | z | b | a
   int ld, T, Tp;         // Tp = T rounded up to whole 64-token chunks
   uint16_t *conv_state;  // this slot's [K-1][C]
-  float *ssm;            // this slot's [Hv][D][D]
+  void *ssm;             // this slot's [Hv][D][D], FP32 or BF16 bits (state_bf16)
+  int state_bf16;
   const uint16_t *conv_w;
   const float *A_log, *dt_bias, *norm_w;
   int Hk, Hv, D, C, Kc;

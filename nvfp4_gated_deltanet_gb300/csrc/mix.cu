@@ -37,7 +37,7 @@ template <int NS>
 __host__ __device__ constexpr int rows_per_warp() { return NS == 1 ? 16 : 8; }
 
 
-template <int D, int NS>
+template <int D, int NS, bool SB>
 __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ? 2 : 0) mix_kernel(MixArgs a) {
   constexpr int kRPW = rows_per_warp<NS>();
   constexpr int R = D / NS;
@@ -94,7 +94,11 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   uint16_t *cst = a.conv_state + (size_t)(live ? slot : 0) * (Kc - 1) * C;
   uint16_t tap[CPT][3];
   const int lr0 = warp * kRPW;
-  float *S = a.ssm_state + (((size_t)(live ? slot : 0) * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
+  // this lane's EPL consecutive d_k elements of each of the warp's rows: FP32,
+  // or BF16 bits when SB (loaded to FP32, stored rounded to nearest even)
+  const size_t s_off = (((size_t)(live ? slot : 0) * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
+  float *S = static_cast<float *>(a.ssm_state) + s_off;
+  uint16_t *Sb = static_cast<uint16_t *>(a.ssm_state) + s_off;
   float st[kRPW][EPL];
   if (live) {
 #pragma unroll
@@ -104,7 +108,20 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
         tap[c][j] = (tid + c * THREADS < NCH && j < Kc - 1) ? cst[(size_t)j * C + ch[c]] : uint16_t(0);
 #pragma unroll
     for (int j = 0; j < kRPW; ++j) {
-      if (EPL == 4) {
+      if (SB) {
+        uint16_t b[EPL];
+        if (EPL == 4) {
+          const uint2 t = *reinterpret_cast<const uint2 *>(Sb + (size_t)j * D);
+          b[0] = t.x & 0xFFFFu; b[1 % EPL] = t.x >> 16; b[2 % EPL] = t.y & 0xFFFFu; b[3 % EPL] = t.y >> 16;
+        } else if (EPL == 2) {
+          const uint32_t t = *reinterpret_cast<const uint32_t *>(Sb + (size_t)j * D);
+          b[0] = t & 0xFFFFu; b[1 % EPL] = t >> 16;
+        } else {
+          b[0] = Sb[(size_t)j * D];
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) st[j][e] = bf16_bits_to_f32(b[e]);
+      } else if (EPL == 4) {
         float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
         st[j][0] = t4.x; st[j][1 % EPL] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
       } else if (EPL == 2) {
@@ -224,7 +241,17 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
     }
 #pragma unroll
     for (int j = 0; j < kRPW; ++j) {
-      if (EPL == 4) {
+      if (SB) {
+        uint32_t b[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) b[e] = f32_to_bf16_bits(st[j][e]);
+        if (EPL == 4)
+          *reinterpret_cast<uint2 *>(Sb + (size_t)j * D) = make_uint2(b[0] | (b[1 % EPL] << 16), b[2 % EPL] | (b[3 % EPL] << 16));
+        else if (EPL == 2)
+          *reinterpret_cast<uint32_t *>(Sb + (size_t)j * D) = b[0] | (b[1 % EPL] << 16);
+        else
+          Sb[(size_t)j * D] = (uint16_t)b[0];
+      } else if (EPL == 4) {
         *reinterpret_cast<float4 *>(S + (size_t)j * D) =
             make_float4(st[j][0], st[j][1 % EPL], st[j][2 % EPL], st[j][3 % EPL]);
       } else if (EPL == 2) {
@@ -286,8 +313,8 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   }
 }
 
-template <int D, int NS>
-cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
+template <int D, int NS, bool SB>
+cudaError_t launch_dn_t(const MixArgs &a, const LaunchCtx &lc) {
   const int G = a.Hv / a.Hk;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.Hv * NS, a.B, 1);
@@ -303,7 +330,12 @@ cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
   attr[1].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mix_kernel<D, NS>, a);
+  return cudaLaunchKernelEx(&cfg, mix_kernel<D, NS, SB>, a);
+}
+
+template <int D, int NS>
+cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
+  return a.state_bf16 ? launch_dn_t<D, NS, true>(a, lc) : launch_dn_t<D, NS, false>(a, lc);
 }
 
 }  // namespace

@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
 
   for (int e = tid; e < R * D; e += blockDim.x) {
     const int r = e / D, d = e % D;
-    S[r * SLD + d] = a.ssm[((size_t)h * D + r0 + r) * D + d];
+    S[r * SLD + d] = state_load(a.ssm, a.state_bf16, ((size_t)h * D + r0 + r) * D + d);
   }
   auto load_wq = [&](int c) {
     const float *w = a.W + ((size_t)h * nc + c) * kC * D;
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
   __syncthreads();
   for (int e = tid; e < R * D; e += blockDim.x) {
     const int r = e / D, d = e % D;
-    a.ssm[((size_t)h * D + r0 + r) * D + d] = S[r * SLD + d];
+    state_store(a.ssm, a.state_bf16, ((size_t)h * D + r0 + r) * D + d, S[r * SLD + d]);
   }
 }
 

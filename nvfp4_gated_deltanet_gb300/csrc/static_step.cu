@@ -125,12 +125,12 @@ using namespace gdn;
 
 extern "C" gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, const uint16_t *x,
                                              const int32_t *slot_ids, int B, uint16_t *out, uint16_t *conv_state,
-                                             float *ssm_state, int num_slots, int32_t *dev_status, void *stream) {
+                                             void *ssm_state, int num_slots, int32_t *dev_status, void *stream) {
   if (!cfg || !w || !x || !slot_ids || !out || !conv_state || !ssm_state) return GDN_E_NULL;
   const gdn_config &c = *cfg;
   if (c.n_k_heads <= 0 || c.n_v_heads <= 0 || c.n_v_heads % c.n_k_heads || c.n_v_heads / c.n_k_heads > 8 ||
       c.d_k != c.d_v || (c.d_k != 32 && c.d_k != 64 && c.d_k != 128) || c.conv_kernel < 2 || c.conv_kernel > 4 ||
-      c.hidden <= 0 || c.hidden % 64 || (c.n_v_heads * c.d_v) % 64)
+      c.hidden <= 0 || c.hidden % 64 || (c.n_v_heads * c.d_v) % 64 || (c.state_bf16 != 0 && c.state_bf16 != 1))
     return GDN_E_SHAPE;
   const int H = c.hidden, Hk = c.n_k_heads, Hv = c.n_v_heads, D = c.d_k;
   const int Nqkvz = 2 * Hk * D + 2 * Hv * D, Nba = 2 * Hv, Nin = Nqkvz + Nba, Vd = Hv * D;
@@ -189,6 +189,7 @@ extern "C" gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_we
   m.num_slots = num_slots;
   m.conv_state = conv_state;
   m.ssm_state = ssm_state;
+  m.state_bf16 = c.state_bf16;
   m.conv_w = w->conv_w;
   m.A_log = w->A_log;
   m.dt_bias = w->dt_bias;

@@ -19,7 +19,11 @@ equations. The readings taken here:
   softplus(x) = x for x > 20; alpha = exp(g).
 * value head h reads key head h // (Hv / Hk).
 * delta rule on S[d_v][d_k]: S <- alpha S; u = beta (v - S k_hat);
-  S <- S + u k_hat^T; o = S q_hat. The state is stored in FP32 after each step.
+  S <- S + u k_hat^T; o = S q_hat. The state is stored in FP32 after each step,
+  or, for a layer whose state is kept in BF16 (Rocket blog, "KDA state tile":
+  the state stored in BF16 beside FP32), rounded FP32 -> BF16 (nearest even)
+  after each decode step; a prefill call then carries the state in FP32 from
+  its first token to its last and rounds once at the end.
 * gated RMSNorm per value head: y = o * (mean(o^2) + eps)^-1/2 * w * SiLU(z).
 * y -> FP32 -> NVFP4 (static s_out) -> W4A4 out_proj -> FP32 -> BF16.
 * a padding row (slot id -1) writes a zero output row and touches no state.
@@ -115,8 +119,9 @@ def gated_rmsnorm(o: np.ndarray, z: np.ndarray, w: np.ndarray, eps: float) -> np
 class Layer:
     """One GDN layer: weights from ``synth.LayerWeights``."""
 
-    def __init__(self, weights):
+    def __init__(self, weights, state_bf16: bool = False):
         self.w = weights
+        self.state_bf16 = bool(state_bf16)
         sh = weights.shape
         self.sh = sh
         self.conv_w = codecs.bf16_to_f32(weights.conv_w).astype(np.float64)
@@ -133,12 +138,15 @@ class Layer:
         return (project(x_bits, self.op_qkvz, self.w.act_scale_in),
                 project(x_bits, self.op_ba, self.w.act_scale_in))
 
-    def mix(self, qkvz_row: np.ndarray, ba_row: np.ndarray, conv_st: np.ndarray, S: np.ndarray):
+    def mix(self, qkvz_row: np.ndarray, ba_row: np.ndarray, conv_st: np.ndarray, S: np.ndarray,
+            state_store: str | None = None):
         """Conv, norms, gates, delta rule and gated norm for one sequence.
 
         qkvz_row, ba_row: BF16 values (float64); conv_st: BF16 bits [K-1][C];
-        S: FP32 [Hv][dv][dk]. Returns (y float64 [Hv*dv], conv_st', S' FP32,
-        extras) where extras holds the intermediates."""
+        S: [Hv][dv][dk] float32 values. Returns (y float64 [Hv*dv], conv_st',
+        S', extras) where extras holds the intermediates and S' is the updated
+        state rounded to its storage type: "f32", or "bf16" (FP32 then BF16,
+        held in float32); by default the layer's own."""
         sh = self.sh
         nq = sh.n_k_heads * sh.d_k
         nv = sh.n_v_heads * sh.d_v
@@ -158,7 +166,11 @@ class Layer:
         y = gated_rmsnorm(o, z, self.norm_w, self.w.rms_eps)
         new_conv = codecs.f32_to_bf16(win_new.astype(np.float32))       # raw BF16 inputs: exact
         extras = dict(conv_out=conv_out, q_hat=q_hat, k_hat=k_hat, v=v, beta=beta, g=g, o=o)
-        return y.reshape(-1), new_conv, S64.astype(np.float32), extras
+        store = state_store or ("bf16" if self.state_bf16 else "f32")
+        S_new = S64.astype(np.float32)
+        if store == "bf16":
+            S_new = codecs.bf16_to_f32(codecs.f32_to_bf16(S_new))
+        return y.reshape(-1), new_conv, S_new, extras
 
     def out_proj(self, y: np.ndarray) -> np.ndarray:
         """y float64 [B][Hv*dv] -> FP32 -> NVFP4 (s_out) -> GEMM -> BF16 bits [B][H]."""
@@ -200,8 +212,10 @@ class Layer:
         qkvz, ba = self.projections(np.asarray(x_bits, dtype=np.uint16))
         T = qkvz.shape[0]
         y = np.empty((T, self.sh.value_dim), dtype=np.float64)
-        for t in range(T):
-            y[t], conv_state[...], ssm_state[...], _ = self.mix(qkvz[t], ba[t], conv_state, ssm_state)
+        for t in range(T):   # the state in FP32 within the call
+            y[t], conv_state[...], ssm_state[...], _ = self.mix(qkvz[t], ba[t], conv_state, ssm_state, "f32")
+        if self.state_bf16:  # stored once, at the end of the call
+            ssm_state[...] = codecs.bf16_to_f32(codecs.f32_to_bf16(ssm_state.astype(np.float32)))
         return self.out_proj(y)
 
 

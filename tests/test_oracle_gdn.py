@@ -211,3 +211,69 @@ def test_layer_stage_extras_consistent(tiny):
     # conv state holds the raw BF16 projection inputs, newest last
     nqkv = 2 * sh.n_k_heads * sh.d_k + sh.n_v_heads * sh.d_v
     np.testing.assert_array_equal(codecs.bf16_to_f32(cst[-1]), qkvz[0, :nqkv].astype(np.float32))
+
+
+# ------------------------------------------------------------------ BF16-stored state
+
+def _bf16_state(sh, seed):
+    """A recurrent state whose values are BF16-representable (float32 array)."""
+    s = synth.ssm_state(sh, seed)
+    return codecs.bf16_to_f32(codecs.f32_to_bf16(s))
+
+
+def test_bf16_state_decode_rounds_the_updated_state_once():
+    """A decode step of the BF16-state layer equals the FP32-state layer's step
+    from the same state, with the updated state rounded FP32 -> BF16 (nearest
+    even): the outputs are identical and the state is rounded after the
+    update, not before it or inside it."""
+    sh = synth.TINY
+    w = synth.layer_weights(sh, 0)
+    L32, L16 = gdn.Layer(w), gdn.Layer(w, state_bf16=True)
+    x = synth.x_tokens(sh, 3, 2)
+    c0 = synth.conv_state(sh, 3)[None]
+    s0 = _bf16_state(sh, 3)[None]
+    ca, sa, cb, sb = c0.copy(), s0.copy(), c0.copy(), s0.copy()
+    out32 = L32.decode_step(x[0:1], [0], ca, sa)
+    out16 = L16.decode_step(x[0:1], [0], cb, sb)
+    np.testing.assert_array_equal(out32, out16)
+    np.testing.assert_array_equal(ca, cb)
+    np.testing.assert_array_equal(sb, codecs.bf16_to_f32(codecs.f32_to_bf16(sa)))
+    assert (sb != sa).any()                      # the rounding did something
+    # every stored value is BF16: its low 16 bits are zero
+    assert not (sb.view(np.uint32) & 0xFFFF).any()
+
+
+def test_bf16_state_identity_update_leaves_state_bit_unchanged():
+    """beta = 0 and g = 0 (A_log = -inf, b -> -inf): the update is the identity,
+    so a BF16 state comes back bit-identical."""
+    sh = synth.TINY
+    w = synth.layer_weights(sh, 0)
+    w.A_log[:] = -np.inf
+    L16 = gdn.Layer(w, state_bf16=True)
+    qkvz = codecs.bf16_to_f32(synth.bf16_normal(1, sh.qkvz_out, 5)[0]).astype(np.float64)
+    ba = np.concatenate([np.full(sh.n_v_heads, -1e4), np.zeros(sh.n_v_heads)])
+    s0 = _bf16_state(sh, 4)
+    with np.errstate(over="ignore"):                 # sigmoid(-1e4) = 1/(1+inf) = 0
+        _, _, s1, ex = L16.mix(qkvz, ba, synth.conv_state(sh, 4), s0)
+    assert (ex["beta"] == 0).all() and (ex["g"] == 0).all()
+    np.testing.assert_array_equal(s1, s0)
+
+
+def test_bf16_state_prefill_carries_fp32_and_rounds_at_the_end():
+    """A prefill call of the BF16-state layer: the FP32 layer's prefill from the
+    same state, the final state rounded once to BF16; outputs identical."""
+    sh = synth.TINY
+    w = synth.layer_weights(sh, 0)
+    L32, L16 = gdn.Layer(w), gdn.Layer(w, state_bf16=True)
+    x = synth.x_tokens(sh, 6, 20)
+    c0, s0 = synth.conv_state(sh, 6), _bf16_state(sh, 6)
+    ca, sa, cb, sb = c0.copy(), s0.copy(), c0.copy(), s0.copy()
+    o32 = L32.prefill(x, ca, sa, init_zero=False)
+    o16 = L16.prefill(x, cb, sb, init_zero=False)
+    np.testing.assert_array_equal(o32, o16)
+    np.testing.assert_array_equal(sb, codecs.bf16_to_f32(codecs.f32_to_bf16(sa)))
+    # and differs from rounding after every token (the decode-step semantics)
+    cc, sc = c0.copy(), s0.copy()
+    for t in range(20):
+        L16.decode_step(x[t:t + 1], [0], cc[None], sc[None])
+    assert rel_l2(sc, sb) > 0
