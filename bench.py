@@ -243,6 +243,35 @@ def make_stack_b(pkg, synth, n_layers, B, device="cuda", state_bf16=False):
     return w, layers, states, xd
 
 
+def time_verify(layers, states, xd, B, r, steps):
+    """Verify of r candidate tokens for B sequences, then the commit of every
+    token, per layer instance of the stack, as one CUDA graph; us per layer."""
+    import torch
+    ids = torch.arange(B, dtype=torch.int32, device="cuda")
+    acc = torch.full((B,), r, dtype=torch.int32, device="cuda")
+    x = xd[:B].unsqueeze(1).expand(B, r, -1).contiguous()
+    snaps = [L.new_snapshots(B, r) for L in layers]
+    outs = [torch.empty(B, r, layers[0].H, dtype=torch.int16, device="cuda") for _ in layers]
+
+    def one_pass():
+        for L, (c, m), (sc, ss), o in zip(layers, states, snaps, outs):
+            L.verify(x, ids, c, m, sc, ss, out=o)
+            L.verify_commit(ids, acc, sc, ss, c, m)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        one_pass()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        one_pass()
+    us = time_graph(g, steps, 3) * 1e3 / len(layers)
+    del g, snaps
+    return {"us_per_layer": round(us, 3), "tokens_per_s": round(B * r / (us * 1e-6)),
+            "note": f"{B} sequences x {r} candidate tokens, verify + commit of all"}
+
+
 def time_prefill(pkg, synth, T, reps=3):
     """Prefill of one T-token sequence from zero state (weights stay resident
     in L2 within the call, as they would in a real prompt)."""
@@ -425,6 +454,8 @@ def main():
             del gB
         extra["c1"] = {"us_per_layer_step": round(us_layer, 3), "hbm_gbs": round(gbs_step, 1),
                        "frac_of_peak": round(gbs_step / hbm_peak, 4)}
+        # multi-token verify: 4 sequences x 4 candidate tokens, then the commit of all
+        extra["verify_b4_r4"] = time_verify(layers, states, xd, 4, 4, max(10, args.steps // 4))
         del layers, states
         torch.cuda.empty_cache()
         # the two-way head-parallel slice (8 key / 16 value heads), benched the same way

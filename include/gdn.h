@@ -179,6 +179,39 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
                        uint16_t *out, uint16_t *conv_state, void *ssm_state, int num_slots,
                        void *stream);
 
+/* Multi-token verify (speculative decoding's check of r candidate tokens per
+ * sequence) and its commit, the pair of passes the pages run beside prompt and
+ * decode on a GDN layer's delta state (bloomery issue #565, §10, PR #1127).
+ *
+ * gdn_verify runs r tokens of each of B sequences through the layer, token by
+ * token, exactly as r successive gdn_decode_step calls would, but leaves the
+ * slots' states untouched: the state after each token goes to the caller's
+ * snapshot buffers instead.
+ *   x:         BF16 [B][r][H], row b's candidate tokens in order
+ *   slot_ids:  int32 [B] (device), as for gdn_decode_step (-1 = padding: zero
+ *              output rows, no snapshot written; its x rows must be finite)
+ *   out:       BF16 [B][r][H]
+ *   conv_state, ssm_state: the slots' states as for gdn_decode_step (read only)
+ *   snap_conv: BF16 [B][r][conv_kernel-1][C]; snap_ssm: [B][r][Hv][d_v][d_k] in
+ *              the state's storage type (FP32, or BF16 bits with state_bf16):
+ *              snapshot (b, t) is row b's state after its token t.
+ * B * r must not exceed max_batch. Errors: as gdn_decode_step, GDN_E_SHAPE for
+ * r < 1 or B * r > max_batch.
+ *
+ * gdn_verify_commit then makes row b's slot take snapshot (b, n-1), where
+ * n = accepted[b] (device int32 [B], read by the kernel so the commit can be
+ * captured in a graph after the acceptance decision): n = 0 keeps the slot's
+ * state, n in 1..r commits the state after the n-th token, n > r sets
+ * GDN_E_RANGE in the status word and leaves that slot untouched. Padding rows
+ * are skipped. Slot ids must be distinct. Errors: GDN_E_NULL, GDN_E_ALIGN,
+ * GDN_E_SHAPE, GDN_E_CUDA. */
+gdn_status gdn_verify(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, int r, uint16_t *out,
+                      const uint16_t *conv_state, const void *ssm_state, int num_slots, uint16_t *snap_conv,
+                      void *snap_ssm, void *stream);
+gdn_status gdn_verify_commit(gdn_ctx *ctx, const int32_t *slot_ids, int B, int r, const int32_t *accepted,
+                             const uint16_t *snap_conv, const void *snap_ssm, uint16_t *conv_state,
+                             void *ssm_state, int num_slots, void *stream);
+
 /* The decode step of gdn_decode_step for callers that cannot allocate device
  * memory or keep a context: runtimes that fix all device memory at start-up,
  * work issued while a CUDA graph is captured, hosts that pass only tensors.

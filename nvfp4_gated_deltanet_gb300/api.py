@@ -122,6 +122,34 @@ class GatedDeltaNetLayer:
         _check(st, "gdn_mix_step")
         return y
 
+    def new_snapshots(self, B: int, r: int, device="cuda"):
+        """Snapshot buffers of a verify pass: conv [B][r][K-1][C] BF16 bits and
+        recurrent [B][r][Hv][dv][dk] in the layer's state type."""
+        conv = torch.empty(B, r, self.Kc - 1, self.C, dtype=torch.int16, device=device)
+        ssm = torch.empty(B, r, self.Hv, self.D, self.D,
+                          dtype=torch.int16 if self.state_bf16 else torch.float32, device=device)
+        return conv, ssm
+
+    def verify(self, x, slot_ids, conv_state, ssm_state, snap_conv, snap_ssm, out=None, stream=None):
+        """x [B][r][H] candidate tokens -> out [B][r][H]; snapshots of the state
+        after every token; the slots' states are not modified."""
+        B, r = x.shape[0], x.shape[1]
+        if out is None:
+            out = torch.empty(B, r, self.H, dtype=torch.int16, device=x.device)
+        st = lib().gdn_verify(self._ctx, _ptr(_dev(x)), _ptr(_dev(slot_ids)), B, r, _ptr(out),
+                              _ptr(_dev(conv_state)), _ptr(self._state(ssm_state)), conv_state.shape[0],
+                              _ptr(_dev(snap_conv)), _ptr(self._state(snap_ssm)), _stream(stream))
+        _check(st, "gdn_verify")
+        return out
+
+    def verify_commit(self, slot_ids, accepted, snap_conv, snap_ssm, conv_state, ssm_state, stream=None):
+        """Slot of row b takes the state after its accepted[b]-th token (device int32 [B]; 0 = keep)."""
+        B, r = snap_conv.shape[0], snap_conv.shape[1]
+        st = lib().gdn_verify_commit(self._ctx, _ptr(_dev(slot_ids)), B, r, _ptr(_dev(accepted)),
+                                     _ptr(_dev(snap_conv)), _ptr(self._state(snap_ssm)), _ptr(_dev(conv_state)),
+                                     _ptr(self._state(ssm_state)), conv_state.shape[0], _stream(stream))
+        _check(st, "gdn_verify_commit")
+
     def prefill(self, x, slot, init_zero, conv_state, ssm_state, out=None, stream=None):
         T = x.shape[0]
         if out is None:

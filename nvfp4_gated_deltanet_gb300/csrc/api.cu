@@ -574,6 +574,79 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   return cuda_status(run_out_proj(ctx, out, B, lc, true, true));
 }
 
+gdn_status gdn_verify(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, int r, uint16_t *out,
+                      const uint16_t *conv_state, const void *ssm_state, int num_slots, uint16_t *snap_conv,
+                      void *snap_ssm, void *stream) {
+  gdn_status st = check_state_args(ctx, x, out, conv_state, ssm_state, num_slots);
+  if (st != GDN_OK) return st;
+  if (!slot_ids || !snap_conv || !snap_ssm) return GDN_E_NULL;
+  if (!aligned16(slot_ids) || !aligned16(snap_conv) || !aligned16(snap_ssm)) return GDN_E_ALIGN;
+  if (B < 1 || r < 1 || (long long)B * r > ctx->cfg.max_batch) return GDN_E_SHAPE;
+  const gdn_config &c = ctx->cfg;
+  const int rows = B * r;
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, true};
+  // every candidate token's projections at once: they do not depend on the state
+  cudaError_t e = run_in_proj(ctx, x, rows, nullptr, 0, lc, true);
+  if (e != cudaSuccess) return cuda_status(e);
+  const size_t conv_elems = (size_t)(c.conv_kernel - 1) * ctx->C;
+  const size_t ssm_elems = (size_t)c.n_v_heads * c.d_v * c.d_k;
+  const size_t esz = c.state_bf16 ? 2 : 4;
+  for (int t = 0; t < r; ++t) {  // the recurrence, token by token
+    MixArgs m = mix_args(ctx);
+    m.qkvz = ctx->proj;
+    m.ld_qkvz = ctx->Nin;
+    m.ba = ctx->proj + ctx->Nqkvz;
+    m.ld_ba = ctx->Nin;
+    m.slot_ids = slot_ids;
+    m.B = B;
+    m.num_slots = num_slots;
+    m.conv_state = const_cast<uint16_t *>(conv_state);  // read only: writes go to the snapshots
+    m.ssm_state = const_cast<void *>(ssm_state);
+    m.io_mul = r;
+    m.io_add = t;
+    m.conv_src = t ? snap_conv + (size_t)(t - 1) * conv_elems : nullptr;
+    m.conv_dst = snap_conv + (size_t)t * conv_elems;
+    m.conv_row_stride = (size_t)r * conv_elems;
+    m.ssm_src = t ? static_cast<const char *>(snap_ssm) + (size_t)(t - 1) * ssm_elems * esz : nullptr;
+    m.ssm_dst = static_cast<char *>(snap_ssm) + (size_t)t * ssm_elems * esz;
+    m.ssm_row_stride = (size_t)r * ssm_elems;
+    m.y_codes = ctx->y_codes;
+    m.y_scales = ctx->y_scales;
+    m.y_sf_tiled = out_proj_tiled(ctx, rows) ? 1 : 0;
+    m.y_f32 = nullptr;
+    // token t > 0 reads the snapshot token t-1 wrote: no early start
+    LaunchCtx lm = lc;
+    if (t > 0) lm.pdl = false;
+    e = launch_mix(m, lm);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return cuda_status(run_out_proj(ctx, out, rows, lc, true));
+}
+
+gdn_status gdn_verify_commit(gdn_ctx *ctx, const int32_t *slot_ids, int B, int r, const int32_t *accepted,
+                             const uint16_t *snap_conv, const void *snap_ssm, uint16_t *conv_state, void *ssm_state,
+                             int num_slots, void *stream) {
+  if (!ctx || !slot_ids || !accepted || !snap_conv || !snap_ssm || !conv_state || !ssm_state) return GDN_E_NULL;
+  if (!aligned16(snap_conv) || !aligned16(snap_ssm) || !aligned16(conv_state) || !aligned16(ssm_state))
+    return GDN_E_ALIGN;
+  if (B < 1 || r < 1 || (long long)B * r > ctx->cfg.max_batch || num_slots < 1) return GDN_E_SHAPE;
+  const gdn_config &c = ctx->cfg;
+  VerifyCommitArgs v{};
+  v.slot_ids = slot_ids;
+  v.accepted = accepted;
+  v.B = B;
+  v.r = r;
+  v.num_slots = num_slots;
+  v.snap_ssm = snap_ssm;
+  v.snap_conv = snap_conv;
+  v.ssm_state = ssm_state;
+  v.conv_state = conv_state;
+  v.ssm_bytes = (size_t)c.n_v_heads * c.d_v * c.d_k * (c.state_bf16 ? 2 : 4);
+  v.conv_bytes = (size_t)(c.conv_kernel - 1) * ctx->C * 2;
+  v.status = ctx->status;
+  return cuda_status(launch_verify_commit(v, static_cast<cudaStream_t>(stream)));
+}
+
 gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, const int32_t *slot_ids, int B,
                         float *y, uint16_t *conv_state, void *ssm_state, int num_slots, void *stream) {
   gdn_status st = check_state_args(ctx, qkvz, y, conv_state, ssm_state, num_slots);

@@ -308,8 +308,32 @@ struct MixArgs {
   int32_t *status;
   int slices;         // d_v slices per head (1, 2, 4), 0 = chosen from B
   int state_bf16;     // recurrent state stored as BF16 (loaded to FP32, stored rounded)
+  // Verify passes (zero for a plain step): row b's q|k|v|z, b|a and y are row
+  // b * io_mul + io_add of their buffers; its states are read from *_src
+  // (row-indexed, element strides below) when set, else from its slot, and
+  // written to *_dst when set, else back to its slot.
+  int io_mul, io_add;
+  const void *ssm_src;
+  void *ssm_dst;
+  const uint16_t *conv_src;
+  uint16_t *conv_dst;
+  size_t ssm_row_stride, conv_row_stride;
 };
 cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc);
+
+// Commit of a verify pass (verify.cu): row b with slot s >= 0 and accepted[b]
+// = n in 1..r takes snapshot (b, n-1) as its slot's state; n = 0 keeps it.
+struct VerifyCommitArgs {
+  const int32_t *slot_ids, *accepted;  // [B] device
+  int B, r, num_slots;
+  const void *snap_ssm;                // [B][r] x ssm_bytes
+  const uint16_t *snap_conv;           // [B][r] x conv_bytes
+  void *ssm_state;                     // [S] x ssm_bytes
+  uint16_t *conv_state;                // [S] x conv_bytes
+  size_t ssm_bytes, conv_bytes;        // per slot, multiples of 16
+  int32_t *status;
+};
+cudaError_t launch_verify_commit(const VerifyCommitArgs &a, cudaStream_t stream);
 
 struct PrefillArgs {
   const uint16_t *proj;  // [T][ld] BF16: q | k | v | z | b | a

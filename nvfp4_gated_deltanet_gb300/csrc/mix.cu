@@ -58,6 +58,7 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   const int h = blockIdx.x / NS, split = blockIdx.x % NS;
   const int kh = h / G;
   const int b = blockIdx.y;
+  const int io = a.io_mul ? b * a.io_mul + a.io_add : b;  // row of the q|k|v|z, b|a and y buffers
   const int row0 = split * R;  // first d_v row of this slice
   const int vd = a.Hv * D;
   const int C = a.C, Kc = a.Kc;
@@ -90,22 +91,32 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
     for (int j = lane; j < a.B; j += 32) dup |= (j != b && a.slot_ids[j] == slot);
     if (__any_sync(0xffffffffu, dup)) { bad = true; live = false; }
   }
-  // state: conv taps and this warp's rows of S
-  uint16_t *cst = a.conv_state + (size_t)(live ? slot : 0) * (Kc - 1) * C;
+  // state: conv taps and this warp's rows of S. A plain step reads and writes
+  // the slot's state; a verify pass reads row b's from *_src (or the slot) and
+  // writes it to *_dst, leaving the slot untouched.
+  uint16_t *cst_slot = a.conv_state + (size_t)(live ? slot : 0) * (Kc - 1) * C;
+  const uint16_t *cst_rd = a.conv_src ? a.conv_src + (size_t)b * a.conv_row_stride : cst_slot;
+  uint16_t *cst = a.conv_dst ? a.conv_dst + (size_t)b * a.conv_row_stride : cst_slot;  // written
   uint16_t tap[CPT][3];
   const int lr0 = warp * kRPW;
   // this lane's EPL consecutive d_k elements of each of the warp's rows: FP32,
   // or BF16 bits when SB (loaded to FP32, stored rounded to nearest even)
-  const size_t s_off = (((size_t)(live ? slot : 0) * a.Hv + h) * D + row0 + lr0) * D + lane * EPL;
-  float *S = static_cast<float *>(a.ssm_state) + s_off;
-  uint16_t *Sb = static_cast<uint16_t *>(a.ssm_state) + s_off;
+  constexpr size_t kEs = SB ? 2 : 4;
+  const size_t s_rel = (((size_t)h * D + row0 + lr0) * D + lane * EPL) * kEs;
+  const size_t s_slot = (size_t)(live ? slot : 0) * a.Hv * D * D * kEs;
+  const char *s_rd = (a.ssm_src ? static_cast<const char *>(a.ssm_src) + (size_t)b * a.ssm_row_stride * kEs
+                                : static_cast<const char *>(a.ssm_state) + s_slot) + s_rel;
+  char *s_wr = (a.ssm_dst ? static_cast<char *>(a.ssm_dst) + (size_t)b * a.ssm_row_stride * kEs
+                          : static_cast<char *>(a.ssm_state) + s_slot) + s_rel;
+  const float *S = reinterpret_cast<const float *>(s_rd);
+  const uint16_t *Sb = reinterpret_cast<const uint16_t *>(s_rd);
   float st[kRPW][EPL];
   if (live) {
 #pragma unroll
     for (int c = 0; c < CPT; ++c)
 #pragma unroll
       for (int j = 0; j < 3; ++j)
-        tap[c][j] = (tid + c * THREADS < NCH && j < Kc - 1) ? cst[(size_t)j * C + ch[c]] : uint16_t(0);
+        tap[c][j] = (tid + c * THREADS < NCH && j < Kc - 1) ? cst_rd[(size_t)j * C + ch[c]] : uint16_t(0);
 #pragma unroll
     for (int j = 0; j < kRPW; ++j) {
       if (SB) {
@@ -136,15 +147,15 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   // ---- the projections come from the preceding kernel
   pdl_wait();
   pdl_launch_dependents();
-  const uint16_t *xin = a.qkvz + (size_t)b * a.ld_qkvz;
+  const uint16_t *xin = a.qkvz + (size_t)io * a.ld_qkvz;
   if (bad && tid == 0 && blockIdx.x == 0) flag_status(a.status, GDN_E_RANGE);
   if (!live) {  // padding: zero y for this slice, touch no state (whole cluster agrees)
     for (int i = tid; i < R; i += blockDim.x) {
-      if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + i] = 0.0f;
-      if (a.y_codes && (i & 1) == 0) a.y_codes[((size_t)b * vd + h * D + row0 + i) >> 1] = 0;
+      if (a.y_f32) a.y_f32[(size_t)io * vd + h * D + row0 + i] = 0.0f;
+      if (a.y_codes && (i & 1) == 0) a.y_codes[((size_t)io * vd + h * D + row0 + i) >> 1] = 0;
       if (a.y_scales && (i & 15) == 0) {
         const int blk = (h * D + row0 + i) >> 4;
-        a.y_scales[a.y_sf_tiled ? sf_tiled_offset(b, blk, vd >> 4) : ((size_t)b * vd >> 4) + blk] = 0;
+        a.y_scales[a.y_sf_tiled ? sf_tiled_offset(io, blk, vd >> 4) : ((size_t)io * vd >> 4) + blk] = 0;
       }
     }
     return;
@@ -153,7 +164,7 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
 #pragma unroll
   for (int c = 0; c < CPT; ++c) xn[c] = (tid + c * THREADS < NCH) ? xin[ch[c]] : uint16_t(0);
   const float zv = tid < R ? bf16_bits_to_f32(xin[2 * a.Hk * D + vd + h * D + row0 + tid]) : 0.0f;
-  const uint16_t *bain = a.ba + (size_t)b * a.ld_ba;
+  const uint16_t *bain = a.ba + (size_t)io * a.ld_ba;
   const float b_raw = bf16_bits_to_f32(bain[h]);
   const float a_raw = bf16_bits_to_f32(bain[a.Hv + h]);
 
@@ -239,6 +250,8 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
       for (int e = 0; e < EPL; ++e) st[j][e] = fmaf(u, kr[e], alpha * st[j][e]);
       if (lane == 0) s_o[lr0 + j] = o;
     }
+    float *Sf = reinterpret_cast<float *>(s_wr);
+    uint16_t *Sw = reinterpret_cast<uint16_t *>(s_wr);
 #pragma unroll
     for (int j = 0; j < kRPW; ++j) {
       if (SB) {
@@ -246,18 +259,18 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
 #pragma unroll
         for (int e = 0; e < EPL; ++e) b[e] = f32_to_bf16_bits(st[j][e]);
         if (EPL == 4)
-          *reinterpret_cast<uint2 *>(Sb + (size_t)j * D) = make_uint2(b[0] | (b[1 % EPL] << 16), b[2 % EPL] | (b[3 % EPL] << 16));
+          *reinterpret_cast<uint2 *>(Sw + (size_t)j * D) = make_uint2(b[0] | (b[1 % EPL] << 16), b[2 % EPL] | (b[3 % EPL] << 16));
         else if (EPL == 2)
-          *reinterpret_cast<uint32_t *>(Sb + (size_t)j * D) = b[0] | (b[1 % EPL] << 16);
+          *reinterpret_cast<uint32_t *>(Sw + (size_t)j * D) = b[0] | (b[1 % EPL] << 16);
         else
-          Sb[(size_t)j * D] = (uint16_t)b[0];
+          Sw[(size_t)j * D] = (uint16_t)b[0];
       } else if (EPL == 4) {
-        *reinterpret_cast<float4 *>(S + (size_t)j * D) =
+        *reinterpret_cast<float4 *>(Sf + (size_t)j * D) =
             make_float4(st[j][0], st[j][1 % EPL], st[j][2 % EPL], st[j][3 % EPL]);
       } else if (EPL == 2) {
-        *reinterpret_cast<float2 *>(S + (size_t)j * D) = make_float2(st[j][0], st[j][1 % EPL]);
+        *reinterpret_cast<float2 *>(Sf + (size_t)j * D) = make_float2(st[j][0], st[j][1 % EPL]);
       } else {
-        S[(size_t)j * D] = st[j][0];
+        Sf[(size_t)j * D] = st[j][0];
       }
     }
   }
@@ -297,7 +310,7 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   if (tid < R) {
     const float y = s_o[tid] * rstd * nw * siluf_(zv);
     s_y[tid] = y;
-    if (a.y_f32) a.y_f32[(size_t)b * vd + h * D + row0 + tid] = y;
+    if (a.y_f32) a.y_f32[(size_t)io * vd + h * D + row0 + tid] = y;
   }
   __syncthreads();
   if (a.y_codes && tid < R / 16) {
@@ -306,10 +319,10 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
     for (int i = 0; i < 16; ++i) v[i] = s_y[tid * 16 + i];
     uint32_t lo, hi, s;
     if (!quant_block16(v, a.ts_out, inv6ts_of(a.ts_out), lo, hi, s)) flag_status(a.status, GDN_E_NONFINITE);
-    const size_t e0 = (size_t)b * vd + h * D + row0 + tid * 16;
+    const size_t e0 = (size_t)io * vd + h * D + row0 + tid * 16;
     *reinterpret_cast<uint2 *>(a.y_codes + (e0 >> 1)) = make_uint2(lo, hi);
     const int blk = (h * D + row0 + tid * 16) >> 4;
-    a.y_scales[a.y_sf_tiled ? sf_tiled_offset(b, blk, vd >> 4) : (e0 >> 4)] = uint8_t(s);
+    a.y_scales[a.y_sf_tiled ? sf_tiled_offset(io, blk, vd >> 4) : (e0 >> 4)] = uint8_t(s);
   }
 }
 

@@ -201,6 +201,42 @@ class Layer:
                 out[r] = 0
         return out
 
+    def verify(self, x_bits: np.ndarray, slot_ids, conv_state: np.ndarray, ssm_state: np.ndarray):
+        """Speculative verify of r candidate tokens per row: x_bits BF16 [B][r][H].
+        Each live row runs its tokens in order from its slot's state, as r
+        decode steps would; the slots are not modified. Returns (out BF16 bits
+        [B][r][H], snapshots) where snapshots[b][t] = (conv, ssm) after token t
+        (None for padding rows)."""
+        x_bits = np.asarray(x_bits, dtype=np.uint16)
+        B, r = x_bits.shape[0], x_bits.shape[1]
+        qkvz, ba = self.projections(x_bits.reshape(B * r, self.sh.hidden))
+        y = np.zeros((B * r, self.sh.value_dim), dtype=np.float64)
+        snaps = []
+        for b, slot in enumerate(slot_ids):
+            if slot < 0:
+                snaps.append(None)
+                continue
+            c, s = conv_state[slot].copy(), ssm_state[slot].copy()
+            row = []
+            for t in range(r):
+                y[b * r + t], c, s, _ = self.mix(qkvz[b * r + t], ba[b * r + t], c, s)
+                row.append((c.copy(), s.copy()))
+            snaps.append(row)
+        out = self.out_proj(y).reshape(B, r, self.sh.hidden)
+        for b, slot in enumerate(slot_ids):
+            if slot < 0:
+                out[b] = 0
+        return out, snaps
+
+    @staticmethod
+    def verify_commit(slot_ids, accepted, snaps, conv_state: np.ndarray, ssm_state: np.ndarray):
+        """Slot of live row b takes its state after token accepted[b] (0 = unchanged)."""
+        for b, slot in enumerate(slot_ids):
+            n = int(accepted[b])
+            if slot < 0 or n <= 0:
+                continue
+            conv_state[slot], ssm_state[slot] = snaps[b][n - 1]
+
     def prefill(self, x_bits: np.ndarray, conv_state: np.ndarray, ssm_state: np.ndarray,
                 init_zero: bool):
         """Token-by-token prefill of one sequence: x_bits BF16 [T][H]; conv_state

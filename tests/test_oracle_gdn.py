@@ -277,3 +277,40 @@ def test_bf16_state_prefill_carries_fp32_and_rounds_at_the_end():
     for t in range(20):
         L16.decode_step(x[t:t + 1], [0], cc[None], sc[None])
     assert rel_l2(sc, sb) > 0
+
+
+# ------------------------------------------------------------------ verify / commit
+
+def test_verify_then_commit_equals_decode_steps(tiny):
+    """r candidate tokens through verify, then commit of n of them: the outputs
+    are the first decode steps' outputs and the slot ends as after n decode
+    steps; n = 0 leaves the slot as it was; a padding row reads zero."""
+    sh = synth.TINY
+    r = 3
+    slots = [0, -1, 1]
+    x = np.stack([synth.x_tokens(sh, 40 + b, r) for b in range(3)])          # [B][r][H]
+    conv0 = np.stack([synth.conv_state(sh, 100 + s) for s in range(2)])
+    ssm0 = np.stack([synth.ssm_state(sh, 100 + s) for s in range(2)])
+    c, s = conv0.copy(), ssm0.copy()
+    out, snaps = tiny.verify(x, slots, c, s)
+    np.testing.assert_array_equal(c, conv0)                                  # slots untouched
+    np.testing.assert_array_equal(s, ssm0)
+    assert not out[1].any() and snaps[1] is None
+    # decode reference: rows 0 and 2 stepped r times
+    cd, sd = conv0.copy(), ssm0.copy()
+    dec = [tiny.decode_step(x[[0, 2], t], [0, 1], cd, sd) for t in range(r)]
+    for t in range(r):
+        np.testing.assert_array_equal(out[0, t], dec[t][0])
+        np.testing.assert_array_equal(out[2, t], dec[t][1])
+    # commit 0 tokens for slot 0 and 2 tokens for slot 1
+    gdn.Layer.verify_commit(slots, [0, 0, 2], snaps, c, s)
+    np.testing.assert_array_equal(s[0], ssm0[0])
+    c2, s2 = conv0.copy(), ssm0.copy()
+    for t in range(2):
+        tiny.decode_step(x[[0, 2], t], [-1, 1], c2, s2)
+    np.testing.assert_array_equal(s[1], s2[1])
+    np.testing.assert_array_equal(c[1], c2[1])
+    # commit all r for slot 0
+    gdn.Layer.verify_commit(slots, [r, 0, 0], snaps, c, s)
+    np.testing.assert_array_equal(s[0], sd[0])
+    np.testing.assert_array_equal(c[0], cd[0])
