@@ -272,6 +272,39 @@ def time_verify(layers, states, xd, B, r, steps):
             "note": f"{B} sequences x {r} candidate tokens, verify + commit of all"}
 
 
+def time_kda(pkg, synth, M, H, D, state_bf16, hbm_peak, l2, steps):
+    """KDA-style recurrent step for M streams x H heads: a graph of n steps over
+    n distinct state buffers (n x state bytes > 4x L2); us per layer-step and
+    GB/s of algorithmic bytes (state read + write, q/k/v/g/beta in, o out)."""
+    import torch
+    q, k, v, g, beta, S = synth.kda_inputs(M, H, D, 5)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    q, k, v, g, beta = dev(q), dev(k), dev(v), dev(g), dev(beta)
+    es = 2 if state_bf16 else 4
+    sbytes = M * H * D * D * es
+    n = min(256, max(4, -(-4 * l2 // sbytes) + 1))
+    S0 = dev(S)
+    if state_bf16:
+        S0 = S0.to(torch.bfloat16).view(torch.int16)
+    states = [S0.clone() for _ in range(n)]
+    o = torch.empty(M, H, D, dtype=torch.float32, device="cuda")
+
+    def one_pass():
+        for st in states:
+            pkg.kda_step(q, k, v, g, beta, st, o=o)
+    one_pass()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        one_pass()
+    us = time_graph(gr, steps, 3) * 1e3 / n
+    nbytes = 2 * sbytes + (5 * M * H * D + M * H) * 4
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del gr, states
+    return {"us_per_layer_step": round(us, 3), "hbm_gbs": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4),
+            "layers": n, "state": "bf16" if state_bf16 else "f32", "shape": f"M{M} H{H} d{D}"}
+
+
 def time_prefill(pkg, synth, T, reps=3):
     """Prefill of one T-token sequence from zero state (weights stay resident
     in L2 within the call, as they would in a real prompt)."""
@@ -488,6 +521,12 @@ def main():
             torch.cuda.empty_cache()
         extra["bf16state_batch256"] = time_batch(pkg, synth, 256, hbm_peak, state_bf16=True)
         torch.cuda.empty_cache()
+        # KDA-style per-channel recurrent step, 64 heads x 128 (the KDA entry's layer)
+        for M in (1, 8, 32):
+            for sb in (False, True):
+                extra[f"kda_m{M}_{'bf16' if sb else 'f32'}"] = time_kda(pkg, synth, M, 64, 128, sb, hbm_peak, l2,
+                                                                        max(10, args.steps // 4))
+                torch.cuda.empty_cache()
         for T in (1024, 4096, 16384):
             extra[f"prefill{T}"] = time_prefill(pkg, synth, T)
             torch.cuda.empty_cache()

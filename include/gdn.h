@@ -212,6 +212,21 @@ gdn_status gdn_verify_commit(gdn_ctx *ctx, const int32_t *slot_ids, int B, int r
                              const uint16_t *snap_conv, const void *snap_ssm, uint16_t *conv_state,
                              void *ssm_state, int num_slots, void *stream);
 
+/* KDA-style recurrent step: the gated delta rule with one decay per key
+ * channel, for M streams x H heads of size d (Rocket blog, "Moving the KDA
+ * state tile out of shared memory is 4.6x at M=8": a 64 x 128 x 128 state per
+ * stream read and written every step). Per (stream, head), with S [d][d] laid
+ * out [d_v][d_k]:
+ *   S <- S diag(exp(g));  u = beta (v - S k);  S <- S + u k^T;  o = S q
+ * q, k, g (per-channel log-decay), v, o: FP32 [M][H][d]; beta: FP32 [M][H];
+ * state: [M][H][d][d], FP32, or BF16 bits when state_bf16 = 1 (loaded to FP32,
+ * stored rounded to nearest even), updated in place. All device pointers,
+ * 16-byte aligned. No normalisation of q or k inside the step. Asynchronous on
+ * `stream`, allocates nothing. Errors: GDN_E_NULL, GDN_E_SHAPE (M, H < 1,
+ * d not 32/64/128, state_bf16 not 0/1), GDN_E_ALIGN, GDN_E_OVERFLOW, GDN_E_CUDA. */
+gdn_status kda_step(const float *q, const float *k, const float *v, const float *g, const float *beta,
+                    void *state, int state_bf16, int M, int H, int d, float *o, void *stream);
+
 /* The decode step of gdn_decode_step for callers that cannot allocate device
  * memory or keep a context: runtimes that fix all device memory at start-up,
  * work issued while a CUDA graph is captured, hosts that pass only tensors.

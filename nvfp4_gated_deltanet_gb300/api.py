@@ -13,7 +13,7 @@ import torch
 
 from . import GdnConfig, GdnNVFP4, GdnWeights, _check, _ptr, _stream, lib
 
-__all__ = ["nvfp4_quantize", "nvfp4_gemm", "GatedDeltaNetLayer", "layer_from_synth", "status_name"]
+__all__ = ["nvfp4_quantize", "nvfp4_gemm", "kda_step", "GatedDeltaNetLayer", "layer_from_synth", "status_name"]
 
 
 def status_name(status: int) -> str:
@@ -54,6 +54,25 @@ def nvfp4_gemm(a_codes, a_scales, a_ts, b_codes, b_scales, b_ts, out_dtype=torch
                           _stream(stream))
     _check(st, "nvfp4_gemm")
     return c
+
+
+def kda_step(q, k, v, g, beta, state, o=None, stream=None):
+    """KDA-style recurrent step in place on `state` [M][H][d][d] (FP32, or BF16
+    bits as int16/bfloat16); q, k, g, v [M][H][d] and beta [M][H] FP32.
+    Returns o [M][H][d] FP32."""
+    M, H, d = q.shape
+    for t in (q, k, v, g, beta):
+        if t.dtype != torch.float32:
+            raise ValueError("q, k, v, g, beta must be float32")
+    bf16 = state.dtype in (torch.int16, torch.bfloat16)
+    if not bf16 and state.dtype != torch.float32:
+        raise ValueError("state must be float32 or BF16 bits")
+    if o is None:
+        o = torch.empty(M, H, d, dtype=torch.float32, device=q.device)
+    st = lib().kda_step(_ptr(_dev(q)), _ptr(_dev(k)), _ptr(_dev(v)), _ptr(_dev(g)), _ptr(_dev(beta)),
+                        _ptr(_dev(state)), int(bf16), M, H, d, _ptr(_dev(o)), _stream(stream))
+    _check(st, "kda_step")
+    return o
 
 
 class GatedDeltaNetLayer:

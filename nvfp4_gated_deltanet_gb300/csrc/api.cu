@@ -647,6 +647,29 @@ gdn_status gdn_verify_commit(gdn_ctx *ctx, const int32_t *slot_ids, int B, int r
   return cuda_status(launch_verify_commit(v, static_cast<cudaStream_t>(stream)));
 }
 
+gdn_status kda_step(const float *q, const float *k, const float *v, const float *g, const float *beta, void *state,
+                    int state_bf16, int M, int H, int d, float *o, void *stream) {
+  if (!q || !k || !v || !g || !beta || !state || !o) return GDN_E_NULL;
+  if (M < 1 || H < 1 || (d != 32 && d != 64 && d != 128) || (state_bf16 != 0 && state_bf16 != 1)) return GDN_E_SHAPE;
+  if ((long long)M * H > (1LL << 24)) return GDN_E_OVERFLOW;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(state) ||
+      !aligned16(o))
+    return GDN_E_ALIGN;
+  KdaArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.state = state;
+  a.o = o;
+  a.M = M;
+  a.H = H;
+  a.D = d;
+  a.state_bf16 = state_bf16;
+  return cuda_status(launch_kda(a, static_cast<cudaStream_t>(stream)));
+}
+
 gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, const int32_t *slot_ids, int B,
                         float *y, uint16_t *conv_state, void *ssm_state, int num_slots, void *stream) {
   gdn_status st = check_state_args(ctx, qkvz, y, conv_state, ssm_state, num_slots);

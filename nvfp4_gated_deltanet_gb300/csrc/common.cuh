@@ -335,6 +335,17 @@ struct VerifyCommitArgs {
 };
 cudaError_t launch_verify_commit(const VerifyCommitArgs &a, cudaStream_t stream);
 
+// KDA-style recurrent step (kda.cu): per-channel log-decays g.
+struct KdaArgs {
+  const float *q, *k, *g;  // [M][H][D]
+  const float *v;          // [M][H][D]
+  const float *beta;       // [M][H]
+  void *state;             // [M][H][D][D] FP32, or BF16 bits (state_bf16)
+  float *o;                // [M][H][D]
+  int M, H, D, state_bf16;
+};
+cudaError_t launch_kda(const KdaArgs &a, cudaStream_t stream);
+
 struct PrefillArgs {
   const uint16_t *proj;  // [T][ld] BF16: q | k | v | z | b | a
   int ld, T, Tp;         // Tp = T rounded up to whole 64-token chunks

@@ -38,6 +38,7 @@ _STREAM = {
     "conv_w": 7, "A_log": 8, "dt_bias": 9, "norm_w": 10,
     "x": 11, "conv_state": 12, "ssm_state": 13,
     "mat.codes": 14, "mat.scales": 15, "mat.values": 16,
+    "kda": 17,
 }
 
 WEIGHT_TENSOR_SCALE = 2.0 ** -6
@@ -176,3 +177,19 @@ def bf16_normal(rows: int, cols: int, seed: int, std: float = 1.0) -> np.ndarray
 def slot_seed(slot: int) -> int:
     """Per-sequence seed of the multi-sequence decode workloads."""
     return 100 + int(slot)
+
+
+def kda_inputs(M: int, H: int, D: int, seed: int):
+    """Inputs of a KDA-style recurrent step for M streams x H heads, head size D:
+    q, k ~ N(0, 1/D) (norm about 1), v ~ N(0, 1), per-channel log-decay
+    g = -0.5 U(0, 1), beta ~ U(0, 1), all FP32; state N(0, 0.1^2) FP32
+    [M][H][D][D]."""
+    r = rng(seed, "kda")
+    s = 1.0 / np.sqrt(D)
+    q = (s * r.standard_normal(size=(M, H, D))).astype(np.float32)
+    k = (s * r.standard_normal(size=(M, H, D))).astype(np.float32)
+    v = r.standard_normal(size=(M, H, D)).astype(np.float32)
+    g = (-0.5 * r.uniform(0.0, 1.0, size=(M, H, D))).astype(np.float32)
+    beta = r.uniform(0.0, 1.0, size=(M, H)).astype(np.float32)
+    S = (0.1 * r.standard_normal(size=(M, H, D, D))).astype(np.float32)
+    return q, k, v, g, beta, S
