@@ -37,7 +37,7 @@ SEQ_BYTES = 4_194_304 + 98_304 + 4_096 + 4_096                       # 4,300,800
 GEMV_IN_BYTES = 12352 * (1024 + 128)                                  # qkvz+ba codes+scales
 # dram__bytes_read.sum + dram__bytes_write.sum of one in-projection GEMV launch
 # (ncu --set full capture of the decode c1 stack; summary in profiles/)
-GEMV_IN_TRAFFIC = 14_260_480
+GEMV_IN_TRAFFIC = 14_263_040
 
 
 def layer_bytes(sh, state_bf16=False):

@@ -65,6 +65,25 @@ GDN_DEV uint32_t e2m1x2_from_f32(float lo, float hi) {
 }
 
 // One byte of two E2M1 codes -> half2 (low nibble in .x), exact.
+// Four E2M1 pairs (one 32-bit word: element 2i in the low nibble of byte i)
+// to four FP16x2 values, exact. The word is split into its bytes by a vector
+// move, so each pair costs one conversion and no shift or mask.
+GDN_DEV void e2m1x8_to_h2x4(uint32_t w, __half2 (&h)[4]) {
+  uint32_t r0, r1, r2, r3;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(w));
+  h[0] = *reinterpret_cast<__half2 *>(&r0);
+  h[1] = *reinterpret_cast<__half2 *>(&r1);
+  h[2] = *reinterpret_cast<__half2 *>(&r2);
+  h[3] = *reinterpret_cast<__half2 *>(&r3);
+}
+
 GDN_DEV __half2 e2m1x2_to_h2(uint32_t byte) {
   uint32_t h2;
   uint16_t in = uint16_t(byte & 0xFFu);

@@ -26,7 +26,7 @@ constexpr int kBarBytes = kWarps * kMaxStages * 8;  // mbarriers, 256 bytes
 
 // TMA = stream weights through the shared ring (K % 256 == 0, so every copy
 // is 16-byte aligned and sized); otherwise lanes read them from global memory.
-template <int MB, bool TMA>
+template <int MB, bool TMA, int NP>
 __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a, int rows_per_warp, int stages) {
   extern __shared__ __align__(128) unsigned char smem[];
   if (a.early_trigger) pdl_launch_dependents();
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a, int rows_
       float acc[MB];
 #pragma unroll
       for (int m = 0; m < MB; ++m) acc[m] = 0.0f;
-      if (r < nr) dot_row<MB>(codes0 + r * cbytes, scales0 + r * sbytes, npiece, a.M, xh, xs, lane, acc);
+      if (r < nr) dot_row<MB, NP>(codes0 + r * cbytes, scales0 + r * sbytes, npiece, a.M, xh, xs, lane, acc);
 #pragma unroll
       for (int m = 0; m < MB; ++m) v[r * MB + m] = acc[m];
     }
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(GemvArgs a, int rows_
   }
 }
 
-template <int MB, bool TMA>
+template <int MB, bool TMA, int NP>
 cudaError_t launch_cfg(const GemvArgs &a, const LaunchCtx &lc) {
   const int npiece = a.K >> 5;
   const size_t act = (size_t)MB * npiece * (4 * sizeof(uint4) + 2 * sizeof(float));
@@ -200,7 +200,7 @@ cudaError_t launch_cfg(const GemvArgs &a, const LaunchCtx &lc) {
   if (smem > budget) return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MB, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MB, TMA, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -215,13 +215,16 @@ cudaError_t launch_cfg(const GemvArgs &a, const LaunchCtx &lc) {
   attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<MB, TMA>, a, rpw, stages);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<MB, TMA, NP>, a, rpw, stages);
 }
 
 template <int MB>
 cudaError_t launch_mb(const GemvArgs &a, const LaunchCtx &lc) {
-  if (a.K % 256 == 0) return launch_cfg<MB, true>(a, lc);
-  return launch_cfg<MB, false>(a, lc);
+  // the layer's two reduction lengths get fully unrolled dot products
+  if (a.K == 2048) return launch_cfg<MB, true, 64>(a, lc);
+  if (a.K == 4096) return launch_cfg<MB, true, 128>(a, lc);
+  if (a.K % 256 == 0) return launch_cfg<MB, true, 0>(a, lc);
+  return launch_cfg<MB, false, 0>(a, lc);
 }
 
 }  // namespace

@@ -13,28 +13,40 @@ namespace gdn {
 //   xh[((m * 2 + blk) * 2 + half) * npiece + p] : uint4 = 4 half2 (8 values)
 //   xs[(m * 2 + blk) * npiece + p]              : float E4M3 block scale
 
-template <int MB>
+// NP = number of pieces per row when known at compile time (a multiple of
+// 32: every lane then takes NP/32 pieces, fully unrolled, with constant shared
+// offsets), 0 = npiece at run time. The arithmetic is the same either way.
+template <int MB, int NP = 0>
 GDN_DEV void dot_row(const uint8_t *codes, const uint8_t *scales, int npiece, int M, const uint4 *xh,
                      const float *xs, int lane, float (&acc)[MB]) {
-  for (int p = lane; p < npiece; p += 32) {
+  static_assert(NP % 32 == 0, "NP multiple of 32");
+  const int np = NP ? NP : npiece;
+  const int iters = NP ? NP / 32 : (npiece - lane + 31) / 32;
+#pragma unroll
+  for (int it = 0; it < (NP ? NP / 32 : iters); ++it) {
+    const int p = lane + 32 * it;
     const uint4 wc = *reinterpret_cast<const uint4 *>(codes + (size_t)p * 16);
     const uint32_t ws = *reinterpret_cast<const uint16_t *>(scales + (size_t)p * 2);
+    float swv[2];
+    {  // both blocks' weight scales with one conversion (exact)
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(uint16_t(ws)));
+      swv[0] = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFFu)));
+      swv[1] = __half2float(__ushort_as_half(uint16_t(h2 >> 16)));
+    }
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
       const uint32_t w0 = blk == 0 ? wc.x : wc.z;
       const uint32_t w1 = blk == 0 ? wc.y : wc.w;
       __half2 wv[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        wv[i] = e2m1x2_to_h2(w0 >> (8 * i));
-        wv[4 + i] = e2m1x2_to_h2(w1 >> (8 * i));
-      }
-      const float sw = e4m3_to_f32(ws >> (8 * blk));
+      e2m1x8_to_h2x4(w0, *reinterpret_cast<__half2(*)[4]>(&wv[0]));
+      e2m1x8_to_h2x4(w1, *reinterpret_cast<__half2(*)[4]>(&wv[4]));
+      const float sw = swv[blk];
 #pragma unroll
       for (int m = 0; m < MB; ++m) {
         if (m < M) {
-          const uint4 x0 = xh[((m * 2 + blk) * 2 + 0) * npiece + p];
-          const uint4 x1 = xh[((m * 2 + blk) * 2 + 1) * npiece + p];
+          const uint4 x0 = xh[((m * 2 + blk) * 2 + 0) * np + p];
+          const uint4 x1 = xh[((m * 2 + blk) * 2 + 1) * np + p];
           const __half2 *xa = reinterpret_cast<const __half2 *>(&x0);
           const __half2 *xb = reinterpret_cast<const __half2 *>(&x1);
           __half2 s2 = __float2half2_rn(0.0f);
@@ -43,7 +55,7 @@ GDN_DEV void dot_row(const uint8_t *codes, const uint8_t *scales, int npiece, in
 #pragma unroll
           for (int i = 0; i < 4; ++i) s2 = __hfma2(wv[4 + i], xb[i], s2);
           const float blocksum = __low2float(s2) + __high2float(s2);
-          acc[m] = fmaf(blocksum, xs[(m * 2 + blk) * npiece + p] * sw, acc[m]);
+          acc[m] = fmaf(blocksum, xs[(m * 2 + blk) * np + p] * sw, acc[m]);
         }
       }
     }
