@@ -236,10 +236,24 @@ GDN_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Every wait is bounded: ~2^31 SM cycles (about one second at 2 GHz), then the
 // caller records GDN_E_TIMEOUT and gives up instead of hanging the GPU.
 constexpr long long kWaitCycles = 1LL << 31;
+// The same test with a suspend-time hint: the thread sleeps until the phase
+// completes or about `ns` nanoseconds pass, instead of spinning on the issue
+// slots its neighbours need.
+GDN_DEV bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 GDN_DEV bool mbar_wait(uint64_t *bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_sleep(bar, parity, 20000u))
     if (clock64() - t0 > kWaitCycles) return false;
   return true;
 }
