@@ -37,7 +37,7 @@ SEQ_BYTES = 4_194_304 + 98_304 + 4_096 + 4_096                       # 4,300,800
 GEMV_IN_BYTES = 12352 * (1024 + 128)                                  # qkvz+ba codes+scales
 # dram__bytes_read.sum + dram__bytes_write.sum of one in-projection GEMV launch
 # (ncu --set full capture of the decode c1 stack; summary in profiles/)
-GEMV_IN_TRAFFIC = 14_263_040
+GEMV_IN_TRAFFIC = 14_252_288
 
 
 def layer_bytes(sh, state_bf16=False):
@@ -179,24 +179,18 @@ def time_graph(g, steps, warmup):
     return e0.elapsed_time(e1) / steps  # ms per bench step
 
 
-def time_gemv(pkg, layers, xcodes, xscales, steps):
-    """The dominant kernel alone: the W4A4 projection GEMV over the stack's
-    qkvz+ba weights (1 activation row, N = 12288 + 64 rows, K = 2048), one
-    launch per layer instance, timed with CUDA events on the launching stream.
-    It is the CUDA-core kernel the c1 decode step runs (selected with tuning
-    knob 0 = 1 for this measurement, restored afterwards)."""
+def time_gemv(pkg, layers, xd, steps):
+    """The dominant kernel alone: the one-row W4A4 in-projection (q|k|v|z|b|a:
+    N = 12288 + 64 rows, K = 2048) of every layer instance of the stack, one
+    launch each through gdn_in_proj (the kernel gdn_decode_step runs for one
+    row), captured as one graph and timed with CUDA events on its stream."""
     import torch
-    pkg.lib().gdn_set_tuning(0, 1)
-    import numpy as np
-    from nvfp4_gated_deltanet_gb300 import synth
-    w = synth.layer_weights(synth.FULL, 1)
-    wc = np.concatenate([w.qkvz.codes, w.ba.codes])
-    ws = np.concatenate([w.qkvz.scales, w.ba.scales])
-    mats = [(torch.from_numpy(wc).cuda(), torch.from_numpy(ws).cuda()) for _ in range(len(layers))]
-    c = torch.empty(1, wc.shape[0], dtype=torch.bfloat16, device="cuda")
+    outs = [None] * len(layers)
+    x1 = xd[:1].contiguous()
+
     def one_pass():
-        for (a, b) in mats:
-            pkg.nvfp4_gemm(xcodes, xscales, 2.0 ** -8, a, b, 2.0 ** -6, c=c)
+        for i, L in enumerate(layers):
+            outs[i] = L.in_proj(x1, out=outs[i])
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -207,8 +201,7 @@ def time_gemv(pkg, layers, xcodes, xscales, steps):
     with torch.cuda.graph(g):
         one_pass()
     ms = time_graph(g, steps, 3)
-    pkg.lib().gdn_set_tuning(0, 0)
-    return ms / len(mats) * 1e3, len(mats)  # us per launch
+    return ms / len(layers) * 1e3, len(layers)  # us per launch
 
 
 def time_batch(pkg, synth, B, hbm_peak, n_layers=2, steps=10, state_bf16=False):
@@ -451,8 +444,7 @@ def main():
     gbs_step = step_bytes(1) / (us_layer * 1e-6) / 1e9
 
     # ---- dominant kernel: the projection GEMV alone, live
-    xq, xs = pkg.nvfp4_quantize(xd[:1], 2.0 ** -8)
-    us_gemv, _ = time_gemv(pkg, layers, xq, xs, max(20, args.steps // 4))
+    us_gemv, _ = time_gemv(pkg, layers, xd, max(20, args.steps // 4))
     gemv_gbs = GEMV_IN_BYTES / (us_gemv * 1e-6) / 1e9
 
     # ---- e2e: the Python API with host buffers, copies inside the timed region
@@ -542,7 +534,7 @@ def main():
                                 f"({l2 / 1e6:.0f} MB)", "graph": "one CUDA graph per bucket over the stack",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs_step": round(gbs_step, 1), "hbm_frac_step": round(gbs_step / hbm_peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<1,1> (W4A4 qkvz+ba projection on CUDA cores, 1 row)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_mma_kernel (one-row W4A4 q|k|v|z|b|a projection, warp-MMA block products)",
                      "achieved": round(gemv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(gemv_gbs / hbm_peak, 4), "peak_kind": peak_kind, "traffic": GEMV_IN_TRAFFIC,
                      "us_per_launch": round(us_gemv, 3), "bytes_per_launch": GEMV_IN_BYTES},

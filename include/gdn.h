@@ -159,6 +159,15 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
                            uint16_t *out, uint16_t *conv_state, void *ssm_state, int num_slots,
                            void *stream);
 
+/* The in-projection stage of gdn_decode_step alone (for stage-wise checks and
+ * timing): x BF16 [B][H] -> proj BF16 [B][2*Hk*d_k + 2*Hv*d_v + 2*Hv], each
+ * row q | k | v | z | b | a; rows whose slot_ids entry is negative are zero
+ * (slot_ids: device int32 [B], or NULL for none). Same kernels and results as
+ * inside gdn_decode_step. Errors: GDN_E_NULL, GDN_E_ALIGN, GDN_E_SHAPE
+ * (B < 1 or > max_batch), GDN_E_CUDA. */
+gdn_status gdn_in_proj(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *proj,
+                       void *stream);
+
 /* The token-mixing stage of gdn_decode_step alone, for stage-wise checks and
  * for callers that run the projections themselves: takes the BF16 projection
  * outputs qkvz [B][2*Hk*d_k + 2*Hv*d_v] and ba [B][2*Hv] and writes the FP32
@@ -271,7 +280,10 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * 128 x 256 tile (0 and 2 = yes, the default; 1 = tensor-map copies from the
  * row-major codes). knob 7: d_v slices per head in the decode mixing kernel
  * (0 = chosen from the batch, the default; 1, 2 or 4, reduced while the
- * cluster of a key head would exceed 8 CTAs).
+ * cluster of a key head would exceed 8 CTAs). knob 8: one-row projections
+ * of a context on the CUDA cores take the block dot products with warp-level
+ * MMA (mma.sync, FP16 in, FP32 out; weights repacked at create) instead of
+ * FP16x2 chains (0 and 2 = yes, the default; 1 = no).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

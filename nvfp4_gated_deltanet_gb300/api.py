@@ -141,6 +141,16 @@ class GatedDeltaNetLayer:
         _check(st, "gdn_mix_step")
         return y
 
+    def in_proj(self, x, slot_ids=None, out=None, stream=None):
+        """x [B][H] -> the in-projection rows [B][Nin] BF16 bits (q|k|v|z|b|a)."""
+        B = x.shape[0]
+        nin = 2 * self.Hk * self.D + 2 * self.Hv * self.D + 2 * self.Hv
+        if out is None:
+            out = torch.empty(B, nin, dtype=torch.int16, device=x.device)
+        st = lib().gdn_in_proj(self._ctx, _ptr(_dev(x)), _ptr(slot_ids), B, _ptr(_dev(out)), _stream(stream))
+        _check(st, "gdn_in_proj")
+        return out
+
     def new_snapshots(self, B: int, r: int, device="cuda"):
         """Snapshot buffers of a verify pass: conv [B][r][K-1][C] BF16 bits and
         recurrent [B][r][Hv][dv][dk] in the layer's state type."""

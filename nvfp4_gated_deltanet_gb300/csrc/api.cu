@@ -27,6 +27,7 @@ struct gdn_ctx {
   uint8_t *xq_codes, *xq_scales;        // [prow][H/2] and tiled scales: x as NVFP4 for the tensor-core GEMM
   uint8_t *w_in_sf_t, *w_out_sf_t;      // the weights' scales in the tiled layout tcgen05.cp reads
   uint8_t *w_in_tiles, *w_out_tiles;    // the weights' codes as pre-swizzled 16 KB MMA tiles
+  uint8_t *w_in_mma, *w_out_mma;        // the weights in the warp-MMA one-row layout
   TcGemm tc_in, tc_out;                 // weight tensor maps of the two projections
   bool tc_in_ok, tc_out_ok;             // K % 256 == 0: the tcgen05 path applies
   int32_t *status;
@@ -55,6 +56,7 @@ struct Tuning {
                            // out-projection only), 1 off, 2 on
   int swizzled_tiles = 0;  // tensor-core weights from the pre-swizzled tile copy: 0 auto (on), 1 off, 2 on
   int mix_slices = 0;      // d_v slices per head in the mixing kernel: 0 auto, 1, 2, 4
+  int gemv_mma = 0;        // one-row projections with warp-level MMA block products: 0 auto (on), 1 off, 2 on
 };
 Tuning g_tune;
 
@@ -156,7 +158,8 @@ MixArgs mix_args(gdn_ctx *c) {
 // x (BF16 rows, padding rows masked by row_slot) -> the in-projection
 // (q|k|v|z|b|a, BF16, ldc = Nin) on tensor cores, or on the CUDA cores.
 cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t *row_slot, int num_slots,
-                        const LaunchCtx &lc, bool allow_tc) {
+                        const LaunchCtx &lc, bool allow_tc, uint16_t *dst = nullptr) {
+  if (!dst) dst = ctx->proj;
   const gdn_config &c = ctx->cfg;
   if (allow_tc && ctx->tc_in_ok && use_tensor_cores(rows)) {
     TcGemm t = ctx->tc_in;
@@ -176,7 +179,7 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
     t.args.Ma = ctx->Nin;
     t.args.Nb = rows;
     t.args.K = c.hidden;
-    t.args.c = ctx->proj;
+    t.args.c = dst;
     t.args.ldc = ctx->Nin;
     t.args.c_is_bf16 = 1;
     t.args.ts_a0 = ctx->ts_qkvz;
@@ -201,12 +204,13 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
   g.ts_w0 = ctx->ts_qkvz;
   g.ts_w1 = ctx->ts_ba;
   g.n_split = ctx->Nqkvz;
-  g.c = ctx->proj;
+  g.c = dst;
   g.c_is_bf16 = 1;
   g.ldc = ctx->Nin;
   g.N = ctx->Nin;
   g.K = c.hidden;
   g.status = ctx->status;
+  g.w_mma = g_tune.gemv_mma != 1 ? ctx->w_in_mma : nullptr;
   return run_gemv(g, lc, rows);
 }
 
@@ -256,6 +260,7 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
   o.N = c.hidden;
   o.K = ctx->Vd;
   o.status = ctx->status;
+  o.w_mma = g_tune.gemv_mma != 1 ? ctx->w_out_mma : nullptr;
   // measured slower for the one-row GEMV chain (its weight prefetch then
   // competes with the mixing kernel), so only on request
   o.early_trigger = early && g_tune.early_trigger == 2 && rows <= 16;  // one launch, the step's last
@@ -334,6 +339,10 @@ gdn_status gdn_set_tuning(int knob, int value) {
       if (value != 0 && value != 1 && value != 2 && value != 4) return GDN_E_RANGE;
       g_tune.mix_slices = value;
       return GDN_OK;
+    case 8:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      g_tune.gemv_mma = value;
+      return GDN_OK;
     default:
       return GDN_E_RANGE;
   }
@@ -410,6 +419,8 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_out_sf_t, sf_tiled_bytes((int)H, (int)Vd));
   if (e == cudaSuccess && H % 256 == 0) e = ctx_alloc(ctx, &ctx->w_in_tiles, swizzled_tiles_bytes((int)Nin, (int)H));
   if (e == cudaSuccess && Vd % 256 == 0) e = ctx_alloc(ctx, &ctx->w_out_tiles, swizzled_tiles_bytes((int)H, (int)Vd));
+  if (e == cudaSuccess && H % 256 == 0) e = ctx_alloc(ctx, &ctx->w_in_mma, mma_tiles_bytes((int)Nin, (int)H));
+  if (e == cudaSuccess && Vd % 256 == 0) e = ctx_alloc(ctx, &ctx->w_out_mma, mma_tiles_bytes((int)H, (int)Vd));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->status, 1);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->grid_bar, 4);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->conv_tmp, (c.conv_kernel - 1) * Cc);
@@ -446,6 +457,10 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess && Vd % 64 == 0) e = launch_tile_scales(ctx->w_out_scales, (int)H, (int)Vd, ctx->w_out_sf_t, s);
   if (e == cudaSuccess && H % 256 == 0) e = launch_swizzle_tiles(ctx->w_in_codes, (int)Nin, (int)H, ctx->w_in_tiles, s);
   if (e == cudaSuccess && Vd % 256 == 0) e = launch_swizzle_tiles(ctx->w_out_codes, (int)H, (int)Vd, ctx->w_out_tiles, s);
+  if (e == cudaSuccess && H % 256 == 0)
+    e = launch_mma_tiles(ctx->w_in_codes, ctx->w_in_scales, (int)Nin, (int)H, ctx->w_in_mma, s);
+  if (e == cudaSuccess && Vd % 256 == 0)
+    e = launch_mma_tiles(ctx->w_out_codes, ctx->w_out_scales, (int)H, (int)Vd, ctx->w_out_mma, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->status, 0, 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->grid_bar, 0, 16, s);
   if (e == cudaSuccess) {
@@ -668,6 +683,16 @@ gdn_status kda_step(const float *q, const float *k, const float *v, const float 
   a.D = d;
   a.state_bf16 = state_bf16;
   return cuda_status(launch_kda(a, static_cast<cudaStream_t>(stream)));
+}
+
+gdn_status gdn_in_proj(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *proj,
+                       void *stream) {
+  if (!ctx || !x || !proj) return GDN_E_NULL;
+  if (!aligned16(x) || !aligned16(proj) || (slot_ids && !aligned16(slot_ids))) return GDN_E_ALIGN;
+  if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, false};
+  // a row is zero when its slot id is negative (no slot range to check here)
+  return cuda_status(run_in_proj(ctx, x, B, slot_ids, 0x7fffffff, lc, true, proj));
 }
 
 gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba, const int32_t *slot_ids, int B,

@@ -318,8 +318,17 @@ struct GemvArgs {
   int M, N, K;
   int32_t *status;
   int early_trigger;  // as TcArgs::early_trigger
+  // Optional: the weights repacked for the warp-MMA one-row kernel
+  // (launch_mma_tiles); used when M == 1 and K % 256 == 0.
+  const uint8_t *w_mma;
 };
 cudaError_t launch_gemv(const GemvArgs &a, const LaunchCtx &lc);
+// Warp-MMA one-row product (gemv_mma.cu) and its weight layout.
+bool gemv_mma_ok(const GemvArgs &a);
+cudaError_t launch_gemv_mma(const GemvArgs &a, const LaunchCtx &lc);
+size_t mma_tiles_bytes(int rows, int K);
+cudaError_t launch_mma_tiles(const uint8_t *codes, const uint8_t *scales, int rows, int K, uint8_t *dst,
+                             cudaStream_t stream);
 
 struct MixArgs {
   const uint16_t *qkvz;  // [B][ld_qkvz] BF16: q | k | v | z

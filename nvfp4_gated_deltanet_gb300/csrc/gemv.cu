@@ -231,6 +231,7 @@ cudaError_t launch_mb(const GemvArgs &a, const LaunchCtx &lc) {
 
 cudaError_t launch_gemv(const GemvArgs &a, const LaunchCtx &lc) {
   if (a.M <= 0 || a.N <= 0) return cudaSuccess;
+  if (gemv_mma_ok(a)) return launch_gemv_mma(a, lc);
   if (a.M == 1) return launch_mb<1>(a, lc);
   if (a.M == 2) return launch_mb<2>(a, lc);
   if (a.M <= 4) return launch_mb<4>(a, lc);

@@ -129,6 +129,7 @@ def test_batch_rows_equal_single_rows(api, path):
     shape = synth.FULL
     L = _layer(api, "FULL", 1)
     api.lib().gdn_set_tuning(0, path)
+    api.lib().gdn_set_tuning(8, 1)   # one row on the same FP16 GEMV as five
     try:
         slots = [0, 1, 2, 3, 4]
         x, conv0, ssm0 = slot_inputs(shape, slots, 1)
@@ -146,6 +147,36 @@ def test_batch_rows_equal_single_rows(api, path):
                 assert rel_l2(to_host(s1)[i], to_host(sb)[i]) <= 1e-5
     finally:
         api.lib().gdn_set_tuning(0, 0)
+        api.lib().gdn_set_tuning(8, 0)
+
+
+@pytest.mark.parametrize("shape_name,seed", [("TINY", 0), ("FULL", 1), ("TP2", 1)])
+def test_one_row_warp_mma_gemv_matches_fp16_gemv_and_oracle(api, shape_name, seed):
+    """The one-row projections with warp-level MMA block products (knob 8,
+    the default) against the FP16x2-chain GEMV (knob 8 = 1) and the oracle:
+    both exact per 16-block, FP32 across blocks in different orders, so the
+    step's outputs agree to the BF16 tolerance and the states to 1e-5."""
+    shape = getattr(synth, shape_name)
+    L = _layer(api, shape_name, seed)
+    O = oracle_layer(shape_name, seed)
+    x, conv0, ssm0 = slot_inputs(shape, [0], 4)
+    ids = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {}
+    try:
+        for knob in (1, 2):
+            api.lib().gdn_set_tuning(8, knob)
+            c, s = to_dev(conv0), to_dev(ssm0)
+            outs = np.stack([to_host(L.decode_step(to_dev(x[t]), ids, c, s)) for t in range(4)])
+            assert L.check() == 0
+            res[knob] = (outs, to_host(s))
+    finally:
+        api.lib().gdn_set_tuning(8, 0)
+    assert rel_l2(_bf16(res[2][0]), _bf16(res[1][0])) <= 4e-3
+    assert rel_l2(res[2][1], res[1][1]) <= 1e-5
+    c, s = conv0.copy(), ssm0.copy()
+    want = np.stack([O.decode_step(x[t], [0], c, s) for t in range(4)])
+    assert rel_l2(_bf16(res[2][0]), _bf16(want)) <= 4e-3
+    assert rel_l2(res[2][1], s) <= 1e-4
 
 
 def test_fused_single_kernel_step_matches_oracle(api):
@@ -212,3 +243,26 @@ def test_in_projection_quantising_inside_the_gemm(api, shape_name, B):
     if B > 1:
         assert not got[:, 1].any()                      # padding row: zero output
         np.testing.assert_array_equal(ssm_g[1], ssm0[1])  # and its slot untouched
+
+
+def test_in_proj_stage_matches_oracle_projections(api):
+    """gdn_in_proj (the in-projection alone, one row and four rows, one padding
+    row): the BF16 projections against the oracle's exact W4A4 product rounded
+    to BF16 -- equal up to the FP32 summation order of the blocks (rel-L2 <= 1e-5
+    on the BF16 values, most elements bit-equal)."""
+    shape = synth.FULL
+    L = _layer(api, "FULL", 1)
+    O = oracle_layer("FULL", 1)
+    for B in (1, 4):
+        x, _, _ = slot_inputs(shape, list(range(B)), 1)
+        ids = list(range(B))
+        if B > 1:
+            ids[2] = -1
+        got = to_host(L.in_proj(to_dev(x[0]), torch.tensor(ids, dtype=torch.int32, device="cuda")))
+        qkvz, ba = O.projections(x[0])
+        want = np.concatenate([qkvz, ba], axis=1)
+        live = [i for i in range(B) if ids[i] >= 0]
+        assert rel_l2(_bf16(got[live]), want[live]) <= 1e-5
+        assert np.mean(_bf16(got[live]) == want[live]) > 0.99
+        if B > 1:
+            assert not got[2].any()
