@@ -22,6 +22,7 @@ struct gdn_ctx {
   uint16_t *proj;                       // [prow][Nin] BF16 projection outputs
   uint8_t *y_codes, *y_scales;          // [prow][Vd/2], [prow][Vd/16]
   float *qn, *kn, *v, *beta, *gl, *o;     // prefill intermediates (head-major, chunk-padded)
+  BatchWs bws;                          // large-batch decode intermediates, max_batch rows
   float *W, *Ut, *Am, *Gam;               // per (value head, 64-token chunk) products
   uint16_t *conv_tmp;                   // [K-1][C]
   uint8_t *xq_codes, *xq_scales;        // [prow][H/2] and tiled scales: x as NVFP4 for the tensor-core GEMM
@@ -57,6 +58,7 @@ struct Tuning {
   int swizzled_tiles = 0;  // tensor-core weights from the pre-swizzled tile copy: 0 auto (on), 1 off, 2 on
   int mix_slices = 0;      // d_v slices per head in the mixing kernel: 0 auto, 1, 2, 4
   int gemv_mma = 0;        // one-row projections with warp-level MMA block products: 0 auto (on), 1 off, 2 on
+  int batch_split = 0;     // decode mixing as prep / delta / gated-norm kernels: 0 auto (B >= 32), 1 off, 2 on
 };
 Tuning g_tune;
 
@@ -343,6 +345,10 @@ gdn_status gdn_set_tuning(int knob, int value) {
       if (value < 0 || value > 2) return GDN_E_RANGE;
       g_tune.gemv_mma = value;
       return GDN_OK;
+    case 9:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      g_tune.batch_split = value;
+      return GDN_OK;
     default:
       return GDN_E_RANGE;
   }
@@ -413,6 +419,15 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->norm_w, D);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->proj, prow * Nin);
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_codes, prow * Vd / 2);
+  {
+    const size_t mb = (size_t)c.max_batch;
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->bws.qn, mb * Hk * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->bws.kn, mb * Hk * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->bws.v, mb * Hv * D);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->bws.beta, mb * Hv);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->bws.gl, mb * Hv);
+    if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->bws.o, mb * Hv * D);
+  }
   // scales sized for both layouts: row-major, or tiled (rows padded to 128)
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->y_scales, sf_tiled_bytes((int)prow, (int)Vd));
   if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->w_in_sf_t, sf_tiled_bytes((int)Nin, (int)H));
@@ -584,7 +599,9 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   m.y_scales = ctx->y_scales;
   m.y_sf_tiled = out_proj_tiled(ctx, B) ? 1 : 0;
   m.y_f32 = nullptr;
-  e = launch_mix(m, lc);
+  // large batches: the state stream in a kernel of its own (bit-identical)
+  const bool split = g_tune.batch_split == 2 || (g_tune.batch_split == 0 && B >= 32);
+  e = split ? launch_batch_mix(m, ctx->bws, lc) : launch_mix(m, lc);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(run_out_proj(ctx, out, B, lc, true, true));
 }

@@ -363,6 +363,16 @@ struct MixArgs {
 };
 cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc);
 
+// Large-batch token mixing split in three kernels (batch.cu), bit-identical
+// to launch_mix; the workspace holds the per-row intermediates.
+struct BatchWs {
+  float *qn, *kn;     // [B][Hk][D]: normalised q (times d^-1/2) and k
+  float *v;           // [B][Hv][D]: conv output of the v channels
+  float *beta, *gl;   // [B][Hv]
+  float *o;           // [B][Hv][D]: delta-rule output
+};
+cudaError_t launch_batch_mix(const MixArgs &a, const BatchWs &w, const LaunchCtx &lc);
+
 // Commit of a verify pass (verify.cu): row b with slot s >= 0 and accepted[b]
 // = n in 1..r takes snapshot (b, n-1) as its slot's state; n = 0 keeps it.
 struct VerifyCommitArgs {
