@@ -285,7 +285,7 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * MMA (mma.sync, FP16 in, FP32 out; weights repacked at create) instead of
  * FP16x2 chains (0 and 2 = yes, the default; 1 = no). knob 9: the decode
  * token mixing as three kernels -- conv/norms/gates, the delta rule alone,
- * gated norm + quantisation -- with bit-identical results (0 = from 32 rows,
+ * gated norm + quantisation -- with bit-identical results (0 = from 96 rows,
  * the default; 1 = never; 2 = always).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */

@@ -1,8 +1,8 @@
 // Token mixing of a large decode batch in three kernels, so the state stream
 // gets a kernel of its own:
-//   batch_prep_kernel   conv + SiLU per (row, head of channels), q/k L2 norm,
-//                       beta and the log-decay per (row, value head); the row's
-//                       conv state is shifted in place
+//   batch_prep_kernel   conv + SiLU of a whole row, q/k L2 norms, beta and the
+//                       log-decay per value head; the row's conv state is
+//                       shifted in place
 //   batch_delta_kernel  the gated delta rule: per (row, value head, d_v slice)
 //                       the state rows in registers, nothing else -- the part
 //                       that moves 4 MB per row
@@ -30,73 +30,75 @@ GDN_DEV bool row_live(const MixArgs &a, int b, int lane, int &slot, bool &bad) {
   return live;
 }
 
+// One CTA per row (1024 threads, channel c handled by thread c % 1024): the
+// conv over every channel into shared memory, one warp per q/k head for its
+// L2 norm (lane-local sums then the butterfly, as in the fused kernel), the
+// gates by the first Hv threads. Shared memory: C floats of conv output.
+constexpr int kPrepThreads = 1024;
+
 template <int D>
-__global__ void __launch_bounds__(D) batch_prep_kernel(MixArgs a, BatchWs w) {
+__global__ void __launch_bounds__(kPrepThreads) batch_prep_kernel(MixArgs a, BatchWs w) {
   constexpr int EPL = D / 32;
-  __shared__ float s_y[D];
-  __shared__ float s_r;
-  const int grp = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ngrp = 2 * a.Hk + a.Hv;
+  extern __shared__ float s_y[];   // [C] conv outputs, then 2*Hk norm factors
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Kc = a.Kc, C = a.C, nqk = 2 * a.Hk;
+  float *s_r = s_y + C;
   int slot;
   bool bad;
   const bool live = row_live(a, b, lane, slot, bad);
-  if (grp == ngrp) {  // gates for every value head of the row
-    pdl_wait();
-    pdl_launch_dependents();
-    if (bad && tid == 0) flag_status(a.status, GDN_E_RANGE);
-    if (!live) return;
-    const uint16_t *bain = a.ba + (size_t)b * a.ld_ba;
-    for (int h = tid; h < a.Hv; h += blockDim.x) {
-      const float b_raw = bf16_bits_to_f32(bain[h]);
-      const float a_raw = bf16_bits_to_f32(bain[a.Hv + h]);
-      w.beta[(size_t)b * a.Hv + h] = sigmoidf_(b_raw);
-      w.gl[(size_t)b * a.Hv + h] = -expf(a.A_log[h]) * softplusf_(a_raw + a.dt_bias[h]);
-    }
-    return;
-  }
-  const int Kc = a.Kc, C = a.C;
-  const int c = grp * D + tid;  // conv channel: q heads, k heads, then v heads
-  float cw[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) cw[j] = j < Kc ? bf16_bits_to_f32(a.conv_w[(size_t)c * Kc + j]) : 0.0f;
   uint16_t *cst = a.conv_state + (size_t)(live ? slot : 0) * (Kc - 1) * C;
-  uint16_t tap[3] = {0, 0, 0};
-  if (live)
-    for (int j = 0; j < Kc - 1; ++j) tap[j] = cst[(size_t)j * C + c];
   pdl_wait();  // the projections come from the preceding kernel
   pdl_launch_dependents();
+  if (bad && tid == 0) flag_status(a.status, GDN_E_RANGE);
   if (!live) return;
-  const uint16_t xn = a.qkvz[(size_t)b * a.ld_qkvz + c];
-  float pre = 0.0f;
+  const uint16_t *xin = a.qkvz + (size_t)b * a.ld_qkvz;
+  for (int c = tid; c < C; c += kPrepThreads) {
+    uint16_t tap[3] = {0, 0, 0};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j < Kc) {
-      const uint16_t bits = j < Kc - 1 ? tap[j < 3 ? j : 2] : xn;
-      pre = fmaf(cw[j], bf16_bits_to_f32(bits), pre);
+    for (int j = 0; j < 3; ++j)
+      if (j < Kc - 1) tap[j] = cst[(size_t)j * C + c];
+    const uint16_t xn = xin[c];
+    float pre = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < Kc) {
+        const uint16_t bits = j < Kc - 1 ? tap[j < 3 ? j : 2] : xn;
+        pre = fmaf(bf16_bits_to_f32(a.conv_w[(size_t)c * Kc + j]), bf16_bits_to_f32(bits), pre);
+      }
     }
+    s_y[c] = siluf_(pre);
+    // the channel's conv state: taps shift by one, newest raw input last
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (j < Kc - 2) cst[(size_t)j * C + c] = tap[j + 1];
+    cst[(size_t)(Kc - 2) * C + c] = xn;
   }
-  const float out = siluf_(pre);
-  // this CTA owns these channels' conv state
-  for (int j = 0; j < Kc - 2; ++j) cst[(size_t)j * C + c] = tap[j + 1 < 3 ? j + 1 : 2];
-  cst[(size_t)(Kc - 2) * C + c] = xn;
-  if (grp < 2 * a.Hk) {  // q or k head: L2 norm, lane-local sums then the butterfly
-    s_y[tid] = out;
-    __syncthreads();
-    if (warp == 0) {
-      float ss = 0.0f;
+  if (tid < a.Hv) {  // gates
+    const uint16_t *bain = a.ba + (size_t)b * a.ld_ba;
+    const float b_raw = bf16_bits_to_f32(bain[tid]);
+    const float a_raw = bf16_bits_to_f32(bain[a.Hv + tid]);
+    w.beta[(size_t)b * a.Hv + tid] = sigmoidf_(b_raw);
+    w.gl[(size_t)b * a.Hv + tid] = -expf(a.A_log[tid]) * softplusf_(a_raw + a.dt_bias[tid]);
+  }
+  __syncthreads();
+  for (int hq = warp; hq < nqk; hq += kPrepThreads / 32) {  // q heads, then k heads
+    float ss = 0.0f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) ss = fmaf(s_y[lane * EPL + e], s_y[lane * EPL + e], ss);
-      ss = warp_sum(ss);
-      if (lane == 0)
-        s_r = grp < a.Hk ? (1.0f / sqrtf(ss + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(ss + a.l2_eps);
-    }
-    __syncthreads();
-    float *dst = grp < a.Hk ? w.qn : w.kn;
-    const int kh = grp < a.Hk ? grp : grp - a.Hk;
-    dst[((size_t)b * a.Hk + kh) * D + tid] = out * s_r;
-  } else {
-    const int h = grp - 2 * a.Hk;
-    w.v[((size_t)b * a.Hv + h) * D + tid] = out;
+    for (int e = 0; e < EPL; ++e) ss = fmaf(s_y[hq * D + lane * EPL + e], s_y[hq * D + lane * EPL + e], ss);
+    ss = warp_sum(ss);
+    if (lane == 0)
+      s_r[hq] = hq < a.Hk ? (1.0f / sqrtf(ss + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(ss + a.l2_eps);
+  }
+  __syncthreads();
+  const int nqkc = nqk * D;
+  for (int c = tid; c < C; c += kPrepThreads) {
+    const float y = s_y[c];
+    if (c < a.Hk * D)
+      w.qn[(size_t)b * a.Hk * D + c] = y * s_r[c / D];
+    else if (c < nqkc)
+      w.kn[(size_t)b * a.Hk * D + (c - a.Hk * D)] = y * s_r[c / D];
+    else
+      w.v[(size_t)b * a.Hv * D + (c - nqkc)] = y;
   }
 }
 
@@ -258,10 +260,12 @@ __global__ void __launch_bounds__(D) batch_gnorm_kernel(MixArgs a, BatchWs w) {
   }
 }
 
-cudaError_t launch_attr(const void *fn, dim3 grid, int threads, const LaunchCtx &lc, void **args) {
+cudaError_t launch_attr(const void *fn, dim3 grid, int threads, const LaunchCtx &lc, void **args,
+                        size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = lc.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -276,8 +280,16 @@ cudaError_t launch_batch_d(const MixArgs &a, const BatchWs &w, const LaunchCtx &
   MixArgs ac = a;
   BatchWs wc = w;
   void *args[] = {&ac, &wc};
-  cudaError_t e = launch_attr(reinterpret_cast<const void *>(batch_prep_kernel<D>),
-                              dim3(2 * a.Hk + a.Hv + 1, a.B), D, lc, args);
+  const size_t prep_smem = ((size_t)a.C + 2 * a.Hk) * sizeof(float);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e0 = cudaFuncSetAttribute(batch_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e0 != cudaSuccess) return e0;
+    configured = true;
+  }
+  if (prep_smem > 200 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = launch_attr(reinterpret_cast<const void *>(batch_prep_kernel<D>), dim3(a.B, 1), kPrepThreads, lc,
+                              args, prep_smem);
   if (e != cudaSuccess) return e;
   const int ns = a.slices > 0 ? a.slices : 1;
   const void *dk = nullptr;
