@@ -59,6 +59,7 @@ struct Tuning {
   int mix_slices = 0;      // d_v slices per head in the mixing kernel: 0 auto, 1, 2, 4
   int gemv_mma = 0;        // one-row projections with warp-level MMA block products: 0 auto (on), 1 off, 2 on
   int batch_split = 0;     // decode mixing as prep / delta / gated-norm kernels: 0 auto (B >= 96), 1 off, 2 on
+  int scan_tc = 0;         // prefill chunk scan products on warp-level tensor cores: 0 auto (on), 1 off, 2 on
 };
 Tuning g_tune;
 
@@ -348,6 +349,10 @@ gdn_status gdn_set_tuning(int knob, int value) {
     case 9:
       if (value < 0 || value > 2) return GDN_E_RANGE;
       g_tune.batch_split = value;
+      return GDN_OK;
+    case 10:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      g_tune.scan_tc = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;
@@ -766,6 +771,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.conv_state = cst;
   p.ssm = S;
   p.state_bf16 = c.state_bf16;
+  p.scan_tc = g_tune.scan_tc != 1;
   p.conv_w = ctx->conv_w;
   p.A_log = ctx->A_log;
   p.dt_bias = ctx->dt_bias;

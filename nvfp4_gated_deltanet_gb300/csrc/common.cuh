@@ -404,6 +404,7 @@ struct PrefillArgs {
   uint16_t *conv_state;  // this slot's [K-1][C]
   void *ssm;             // this slot's [Hv][D][D], FP32 or BF16 bits (state_bf16)
   int state_bf16;
+  int scan_tc;           // chunk scan on warp-level tensor-core MMA (D = 128)
   const uint16_t *conv_w;
   const float *A_log, *dt_bias, *norm_w;
   int Hk, Hv, D, C, Kc;

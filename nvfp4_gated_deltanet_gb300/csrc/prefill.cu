@@ -389,6 +389,207 @@ __global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- chunk_scan on tensor cores
+// The same chunk recurrence as chunk_scan_kernel for D = 128, with its three
+// products on warp-level MMA (mma.sync m16n8k8, TF32 in, FP32 accumulation)
+// in the split form x = hi + lo (hi = TF32(x), lo = TF32(x - hi)) and
+// a.b ~ hi.hi + hi.lo + lo.hi: about 21 of FP32's 24 mantissa bits per
+// product (the delta rule of a prompt keeps the one-token rule's precision,
+// as the pages ask of their split-BF16 prefill), lo terms added first.
+//   P = [W; Q] S^T          (128 x 32, K = 128)
+//   O = diag(e^Gamma) Pq + A U   (64 x 32, K = 64; A is zero above the diagonal)
+//   S <- e^Gamma_64 S + Cf^T K   (32 x 128, K = 64)
+// Shared tiles are padded so every fragment load is conflict-free.
+GDN_DEV uint32_t tf32_of(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+GDN_DEV void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  hi = tf32_of(x);
+  lo = tf32_of(x - __uint_as_float(hi));
+}
+GDN_DEV void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A B with A (16x8) as af[0..3] (row g, k t / g+8, t / g, t+4 / g+8, t+4) and
+// B (8x8) as bf[0..1] (k t / t+4, column g), both split into hi and lo parts.
+GDN_DEV void mma3(float (&d)[4], const float (&af)[4], const float (&bf)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(af[i], ah[i], al[i]);
+  split_tf32(bf[0], bh[0], bl[0]);
+  split_tf32(bf[1], bh[1], bl[1]);
+  mma_tf32(d, al, bh[0], bh[1]);
+  mma_tf32(d, ah, bl[0], bl[1]);
+  mma_tf32(d, ah, bh[0], bh[1]);
+}
+
+__global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
+  constexpr int D = 128, R = 32, NSL = D / R;
+  constexpr int XLD = D + 4;   // W, Q, K rows
+  constexpr int SLD = D + 4;   // S rows
+  constexpr int ULD = R + 8;   // U, Cf rows
+  constexpr int ALD = kC + 4;  // A rows
+  constexpr int PLD = R + 1;   // P rows
+  extern __shared__ __align__(16) float sm[];
+  float *Ws = sm;                    // [kC][XLD]
+  float *Qs = Ws + kC * XLD;         // [kC][XLD]
+  float *Ks = Qs + kC * XLD;         // [kC][XLD]
+  float *Us = Ks + kC * XLD;         // [kC][ULD]  Ut slice, then U
+  float *As = Us + kC * ULD;         // [kC][ALD]
+  float *Gs = As + kC * ALD;         // [kC]
+  float *S = Gs + kC;                // [R][SLD]
+  float *P = S + R * SLD;            // [2 kC][PLD]: W S0^T then Q S0^T
+  float *Cf = P + 2 * kC * PLD;      // [kC][ULD]: e^(Gamma_64 - Gamma_j) u_j
+
+  const int h = blockIdx.x / NSL, r0 = (blockIdx.x % NSL) * R;
+  const int kh = h / (a.Hv / a.Hk);
+  const int nc = a.Tp / kC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  for (int e = tid; e < R * D; e += blockDim.x) {
+    const int r = e / D, d = e % D;
+    S[r * SLD + d] = state_load(a.ssm, a.state_bf16, ((size_t)h * D + r0 + r) * D + d);
+  }
+  auto load_wq = [&](int c) {
+    const float *w = a.W + ((size_t)h * nc + c) * kC * D;
+    const float *q = a.qn + ((size_t)kh * a.Tp + (size_t)c * kC) * D;
+    for (int e = tid; e < kC * D / 4; e += blockDim.x) {
+      const int i = (4 * e) / D, d = (4 * e) % D;
+      cp_async16(Ws + i * XLD + d, w + 4 * e, true);
+      cp_async16(Qs + i * XLD + d, q + 4 * e, c * kC + i < a.T);
+    }
+  };
+  auto load_rest = [&](int c) {
+    const float *k = a.kn + ((size_t)kh * a.Tp + (size_t)c * kC) * D;
+    for (int e = tid; e < kC * D / 4; e += blockDim.x) {
+      const int i = (4 * e) / D, d = (4 * e) % D;
+      cp_async16(Ks + i * XLD + d, k + 4 * e, c * kC + i < a.T);
+    }
+    const float *u = a.Ut + ((size_t)h * nc + c) * kC * D + r0;
+    for (int e = tid; e < kC * R / 4; e += blockDim.x) {
+      const int i = (4 * e) / R, r = (4 * e) % R;
+      cp_async16(Us + i * ULD + r, u + (size_t)i * D + r, true);
+    }
+    const float *am = a.Am + ((size_t)h * nc + c) * kC * kC;
+    for (int e = tid; e < kC * kC / 4; e += blockDim.x) {
+      const int i = (4 * e) / kC, j = (4 * e) % kC;
+      cp_async16(As + i * ALD + j, am + 4 * e, true);
+    }
+    if (tid < kC / 4) cp_async16(Gs + 4 * tid, a.Gam + ((size_t)h * nc + c) * kC + 4 * tid, true);
+  };
+  load_wq(0);
+  load_rest(0);
+  cp_async_commit();
+
+  for (int c = 0; c < nc; ++c) {
+    cp_async_wait_all();
+    __syncthreads();
+    // ---- P = [W; Q] S0^T: warp -> one 16-row tile of [W; Q], two 8-column tiles
+    {
+      const int m0 = 16 * (warp >> 1), n0 = 16 * (warp & 1);
+      const float *X = m0 < kC ? Ws + m0 * XLD : Qs + (m0 - kC) * XLD;
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int k0 = 0; k0 < D; k0 += 8) {
+        const float af[4] = {X[g * XLD + k0 + t], X[(g + 8) * XLD + k0 + t], X[g * XLD + k0 + t + 4],
+                             X[(g + 8) * XLD + k0 + t + 4]};
+        const float b0[2] = {S[(n0 + g) * SLD + k0 + t], S[(n0 + g) * SLD + k0 + t + 4]};
+        const float b1[2] = {S[(n0 + 8 + g) * SLD + k0 + t], S[(n0 + 8 + g) * SLD + k0 + t + 4]};
+        mma3(d0, af, b0);
+        mma3(d1, af, b1);
+      }
+      P[(m0 + g) * PLD + n0 + 2 * t] = d0[0];
+      P[(m0 + g) * PLD + n0 + 2 * t + 1] = d0[1];
+      P[(m0 + g + 8) * PLD + n0 + 2 * t] = d0[2];
+      P[(m0 + g + 8) * PLD + n0 + 2 * t + 1] = d0[3];
+      P[(m0 + g) * PLD + n0 + 8 + 2 * t] = d1[0];
+      P[(m0 + g) * PLD + n0 + 8 + 2 * t + 1] = d1[1];
+      P[(m0 + g + 8) * PLD + n0 + 8 + 2 * t] = d1[2];
+      P[(m0 + g + 8) * PLD + n0 + 8 + 2 * t + 1] = d1[3];
+    }
+    __syncthreads();
+    if (c + 1 < nc) {  // W and Q of this chunk are consumed
+      load_wq(c + 1);
+      cp_async_commit();
+    }
+    // ---- U = Ut - W S0^T (in place), and the state-update coefficients
+    const float gC = Gs[kC - 1];
+    for (int e = tid; e < kC * R; e += blockDim.x) {
+      const int i = e / R, r = e % R;
+      const float u = Us[i * ULD + r] - P[i * PLD + r];
+      Us[i * ULD + r] = u;
+      Cf[i * ULD + r] = expf(gC - Gs[i]) * u;
+    }
+    __syncthreads();
+    // ---- O = diag(e^Gamma) (Q S0^T) + A U: warp -> one 16 x 8 tile
+    {
+      const int m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
+      const float e0 = expf(Gs[m0 + g]), e1 = expf(Gs[m0 + g + 8]);
+      float d[4] = {e0 * P[(kC + m0 + g) * PLD + n0 + 2 * t], e0 * P[(kC + m0 + g) * PLD + n0 + 2 * t + 1],
+                    e1 * P[(kC + m0 + g + 8) * PLD + n0 + 2 * t], e1 * P[(kC + m0 + g + 8) * PLD + n0 + 2 * t + 1]};
+      for (int k0 = 0; k0 < m0 + 16; k0 += 8) {  // A is zero above the diagonal
+        const float af[4] = {As[(m0 + g) * ALD + k0 + t], As[(m0 + g + 8) * ALD + k0 + t],
+                             As[(m0 + g) * ALD + k0 + t + 4], As[(m0 + g + 8) * ALD + k0 + t + 4]};
+        const float bf[2] = {Us[(k0 + t) * ULD + n0 + g], Us[(k0 + t + 4) * ULD + n0 + g]};
+        mma3(d, af, bf);
+      }
+      const int i0 = c * kC + m0 + g, i1 = i0 + 8;
+      if (i0 < a.T) {
+        a.o[((size_t)i0 * a.Hv + h) * D + r0 + n0 + 2 * t] = d[0];
+        a.o[((size_t)i0 * a.Hv + h) * D + r0 + n0 + 2 * t + 1] = d[1];
+      }
+      if (i1 < a.T) {
+        a.o[((size_t)i1 * a.Hv + h) * D + r0 + n0 + 2 * t] = d[2];
+        a.o[((size_t)i1 * a.Hv + h) * D + r0 + n0 + 2 * t + 1] = d[3];
+      }
+    }
+    // ---- S <- e^Gamma_64 S + Cf^T K: warp -> one 16-row tile of S, two 8-column tiles
+    {
+      const float dC = expf(gC);
+      const int m0 = 16 * (warp >> 3), n0 = 16 * (warp & 7);
+      float d0[4] = {dC * S[(m0 + g) * SLD + n0 + 2 * t], dC * S[(m0 + g) * SLD + n0 + 2 * t + 1],
+                     dC * S[(m0 + g + 8) * SLD + n0 + 2 * t], dC * S[(m0 + g + 8) * SLD + n0 + 2 * t + 1]};
+      float d1[4] = {dC * S[(m0 + g) * SLD + n0 + 8 + 2 * t], dC * S[(m0 + g) * SLD + n0 + 8 + 2 * t + 1],
+                     dC * S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t], dC * S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t + 1]};
+#pragma unroll 4
+      for (int k0 = 0; k0 < kC; k0 += 8) {
+        const float af[4] = {Cf[(k0 + t) * ULD + m0 + g], Cf[(k0 + t) * ULD + m0 + g + 8],
+                             Cf[(k0 + t + 4) * ULD + m0 + g], Cf[(k0 + t + 4) * ULD + m0 + g + 8]};
+        const float b0[2] = {Ks[(k0 + t) * XLD + n0 + g], Ks[(k0 + t + 4) * XLD + n0 + g]};
+        const float b1[2] = {Ks[(k0 + t) * XLD + n0 + 8 + g], Ks[(k0 + t + 4) * XLD + n0 + 8 + g]};
+        mma3(d0, af, b0);
+        mma3(d1, af, b1);
+      }
+      S[(m0 + g) * SLD + n0 + 2 * t] = d0[0];
+      S[(m0 + g) * SLD + n0 + 2 * t + 1] = d0[1];
+      S[(m0 + g + 8) * SLD + n0 + 2 * t] = d0[2];
+      S[(m0 + g + 8) * SLD + n0 + 2 * t + 1] = d0[3];
+      S[(m0 + g) * SLD + n0 + 8 + 2 * t] = d1[0];
+      S[(m0 + g) * SLD + n0 + 8 + 2 * t + 1] = d1[1];
+      S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t] = d1[2];
+      S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t + 1] = d1[3];
+    }
+    __syncthreads();
+    if (c + 1 < nc) {  // K, U, A and Gamma of this chunk are consumed
+      load_rest(c + 1);
+      cp_async_commit();
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  for (int e = tid; e < R * D; e += blockDim.x) {
+    const int r = e / D, d = e % D;
+    state_store(a.ssm, a.state_bf16, ((size_t)h * D + r0 + r) * D + d, S[r * SLD + d]);
+  }
+}
+
 // one CTA per token; thread i owns 16-block i of y (head i / (D/16))
 __global__ void gnorm_kernel(PrefillArgs a) {
   const int t = blockIdx.x;
@@ -455,7 +656,19 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
   }
   const int nc = a.Tp / kC;
   chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
-  chunk_scan_kernel<D><<<a.Hv * (D / 32), 512, sm_scan, lc.stream>>>(a);
+  if (D == 128 && a.scan_tc) {
+    const size_t sm_tc = (size_t)(3 * kC * (D + 4) + kC * 40 + kC * (kC + 4) + kC + 32 * (D + 4) + 2 * kC * 33 +
+                                  kC * 40) * sizeof(float);
+    static bool configured_tc = false;
+    if (!configured_tc) {
+      cudaError_t e = cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_tc);
+      if (e != cudaSuccess) return e;
+      configured_tc = true;
+    }
+    chunk_scan_tc_kernel<<<a.Hv * (D / 32), 512, sm_tc, lc.stream>>>(a);
+  } else {
+    chunk_scan_kernel<D><<<a.Hv * (D / 32), 512, sm_scan, lc.stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
