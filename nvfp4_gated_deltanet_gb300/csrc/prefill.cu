@@ -394,8 +394,9 @@ __global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
 // products on warp-level MMA (mma.sync m16n8k8, TF32 in, FP32 accumulation)
 // in the split form x = hi + lo (hi = TF32(x), lo = TF32(x - hi)) and
 // a.b ~ hi.hi + hi.lo + lo.hi: about 21 of FP32's 24 mantissa bits per
-// product (the delta rule of a prompt keeps the one-token rule's precision,
-// as the pages ask of their split-BF16 prefill), lo terms added first.
+// product, so chunked prefill stays as precise as the per-token recurrence
+// (bloomery issue #565, §10, splits FP32 operands into BF16 parts for the same
+// reason); lo terms added first.
 //   P = [W; Q] S^T          (128 x 32, K = 128)
 //   O = diag(e^Gamma) Pq + A U   (64 x 32, K = 64; A is zero above the diagonal)
 //   S <- e^Gamma_64 S + Cf^T K   (32 x 128, K = 64)
