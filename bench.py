@@ -343,6 +343,9 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    # one host thread, stated as such (numpy's BLAS would otherwise pick its own)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
     import numpy as np
     from nvfp4_gated_deltanet_gb300 import synth
     from oracle import gdn
@@ -358,7 +361,7 @@ def reference_arm(args):
         L.decode_step(x[args.warmup + i:args.warmup + i + 1], [0], c, s)
     el = time.time() - t
     us = el / args.steps * 1e6
-    cores = int(os.environ.get("OMP_NUM_THREADS", "0")) or (os.cpu_count() or 1)
+    cores = 1
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
