@@ -400,7 +400,9 @@ __global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
 //   P = [W; Q] S^T          (128 x 32, K = 128)
 //   O = diag(e^Gamma) Pq + A U   (64 x 32, K = 64; A is zero above the diagonal)
 //   S <- e^Gamma_64 S + Cf^T K   (32 x 128, K = 64)
-// Shared tiles are padded so every fragment load is conflict-free.
+// Shared tiles are padded so every fragment load is conflict-free. The state
+// slice and the update coefficients are kept pre-split (hi and lo parts next
+// to the FP32 state), since eight warps read each of their fragments.
 GDN_DEV uint32_t tf32_of(float x) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -417,17 +419,28 @@ GDN_DEV void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// D += A B with A (16x8) as af[0..3] (row g, k t / g+8, t / g, t+4 / g+8, t+4) and
-// B (8x8) as bf[0..1] (k t / t+4, column g), both split into hi and lo parts.
-GDN_DEV void mma3(float (&d)[4], const float (&af)[4], const float (&bf)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) split_tf32(af[i], ah[i], al[i]);
-  split_tf32(bf[0], bh[0], bl[0]);
-  split_tf32(bf[1], bh[1], bl[1]);
+// D += A B with A (16x8) as (row g, k t / g+8, t / g, t+4 / g+8, t+4) and B (8x8)
+// as (k t / t+4, column g), each given as hi and lo TF32 parts.
+GDN_DEV void mma3_split(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], const uint32_t (&bh)[2],
+                        const uint32_t (&bl)[2]) {
   mma_tf32(d, al, bh[0], bh[1]);
   mma_tf32(d, ah, bl[0], bl[1]);
   mma_tf32(d, ah, bh[0], bh[1]);
+}
+GDN_DEV void split4(const float (&f)[4], uint32_t (&h)[4], uint32_t (&l)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(f[i], h[i], l[i]);
+}
+GDN_DEV void split2(const float (&f)[2], uint32_t (&h)[2], uint32_t (&l)[2]) {
+  split_tf32(f[0], h[0], l[0]);
+  split_tf32(f[1], h[1], l[1]);
+}
+// both operands split here
+GDN_DEV void mma3(float (&d)[4], const float (&af)[4], const float (&bf)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+  split4(af, ah, al);
+  split2(bf, bh, bl);
+  mma3_split(d, ah, al, bh, bl);
 }
 
 __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
@@ -446,7 +459,10 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
   float *Gs = As + kC * ALD;         // [kC]
   float *S = Gs + kC;                // [R][SLD]
   float *P = S + R * SLD;            // [2 kC][PLD]: W S0^T then Q S0^T
-  float *Cf = P + 2 * kC * PLD;      // [kC][ULD]: e^(Gamma_64 - Gamma_j) u_j
+  uint32_t *Cfh = reinterpret_cast<uint32_t *>(P + 2 * kC * PLD);  // [kC][ULD]: e^(Gamma_64 - Gamma_j) u_j, hi
+  uint32_t *Cfl = Cfh + kC * ULD;                                   // ... lo
+  uint32_t *Sh = Cfl + kC * ULD;                                    // [R][SLD]: S, hi
+  uint32_t *Sl = Sh + R * SLD;                                      // ... lo
 
   const int h = blockIdx.x / NSL, r0 = (blockIdx.x % NSL) * R;
   const int kh = h / (a.Hv / a.Hk);
@@ -456,7 +472,9 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
 
   for (int e = tid; e < R * D; e += blockDim.x) {
     const int r = e / D, d = e % D;
-    S[r * SLD + d] = state_load(a.ssm, a.state_bf16, ((size_t)h * D + r0 + r) * D + d);
+    const float v = state_load(a.ssm, a.state_bf16, ((size_t)h * D + r0 + r) * D + d);
+    S[r * SLD + d] = v;
+    split_tf32(v, Sh[r * SLD + d], Sl[r * SLD + d]);
   }
   auto load_wq = [&](int c) {
     const float *w = a.W + ((size_t)h * nc + c) * kC * D;
@@ -501,10 +519,14 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
       for (int k0 = 0; k0 < D; k0 += 8) {
         const float af[4] = {X[g * XLD + k0 + t], X[(g + 8) * XLD + k0 + t], X[g * XLD + k0 + t + 4],
                              X[(g + 8) * XLD + k0 + t + 4]};
-        const float b0[2] = {S[(n0 + g) * SLD + k0 + t], S[(n0 + g) * SLD + k0 + t + 4]};
-        const float b1[2] = {S[(n0 + 8 + g) * SLD + k0 + t], S[(n0 + 8 + g) * SLD + k0 + t + 4]};
-        mma3(d0, af, b0);
-        mma3(d1, af, b1);
+        uint32_t ah[4], al[4];
+        split4(af, ah, al);
+        const uint32_t b0h[2] = {Sh[(n0 + g) * SLD + k0 + t], Sh[(n0 + g) * SLD + k0 + t + 4]};
+        const uint32_t b0l[2] = {Sl[(n0 + g) * SLD + k0 + t], Sl[(n0 + g) * SLD + k0 + t + 4]};
+        const uint32_t b1h[2] = {Sh[(n0 + 8 + g) * SLD + k0 + t], Sh[(n0 + 8 + g) * SLD + k0 + t + 4]};
+        const uint32_t b1l[2] = {Sl[(n0 + 8 + g) * SLD + k0 + t], Sl[(n0 + 8 + g) * SLD + k0 + t + 4]};
+        mma3_split(d0, ah, al, b0h, b0l);
+        mma3_split(d1, ah, al, b1h, b1l);
       }
       P[(m0 + g) * PLD + n0 + 2 * t] = d0[0];
       P[(m0 + g) * PLD + n0 + 2 * t + 1] = d0[1];
@@ -526,7 +548,7 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
       const int i = e / R, r = e % R;
       const float u = Us[i * ULD + r] - P[i * PLD + r];
       Us[i * ULD + r] = u;
-      Cf[i * ULD + r] = expf(gC - Gs[i]) * u;
+      split_tf32(expf(gC - Gs[i]) * u, Cfh[i * ULD + r], Cfl[i * ULD + r]);
     }
     __syncthreads();
     // ---- O = diag(e^Gamma) (Q S0^T) + A U: warp -> one 16 x 8 tile
@@ -561,21 +583,28 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
                      dC * S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t], dC * S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t + 1]};
 #pragma unroll 4
       for (int k0 = 0; k0 < kC; k0 += 8) {
-        const float af[4] = {Cf[(k0 + t) * ULD + m0 + g], Cf[(k0 + t) * ULD + m0 + g + 8],
-                             Cf[(k0 + t + 4) * ULD + m0 + g], Cf[(k0 + t + 4) * ULD + m0 + g + 8]};
+        const uint32_t ah[4] = {Cfh[(k0 + t) * ULD + m0 + g], Cfh[(k0 + t) * ULD + m0 + g + 8],
+                                Cfh[(k0 + t + 4) * ULD + m0 + g], Cfh[(k0 + t + 4) * ULD + m0 + g + 8]};
+        const uint32_t al[4] = {Cfl[(k0 + t) * ULD + m0 + g], Cfl[(k0 + t) * ULD + m0 + g + 8],
+                                Cfl[(k0 + t + 4) * ULD + m0 + g], Cfl[(k0 + t + 4) * ULD + m0 + g + 8]};
         const float b0[2] = {Ks[(k0 + t) * XLD + n0 + g], Ks[(k0 + t + 4) * XLD + n0 + g]};
         const float b1[2] = {Ks[(k0 + t) * XLD + n0 + 8 + g], Ks[(k0 + t + 4) * XLD + n0 + 8 + g]};
-        mma3(d0, af, b0);
-        mma3(d1, af, b1);
+        uint32_t bh[2], bl[2];
+        split2(b0, bh, bl);
+        mma3_split(d0, ah, al, bh, bl);
+        split2(b1, bh, bl);
+        mma3_split(d1, ah, al, bh, bl);
       }
-      S[(m0 + g) * SLD + n0 + 2 * t] = d0[0];
-      S[(m0 + g) * SLD + n0 + 2 * t + 1] = d0[1];
-      S[(m0 + g + 8) * SLD + n0 + 2 * t] = d0[2];
-      S[(m0 + g + 8) * SLD + n0 + 2 * t + 1] = d0[3];
-      S[(m0 + g) * SLD + n0 + 8 + 2 * t] = d1[0];
-      S[(m0 + g) * SLD + n0 + 8 + 2 * t + 1] = d1[1];
-      S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t] = d1[2];
-      S[(m0 + g + 8) * SLD + n0 + 8 + 2 * t + 1] = d1[3];
+      const int sidx[8] = {(m0 + g) * SLD + n0 + 2 * t,         (m0 + g) * SLD + n0 + 2 * t + 1,
+                           (m0 + g + 8) * SLD + n0 + 2 * t,     (m0 + g + 8) * SLD + n0 + 2 * t + 1,
+                           (m0 + g) * SLD + n0 + 8 + 2 * t,     (m0 + g) * SLD + n0 + 8 + 2 * t + 1,
+                           (m0 + g + 8) * SLD + n0 + 8 + 2 * t, (m0 + g + 8) * SLD + n0 + 8 + 2 * t + 1};
+      const float sv[8] = {d0[0], d0[1], d0[2], d0[3], d1[0], d1[1], d1[2], d1[3]};
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        S[sidx[x]] = sv[x];
+        split_tf32(sv[x], Sh[sidx[x]], Sl[sidx[x]]);
+      }
     }
     __syncthreads();
     if (c + 1 < nc) {  // K, U, A and Gamma of this chunk are consumed
@@ -659,7 +688,7 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
   chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
   if (D == 128 && a.scan_tc) {
     const size_t sm_tc = (size_t)(3 * kC * (D + 4) + kC * 40 + kC * (kC + 4) + kC + 32 * (D + 4) + 2 * kC * 33 +
-                                  kC * 40) * sizeof(float);
+                                  2 * kC * 40 + 2 * 32 * (D + 4)) * sizeof(float);
     static bool configured_tc = false;
     if (!configured_tc) {
       cudaError_t e = cudaFuncSetAttribute(chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_tc);
