@@ -122,23 +122,66 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- split-TF32 warp MMA
+// (used by chunk_prep and chunk_scan_tc: see the latter's comment)
+GDN_DEV uint32_t tf32_of(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+GDN_DEV void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  hi = tf32_of(x);
+  lo = tf32_of(x - __uint_as_float(hi));
+}
+GDN_DEV void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A B with A (16x8) as (row g, k t / g+8, t / g, t+4 / g+8, t+4) and B (8x8)
+// as (k t / t+4, column g), each given as hi and lo TF32 parts.
+GDN_DEV void mma3_split(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], const uint32_t (&bh)[2],
+                        const uint32_t (&bl)[2]) {
+  mma_tf32(d, al, bh[0], bh[1]);
+  mma_tf32(d, ah, bl[0], bl[1]);
+  mma_tf32(d, ah, bh[0], bh[1]);
+}
+GDN_DEV void split4(const float (&f)[4], uint32_t (&h)[4], uint32_t (&l)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split_tf32(f[i], h[i], l[i]);
+}
+GDN_DEV void split2(const float (&f)[2], uint32_t (&h)[2], uint32_t (&l)[2]) {
+  split_tf32(f[0], h[0], l[0]);
+  split_tf32(f[1], h[1], l[1]);
+}
+// both operands split here
+GDN_DEV void mma3(float (&d)[4], const float (&af)[4], const float (&bf)[2]) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+  split4(af, ah, al);
+  split2(bf, bh, bl);
+  mma3_split(d, ah, al, bh, bl);
+}
+
+
 // ---------------------------------------------------------------- chunk_prep
 // One CTA (256 threads) per (chunk, value head). Tokens past T count as zero
 // (k = q = v = 0, beta = 0, g = 0), which adds nothing to any product.
 template <int D>
 __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
-  constexpr int LD = kC + 4;  // row stride of the transposed tiles (float4 aligned)
+  constexpr int XLD = D + 4;  // padded row stride of K and Q (conflict-free fragment loads)
   extern __shared__ __align__(16) float sm[];
-  float *KT = sm;                 // [D][LD]: KT[d][i] = k_i[d]
-  float *QT = KT + D * LD;        // [D][LD]
-  float *Lm = QT + D * LD;        // [kC][kC]
+  float *KR = sm;                 // [kC][XLD]: k_i
+  float *QR = KR + kC * XLD;      // [kC][XLD]: q_i
+  float *Lm = QR + kC * XLD;      // [kC][kC]
   float *gam = Lm + kC * kC;      // [kC]
   float *bet = gam + kC;          // [kC]
   const int c = blockIdx.x, h = blockIdx.y;
   const int kh = h / (a.Hv / a.Hk);
   const int t0 = c * kC;
   const int nc = a.Tp / kC;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   for (int e = tid; e < kC * D / 4; e += blockDim.x) {
     const int i = (4 * e) / D, d = (4 * e) % D;
@@ -147,8 +190,8 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 qv = live ? *reinterpret_cast<const float4 *>(a.qn + ((size_t)kh * a.Tp + t0 + i) * D + d)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    KT[d * LD + i] = kv.x; KT[(d + 1) * LD + i] = kv.y; KT[(d + 2) * LD + i] = kv.z; KT[(d + 3) * LD + i] = kv.w;
-    QT[d * LD + i] = qv.x; QT[(d + 1) * LD + i] = qv.y; QT[(d + 2) * LD + i] = qv.z; QT[(d + 3) * LD + i] = qv.w;
+    *reinterpret_cast<float4 *>(KR + i * XLD + d) = kv;
+    *reinterpret_cast<float4 *>(QR + i * XLD + d) = qv;
   }
   if (tid < kC) {
     const bool live = t0 + tid < a.T;
@@ -164,38 +207,49 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
   __syncthreads();
   if (tid < kC) a.Gam[((size_t)h * nc + c) * kC + tid] = gam[tid];
 
-  // k.k and q.k on a 4x4 register tile per thread
+  // K K^T (warps 0..3) and Q K^T (warps 4..7) on split-TF32 warp MMA: warp ->
+  // one 16-row band of the 64 x 64 product, all eight 8-column tiles
   {
-    const int ti = tid >> 4, tj = tid & 15;
-    float kk[4][4] = {}, qk[4][4] = {};
-    for (int d = 0; d < D; ++d) {
-      const float4 ka = *reinterpret_cast<const float4 *>(KT + d * LD + 4 * ti);
-      const float4 qa = *reinterpret_cast<const float4 *>(QT + d * LD + 4 * ti);
-      const float4 kb = *reinterpret_cast<const float4 *>(KT + d * LD + 4 * tj);
-      const float av[4] = {ka.x, ka.y, ka.z, ka.w}, qv[4] = {qa.x, qa.y, qa.z, qa.w};
-      const float bv[4] = {kb.x, kb.y, kb.z, kb.w};
+    const int g = lane >> 2, t = lane & 3;
+    const int m0 = 16 * (warp & 3);
+    const bool isq = warp >= 4;
+    const float *X = isq ? QR : KR;
+    float acc[8][4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
+    for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+#pragma unroll 2
+    for (int k0 = 0; k0 < D; k0 += 8) {
+      const float af[4] = {X[(m0 + g) * XLD + k0 + t], X[(m0 + g + 8) * XLD + k0 + t], X[(m0 + g) * XLD + k0 + t + 4],
+                           X[(m0 + g + 8) * XLD + k0 + t + 4]};
+      uint32_t ah[4], al[4];
+      split4(af, ah, al);
 #pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          kk[x][y] = fmaf(av[x], bv[y], kk[x][y]);
-          qk[x][y] = fmaf(qv[x], bv[y], qk[x][y]);
-        }
+      for (int n = 0; n < 8; ++n) {
+        const float bf[2] = {KR[(8 * n + g) * XLD + k0 + t], KR[(8 * n + g) * XLD + k0 + t + 4]};
+        uint32_t bh[2], bl[2];
+        split2(bf, bh, bl);
+        mma3_split(acc[n], ah, al, bh, bl);
+      }
     }
     float *Ag = a.Am + ((size_t)h * nc + c) * kC * kC;
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int i = 4 * ti + x;
-      float lrow[4], arow[4];
+    for (int n = 0; n < 8; ++n) {
 #pragma unroll
-      for (int y = 0; y < 4; ++y) {
-        const int j = 4 * tj + y;
-        const float dec = j <= i ? expf(gam[i] - gam[j]) : 0.0f;
-        lrow[y] = j < i ? bet[i] * dec * kk[x][y] : 0.0f;
-        arow[y] = dec * qk[x][y];
+      for (int hh = 0; hh < 2; ++hh) {  // rows g and g + 8
+        const int i = m0 + g + 8 * hh, j0 = 8 * n + 2 * t;
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = j0 + e;
+          const float dec = j <= i ? expf(gam[i] - gam[j]) : 0.0f;
+          const float x = acc[n][2 * hh + e];
+          v[e] = isq ? dec * x : (j < i ? bet[i] * dec * x : 0.0f);
+        }
+        if (isq)
+          *reinterpret_cast<float2 *>(Ag + (size_t)i * kC + j0) = make_float2(v[0], v[1]);
+        else
+          *reinterpret_cast<float2 *>(Lm + i * kC + j0) = make_float2(v[0], v[1]);
       }
-      *reinterpret_cast<float4 *>(Lm + i * kC + 4 * tj) = make_float4(lrow[0], lrow[1], lrow[2], lrow[3]);
-      *reinterpret_cast<float4 *>(Ag + (size_t)i * kC + 4 * tj) = make_float4(arow[0], arow[1], arow[2], arow[3]);
     }
   }
   __syncthreads();
@@ -209,7 +263,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
 #pragma unroll
     for (int i = 0; i < kC; ++i) {
       if (col < D)
-        X[i] = bet[i] * expf(gam[i]) * KT[col * LD + i];
+        X[i] = bet[i] * expf(gam[i]) * KR[i * XLD + col];
       else
         X[i] = (t0 + i < a.T) ? bet[i] * a.v[((size_t)h * a.Tp + t0 + i) * D + (col - D)] : 0.0f;
     }
@@ -403,46 +457,6 @@ __global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
 // Shared tiles are padded so every fragment load is conflict-free. The state
 // slice and the update coefficients are kept pre-split (hi and lo parts next
 // to the FP32 state), since eight warps read each of their fragments.
-GDN_DEV uint32_t tf32_of(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
-GDN_DEV void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-  hi = tf32_of(x);
-  lo = tf32_of(x - __uint_as_float(hi));
-}
-GDN_DEV void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// D += A B with A (16x8) as (row g, k t / g+8, t / g, t+4 / g+8, t+4) and B (8x8)
-// as (k t / t+4, column g), each given as hi and lo TF32 parts.
-GDN_DEV void mma3_split(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4], const uint32_t (&bh)[2],
-                        const uint32_t (&bl)[2]) {
-  mma_tf32(d, al, bh[0], bh[1]);
-  mma_tf32(d, ah, bl[0], bl[1]);
-  mma_tf32(d, ah, bh[0], bh[1]);
-}
-GDN_DEV void split4(const float (&f)[4], uint32_t (&h)[4], uint32_t (&l)[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) split_tf32(f[i], h[i], l[i]);
-}
-GDN_DEV void split2(const float (&f)[2], uint32_t (&h)[2], uint32_t (&l)[2]) {
-  split_tf32(f[0], h[0], l[0]);
-  split_tf32(f[1], h[1], l[1]);
-}
-// both operands split here
-GDN_DEV void mma3(float (&d)[4], const float (&af)[4], const float (&bf)[2]) {
-  uint32_t ah[4], al[4], bh[2], bl[2];
-  split4(af, ah, al);
-  split2(bf, bh, bl);
-  mma3_split(d, ah, al, bh, bl);
-}
-
 __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
   constexpr int D = 128, R = 32, NSL = D / R;
   constexpr int XLD = D + 4;   // W, Q, K rows
@@ -672,8 +686,7 @@ __global__ void copy_u16_kernel(uint16_t *dst, const uint16_t *src, int n) {
 
 template <int D>
 cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
-  constexpr int LD = kC + 4;
-  const size_t sm_prep = (size_t)(2 * D * LD + kC * kC + 2 * kC) * sizeof(float);
+  const size_t sm_prep = (size_t)(2 * kC * (D + 4) + kC * kC + 2 * kC) * sizeof(float);
   const size_t sm_scan =
       (size_t)(3 * kC * D + kC * 32 + kC * kC + kC + 32 * (D + 1) + 2 * kC * 33 + kC * 33) * sizeof(float);
   static bool configured = false;
