@@ -289,7 +289,11 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * the default; 1 = never; 2 = always). knob 10: the prefill chunk scan's
  * products (W S^T, Q S^T, A U, the state update) on warp-level tensor-core MMA
  * in split TF32 (hi.hi + hi.lo + lo.hi) for d = 128 (0 and 2 = yes, the
- * default; 1 = FP32 on the CUDA cores).
+ * default; 1 = FP32 on the CUDA cores). knob 11: tensor-core projections with
+ * 128-row activation tiles, tiled scales and BF16 output as one persistent CTA
+ * per SM (operand ring running across output tiles, two TMEM accumulators so
+ * the epilogue overlaps the next tile's MMAs): 0 = when there are at least two
+ * output tiles per SM, the default; 1 = never; 2 = whenever the form allows.
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

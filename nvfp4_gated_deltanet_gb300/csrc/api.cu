@@ -60,6 +60,8 @@ struct Tuning {
   int gemv_mma = 0;        // one-row projections with warp-level MMA block products: 0 auto (on), 1 off, 2 on
   int batch_split = 0;     // decode mixing as prep / delta / gated-norm kernels: 0 auto (B >= 96), 1 off, 2 on
   int scan_tc = 0;         // prefill chunk scan products on warp-level tensor cores: 0 auto (on), 1 off, 2 on
+  int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto (two tiles per SM
+                           // or more), 1 off, 2 whenever the form allows
 };
 Tuning g_tune;
 
@@ -195,6 +197,7 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
     t.args.sfb_tiled = ctx->xq_scales;
     t.args.status = ctx->status;
     t.split_k = split_for(g_tune.split_in, rows, 2);
+    t.persist = g_tune.persist_gemm;
     return launch_tc_gemm(t, lc);
   }
   GemvArgs g{};
@@ -246,6 +249,7 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
     t.args.sfb_tiled = ctx->y_scales;  // written tiled by the mixing stage (out_proj_tiled)
     t.args.status = ctx->status;
     t.split_k = split_for(g_tune.split_out, rows, 4);
+    t.persist = g_tune.persist_gemm;
     t.args.early_trigger = early && g_tune.early_trigger != 1;
     return launch_tc_gemm(t, lc);
   }
@@ -351,8 +355,9 @@ gdn_status gdn_set_tuning(int knob, int value) {
       g_tune.batch_split = value;
       return GDN_OK;
     case 10:
+    case 11:
       if (value < 0 || value > 2) return GDN_E_RANGE;
-      g_tune.scan_tc = value;
+      (knob == 10 ? g_tune.scan_tc : g_tune.persist_gemm) = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;
