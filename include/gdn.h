@@ -290,10 +290,16 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * products (W S^T, Q S^T, A U, the state update) on warp-level tensor-core MMA
  * in split TF32 (hi.hi + hi.lo + lo.hi) for d = 128 (0 and 2 = yes, the
  * default; 1 = FP32 on the CUDA cores). knob 11: tensor-core projections with
- * 128-row activation tiles, tiled scales and BF16 output as one persistent CTA
- * per SM (operand ring running across output tiles, two TMEM accumulators so
- * the epilogue overlaps the next tile's MMAs): 0 = when there are at least two
- * output tiles per SM, the default; 1 = never; 2 = whenever the form allows.
+ * 128-token activation tiles, tiled scales and BF16 output as one persistent
+ * CTA per SM with two TMEM accumulators, so that the epilogue of one output
+ * tile overlaps the MMAs of the next. Two forms: streaming (both operands
+ * through one shared-memory ring that runs across tiles) and, for a reduction
+ * length of 2048, weight-stationary (a CTA keeps a 128-row weight tile and its
+ * scales resident and streams only activation tiles). 0 = automatic, the
+ * default: weight-stationary with at least 16 token tiles and two output tiles
+ * per SM, else streaming from two output tiles per SM, else one tile per CTA;
+ * 1 = one tile per CTA; 2 = streaming whenever the form allows; 3 =
+ * weight-stationary whenever the form allows.
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

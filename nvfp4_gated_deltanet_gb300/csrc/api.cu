@@ -60,8 +60,8 @@ struct Tuning {
   int gemv_mma = 0;        // one-row projections with warp-level MMA block products: 0 auto (on), 1 off, 2 on
   int batch_split = 0;     // decode mixing as prep / delta / gated-norm kernels: 0 auto (B >= 96), 1 off, 2 on
   int scan_tc = 0;         // prefill chunk scan products on warp-level tensor cores: 0 auto (on), 1 off, 2 on
-  int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto (two tiles per SM
-                           // or more), 1 off, 2 whenever the form allows
+  int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto, 1 off, 2 streaming
+                           // form whenever allowed, 3 weight-stationary form whenever allowed
 };
 Tuning g_tune;
 
@@ -355,9 +355,12 @@ gdn_status gdn_set_tuning(int knob, int value) {
       g_tune.batch_split = value;
       return GDN_OK;
     case 10:
-    case 11:
       if (value < 0 || value > 2) return GDN_E_RANGE;
-      (knob == 10 ? g_tune.scan_tc : g_tune.persist_gemm) = value;
+      g_tune.scan_tc = value;
+      return GDN_OK;
+    case 11:
+      if (value < 0 || value > 3) return GDN_E_RANGE;
+      g_tune.persist_gemm = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;

@@ -460,8 +460,8 @@ struct TcGemm {
   const uint8_t *b_codes, *b_scales;
   TcArgs args;
   int split_k;  // 0 = automatic
-  int persist;  // persistent form (gemm_nvf4_persist_kernel): 0 = two output tiles per SM or more, 1 = never, 2 = when
-                // the form allows
+  int persist;  // persistent forms: 0 = automatic, 1 = never, 2 = streaming (gemm_nvf4_persist_kernel) whenever
+                // allowed, 3 = weight-stationary (gemm_nvf4_wstat_kernel, K = 2048) whenever allowed
 };
 bool tc_make_weight_maps(TcGemm &g, const uint8_t *w_codes, const uint8_t *w_scales, int rows, int K);
 cudaError_t launch_tc_gemm(const TcGemm &g, const LaunchCtx &lc);

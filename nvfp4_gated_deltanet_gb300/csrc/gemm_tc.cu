@@ -625,6 +625,215 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- weight-stationary form
+// K = 2048 (the in-projection): a 128-row weight tile is 128 KB of codes and
+// 16 KB of scales, so it stays in shared memory while the CTA walks a run of
+// token tiles. CTA c takes the output tiles [c U / G, (c + 1) U / G) of the U
+// tiles in weight-tile-major order (G CTAs, one per SM), so it holds one or two
+// weight tiles in turn; only the 128-token activation tiles stream through the
+// S-stage ring. The weight scales go into TMEM once per weight tile (columns
+// 0..127, four per 64-wide K step); accumulators at columns 128 and 256; the
+// activation scales of ring stage s at 384 + 16 s. The MMA thread commits
+// `afree` after the last MMA on a weight tile; the producer reloads the
+// weights only after it fires. The epilogue stores straight from registers.
+constexpr int kWK = 2048;
+constexpr int kWKt = kWK / 256;                 // 256-wide K tiles
+constexpr int kWCodes = kWKt * kATile;          // 128 KB
+constexpr int kWScales = (kWK / 64) * kSFAtom;  // 16 KB
+constexpr int kWStages = 4;
+constexpr int kWCpBatch = 2;  // ring stages per scale-copy batch (divides kWKt and kWStages; 2 measured best)
+static_assert(kWKt % kWCpBatch == 0 && kWStages % kWCpBatch == 0, "scale-copy batches");
+
+constexpr size_t wstat_smem_bytes() {
+  return 1024 + (size_t)kWCodes + (size_t)kWStages * (128 * 128) + kWScales + (size_t)kWStages * 4 * kSFAtom +
+         (2 * kWStages + 6) * 8 + 16;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_nvf4_wstat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           TcArgs a) {
+  constexpr int S = kWStages;
+  static_assert(384 + 16 * S <= kPTmemCols, "scale columns exceed the allocation");
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  unsigned char *sA = sm;                            // [kWKt][16 KB] swizzled weight codes
+  unsigned char *sB0 = sA + kWCodes;                 // [S][16 KB] swizzled activation codes
+  unsigned char *sSFA = sB0 + S * 128 * 128;         // [32][512 B] weight scale atoms
+  unsigned char *sSFB0 = sSFA + kWScales;            // [S][4][512 B] activation scale atoms
+  uint64_t *full = reinterpret_cast<uint64_t *>(sSFB0 + S * 4 * kSFAtom);
+  uint64_t *empty = full + S;
+  uint64_t *tfull = empty + S;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *afull = tempty + 2;
+  uint64_t *afree = afull + 1;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(afree + 1);
+  volatile uint32_t *eflag = tmem_holder + 1;  // [2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (a.Ma + 127) >> 7, n_tiles = (a.Nb + 127) >> 7;
+  const long long U = (long long)m_tiles * n_tiles;
+  const int u0 = (int)(U * blockIdx.x / gridDim.x), u1 = (int)(U * (blockIdx.x + 1) / gridDim.x);
+  constexpr int ksteps = kWK / 64;
+  if (a.early_trigger) pdl_launch_dependents();
+  if (a.K != kWK) {  // host-side contract broken: refuse, uniformly
+    if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(a.status, GDN_E_SHAPE);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, 128);
+    }
+    mbar_init(afull, 1);
+    mbar_init(afree, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, kPTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      auto load_w = [&](int mt) {
+        mbar_arrive_expect_tx(afull, kWCodes + kWScales);
+        for (int kt = 0; kt < kWKt; ++kt) {
+          if (a.a_tiles)
+            bulk_g2s(sA + kt * kATile, a.a_tiles + ((size_t)mt * kWKt + kt) * kATile, kATile, afull);
+          else
+            tma_load_2d(sA + kt * kATile, &tmA, kt * 128, mt * 128, afull);
+        }
+        bulk_g2s(sSFA, a.sfa_tiled + (size_t)mt * ksteps * kSFAtom, kWScales, afull);
+      };
+      int cur = -1, na = 0, g = 0;
+      if (u0 < u1 && a.a_const) {  // the weights do not depend on the preceding kernel
+        cur = u0 / n_tiles;
+        load_w(cur);
+        na = 1;
+      }
+      pdl_wait();
+      if (!a.early_trigger) pdl_launch_dependents();
+      for (int u = u0; ok && u < u1; ++u) {
+        const int mt = u / n_tiles, nt = u % n_tiles;
+        if (mt != cur) {
+          if (na > 0 && !mbar_wait(afree, (uint32_t)((na - 1) & 1))) { ok = false; break; }
+          load_w(mt);
+          cur = mt;
+          ++na;
+        }
+        for (int kt = 0; kt < kWKt; ++kt, ++g) {
+          const int s = g % S, r = g / S;
+          if (r > 0 && !mbar_wait(empty + s, (uint32_t)((r - 1) & 1))) { ok = false; break; }
+          mbar_arrive_expect_tx(full + s, 128 * 128 + 4 * kSFAtom);
+          tma_load_2d(sB0 + s * 128 * 128, &tmB, kt * 128, nt * 128, full + s);
+          bulk_g2s(sSFB0 + s * 4 * kSFAtom, a.sfb_tiled + ((size_t)nt * ksteps + (size_t)kt * 4) * kSFAtom,
+                   4 * kSFAtom, full + s);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_nvf4<128>();
+      int cur = -1, na = 0, g = 0, i = 0;
+      for (int u = u0; ok && u < u1; ++u, ++i) {
+        const int mt = u / n_tiles, b = i & 1;
+        if (mt != cur) {
+          if (na > 0) tc_commit(afree);  // every MMA on the previous weight tile
+          if (!mbar_wait(afull, (uint32_t)(na & 1))) { ok = false; break; }
+          tc_fence_after();
+          for (int j = 0; j < ksteps; ++j) tc_cp_scales(tmem + 4 * j, desc_scales(smem_u32(sSFA) + j * kSFAtom));
+          cur = mt;
+          ++na;
+        }
+        if (i >= 2 && !mbar_wait(tempty + b, (uint32_t)(((i >> 1) - 1) & 1))) { ok = false; break; }
+        tc_fence_after();
+        // kWCpBatch ring stages at a time: their scale copies, then their MMAs
+        for (int kt = 0; kt < kWKt; kt += kWCpBatch, g += kWCpBatch) {
+#pragma unroll
+          for (int p = 0; p < kWCpBatch; ++p)
+            if (ok && !mbar_wait(full + (g + p) % S, (uint32_t)(((g + p) / S) & 1))) ok = false;
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int p = 0; p < kWCpBatch; ++p) {
+            const int s = (g + p) % S;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc_cp_scales(tmem + 384 + 16 * s + 4 * j, desc_scales(smem_u32(sSFB0 + s * 4 * kSFAtom) + j * kSFAtom));
+          }
+#pragma unroll
+          for (int p = 0; p < kWCpBatch; ++p) {
+            const int s = (g + p) % S, k = kt + p;
+            const uint32_t sfb = tmem + 384 + 16 * s;
+            const uint64_t ad = desc_sw128(smem_u32(sA + k * kATile)), bd = desc_sw128(smem_u32(sB0 + s * 128 * 128));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc_mma_nvf4(tmem + 128 + b * 128, ad + 2 * j, bd + 2 * j, idesc, tmem + 4 * (k * 4 + j), sfb + 4 * j,
+                          (k | j) != 0);
+            tc_commit(empty + s);
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull + b);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const int t = threadIdx.x - 64;
+    uint16_t *C = static_cast<uint16_t *>(a.c);
+    int i = 0;
+    for (int u = u0; u < u1; ++u, ++i) {
+      const int b = i & 1;
+      const int mt = u / n_tiles, nt = u % n_tiles;
+      // one thread waits, all 128 leave together if the wait gives up; the flag
+      // alternates so that one barrier per tile keeps its reads and writes apart
+      if (t == 0) eflag[b] = mbar_wait(tfull + b, (uint32_t)((i >> 1) & 1)) ? 1u : 0u;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (eflag[b] == 0) { ok = false; break; }
+      tc_fence_after();
+      const int m = mt * 128 + row;
+      const float ts = (m < a.a_split ? a.ts_a0 : a.ts_a1) * a.ts_b;
+      const int nlim = min(128, a.Nb - nt * 128);
+      uint16_t *dst = C + (size_t)nt * 128 * a.ldc + m;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + 128 + b * 128 + c0, r);
+        tmem_ld_wait();
+        if (m < a.Ma) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (c0 + c < nlim) dst[(size_t)(c0 + c) * a.ldc] = f32_to_bf16_bits(__uint_as_float(r[c]) * ts);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty + b);  // the accumulator may take the tile after next
+    }
+  }
+  if (!ok && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -702,6 +911,34 @@ constexpr size_t kSmemCap = 227 * 1024;
 constexpr int kPersistStages = 5;
 static_assert(persist_smem_bytes<kPersistStages>() <= kSmemCap, "persistent GEMM shared memory");
 
+static_assert(wstat_smem_bytes() <= kSmemCap, "weight-stationary GEMM shared memory");
+
+cudaError_t launch_wstat(const TcGemm &g, const LaunchCtx &lc) {
+  CUtensorMap mB;
+  if (!make_map(&mB, g.b_codes, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 2, 128, 128, true))
+    return cudaErrorInvalidValue;
+  constexpr size_t smem = wstat_smem_bytes();
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_nvf4_wstat_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int ntiles = ((g.args.Ma + 127) / 128) * ((g.args.Nb + 127) / 128);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(min(ntiles, lc.num_sms), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_nvf4_wstat_kernel, g.mapA, mB, g.args);
+}
+
 cudaError_t launch_persist(const TcGemm &g, const LaunchCtx &lc) {
   CUtensorMap mB;
   if (!make_map(&mB, g.b_codes, (uint64_t)g.args.Nb, (uint64_t)g.args.K / 2, 128, 128, true))
@@ -766,12 +1003,17 @@ cudaError_t launch_tc_gemm(const TcGemm &g, const LaunchCtx &lc) {
     while (ks < 8 && (a.K / 256) / ks > 4) ks *= 2;
     if ((a.K / 256) % ks || (a.K / 256) / ks > 4) return cudaErrorInvalidValue;
   }
-  // persistent form: 128-row activation tiles, at least two output tiles per SM
-  // (measured on GB300: prefill T = 16384 4.76 -> 4.47 ms; with 1.3 tiles per
-  // SM, batch 256, the tile-per-CTA kernel is faster)
-  if (!a.b_bf16 && a.sfa_tiled && a.sfb_tiled && a.c_is_bf16 && ks == 1 && bn == 128 && g.persist != 1 &&
-      (g.persist == 2 || m_tiles * n_tiles >= 2 * lc.num_sms))
-    return launch_persist(g, lc);
+  // persistent forms: 128-token activation tiles, tiled scales, BF16 out.
+  // Weight-stationary for K = 2048 with at least 16 token tiles per weight
+  // tile; else the streaming persistent kernel from two output tiles per SM
+  // (measured on GB300: with 1.3 tiles per SM, batch 256, the tile-per-CTA
+  // kernel is faster).
+  if (!a.b_bf16 && a.sfa_tiled && a.sfb_tiled && a.c_is_bf16 && ks == 1 && bn == 128 && g.persist != 1) {
+    const bool wstat_ok = a.K == kWK && a.a_const;
+    if (g.persist == 3 ? wstat_ok : (g.persist == 0 && wstat_ok && n_tiles >= 16 && m_tiles * n_tiles >= 2 * lc.num_sms))
+      return launch_wstat(g, lc);
+    if (g.persist == 2 || m_tiles * n_tiles >= 2 * lc.num_sms) return launch_persist(g, lc);
+  }
   switch (bn) {
     case 16: return launch_bn<16>(g, ks, lc);
     case 32: return launch_bn<32>(g, ks, lc);

@@ -1,11 +1,13 @@
-"""The persistent form of the tensor-core projections (tuning knob 11: one CTA
-per SM walking the 128 x 128 output tiles, an operand ring that runs across
-tiles and two TMEM accumulators) issues the same MMAs in the same K order into
-one accumulator per tile and applies the same epilogue as the one-tile-per-CTA
-kernel, so prefill and large-batch decode are bit-identical between the two:
-outputs, recurrent and conv states. The sizes give each CTA several tiles
-(both accumulators reused, the ring wrapping mid-tile) and ragged edges in
-both the token and the weight-row direction."""
+"""The persistent forms of the tensor-core projections (tuning knob 11: one CTA
+per SM walking the 128 x 128 output tiles with two TMEM accumulators; the
+streaming form runs one operand ring across tiles, the weight-stationary form
+keeps a weight tile and its scales resident while it walks token tiles) issue
+the same MMAs in the same K order into one accumulator per tile and apply the
+same scaling as the one-tile-per-CTA kernel, so prefill and large-batch decode
+are bit-identical between all three: outputs, recurrent and conv states. The
+sizes give each CTA several tiles (both accumulators reused, the ring wrapping
+mid-tile, weight tiles reloaded mid-run) and ragged edges in both the token and
+the weight-row direction."""
 import numpy as np
 import pytest
 
@@ -26,10 +28,10 @@ def api():
     return pkg
 
 
-def _both(api, run):
+def _all(api, run):
     res = {}
     try:
-        for knob in (1, 2):
+        for knob in (1, 2, 3):
             api.lib().gdn_set_tuning(KNOB, knob)
             res[knob] = run()
     finally:
@@ -50,9 +52,10 @@ def test_persistent_prefill_is_bitwise_the_tile_kernel(api, shape_name, T):
         assert layer.check() == 0
         return out, to_host(conv), to_host(ssm)
 
-    res = _both(api, run)
-    for a, b in zip(res[1], res[2]):
-        np.testing.assert_array_equal(a, b)
+    res = _all(api, run)
+    for k in (2, 3):
+        for a, b in zip(res[1], res[k]):
+            np.testing.assert_array_equal(a, b)
     assert np.any(res[2][0])
 
 
@@ -68,6 +71,7 @@ def test_persistent_large_batch_is_bitwise_the_tile_kernel(api, B):
         assert layer.check() == 0
         return outs, to_host(c), to_host(s)
 
-    res = _both(api, run)
-    for a, b in zip(res[1], res[2]):
-        np.testing.assert_array_equal(a, b)
+    res = _all(api, run)
+    for k in (2, 3):
+        for a, b in zip(res[1], res[k]):
+            np.testing.assert_array_equal(a, b)
