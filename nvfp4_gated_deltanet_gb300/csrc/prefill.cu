@@ -183,7 +183,9 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
   const int nc = a.Tp / kC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  for (int e = tid; e < kC * D / 4; e += blockDim.x) {
+  // every load of the staging is issued before any of them is waited on
+#pragma unroll
+  for (int e = tid; e < kC * D / 4; e += 256) {
     const int i = (4 * e) / D, d = (4 * e) % D;
     const bool live = t0 + i < a.T;
     const float4 kv = live ? *reinterpret_cast<const float4 *>(a.kn + ((size_t)kh * a.Tp + t0 + i) * D + d)
@@ -196,11 +198,13 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
   if (tid < kC) {
     const bool live = t0 + tid < a.T;
     bet[tid] = live ? a.beta[(size_t)h * a.Tp + t0 + tid] : 0.0f;
+    gam[tid] = live ? a.gl[(size_t)h * a.Tp + t0 + tid] : 0.0f;
   }
-  if (tid == 0) {  // cumulative log-decay, in token order
+  __syncthreads();
+  if (tid == 0) {  // cumulative log-decay, in token order, from shared memory
     float acc = 0.0f;
     for (int i = 0; i < kC; ++i) {
-      acc += (t0 + i < a.T) ? a.gl[(size_t)h * a.Tp + t0 + i] : 0.0f;
+      acc += gam[i];
       gam[i] = acc;
     }
   }
@@ -459,7 +463,8 @@ __global__ void __launch_bounds__(512) chunk_scan_kernel(PrefillArgs a) {
 // to the FP32 state), since eight warps read each of their fragments.
 __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
   constexpr int D = 128, R = 32, NSL = D / R;
-  constexpr int XLD = D + 4;   // W, Q, K rows
+  constexpr int XLD = D + 4;   // W, Q rows
+  constexpr int KLD = D + 8;   // K rows (read with the token index across lanes)
   constexpr int SLD = D + 4;   // S rows
   constexpr int ULD = R + 8;   // U, Cf rows
   constexpr int ALD = kC + 4;  // A rows
@@ -467,8 +472,8 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
   extern __shared__ __align__(16) float sm[];
   float *Ws = sm;                    // [kC][XLD]
   float *Qs = Ws + kC * XLD;         // [kC][XLD]
-  float *Ks = Qs + kC * XLD;         // [kC][XLD]
-  float *Us = Ks + kC * XLD;         // [kC][ULD]  Ut slice, then U
+  float *Ks = Qs + kC * XLD;         // [kC][KLD]
+  float *Us = Ks + kC * KLD;         // [kC][ULD]  Ut slice, then U
   float *As = Us + kC * ULD;         // [kC][ALD]
   float *Gs = As + kC * ALD;         // [kC]
   float *S = Gs + kC;                // [R][SLD]
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
     const float *k = a.kn + ((size_t)kh * a.Tp + (size_t)c * kC) * D;
     for (int e = tid; e < kC * D / 4; e += blockDim.x) {
       const int i = (4 * e) / D, d = (4 * e) % D;
-      cp_async16(Ks + i * XLD + d, k + 4 * e, c * kC + i < a.T);
+      cp_async16(Ks + i * KLD + d, k + 4 * e, c * kC + i < a.T);
     }
     const float *u = a.Ut + ((size_t)h * nc + c) * kC * D + r0;
     for (int e = tid; e < kC * R / 4; e += blockDim.x) {
@@ -601,8 +606,8 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
                                 Cfh[(k0 + t + 4) * ULD + m0 + g], Cfh[(k0 + t + 4) * ULD + m0 + g + 8]};
         const uint32_t al[4] = {Cfl[(k0 + t) * ULD + m0 + g], Cfl[(k0 + t) * ULD + m0 + g + 8],
                                 Cfl[(k0 + t + 4) * ULD + m0 + g], Cfl[(k0 + t + 4) * ULD + m0 + g + 8]};
-        const float b0[2] = {Ks[(k0 + t) * XLD + n0 + g], Ks[(k0 + t + 4) * XLD + n0 + g]};
-        const float b1[2] = {Ks[(k0 + t) * XLD + n0 + 8 + g], Ks[(k0 + t + 4) * XLD + n0 + 8 + g]};
+        const float b0[2] = {Ks[(k0 + t) * KLD + n0 + g], Ks[(k0 + t + 4) * KLD + n0 + g]};
+        const float b1[2] = {Ks[(k0 + t) * KLD + n0 + 8 + g], Ks[(k0 + t + 4) * KLD + n0 + 8 + g]};
         uint32_t bh[2], bl[2];
         split2(b0, bh, bl);
         mma3_split(d0, ah, al, bh, bl);
@@ -700,7 +705,7 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
   const int nc = a.Tp / kC;
   chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
   if (D == 128 && a.scan_tc) {
-    const size_t sm_tc = (size_t)(3 * kC * (D + 4) + kC * 40 + kC * (kC + 4) + kC + 32 * (D + 4) + 2 * kC * 33 +
+    const size_t sm_tc = (size_t)(2 * kC * (D + 4) + kC * (D + 8) + kC * 40 + kC * (kC + 4) + kC + 32 * (D + 4) + 2 * kC * 33 +
                                   2 * kC * 40 + 2 * 32 * (D + 4)) * sizeof(float);
     static bool configured_tc = false;
     if (!configured_tc) {
