@@ -79,6 +79,16 @@ GDN_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 GDN_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 16 consecutive 32-bit columns of this warp's TMEM lane quarter from registers
+GDN_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+GDN_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 GDN_DEV void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 GDN_DEV void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -633,23 +643,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 // weight tiles in turn; only the 128-token activation tiles stream through the
 // S-stage ring. The weight scales go into TMEM once per weight tile (columns
 // 0..127, four per 64-wide K step); accumulators at columns 128 and 256; the
-// activation scales of ring stage s at 384 + 16 s. The MMA thread commits
-// `afree` after the last MMA on a weight tile; the producer reloads the
-// weights only after it fires. The epilogue stores straight from registers.
+// activation scales of ring stage s at 384 + 16 s. The activation scales are
+// put into TMEM by four warps of their own with tcgen05.st (each writes its
+// lane quarter: the 16-byte scale row of each 64-wide K step, the layout
+// tcgen05.cp.32x128b.warpx4 would give), so the MMA thread issues only MMAs
+// per ring stage. The MMA thread commits `afree` after the last MMA on a
+// weight tile; the producer reloads the weights only after it fires. The
+// epilogue stores straight from registers. Warps: 0 producer, 1 MMA, 2..5
+// epilogue, 6..9 activation scales.
 constexpr int kWK = 2048;
 constexpr int kWKt = kWK / 256;                 // 256-wide K tiles
 constexpr int kWCodes = kWKt * kATile;          // 128 KB
 constexpr int kWScales = (kWK / 64) * kSFAtom;  // 16 KB
 constexpr int kWStages = 4;
-constexpr int kWCpBatch = 2;  // ring stages per scale-copy batch (divides kWKt and kWStages; 2 measured best)
-static_assert(kWKt % kWCpBatch == 0 && kWStages % kWCpBatch == 0, "scale-copy batches");
+constexpr int kWThreads = 320;
 
 constexpr size_t wstat_smem_bytes() {
   return 1024 + (size_t)kWCodes + (size_t)kWStages * (128 * 128) + kWScales + (size_t)kWStages * 4 * kSFAtom +
-         (2 * kWStages + 6) * 8 + 16;
+         (3 * kWStages + 6) * 8 + 16;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kWThreads, 1)
     gemm_nvf4_wstat_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            TcArgs a) {
   constexpr int S = kWStages;
@@ -663,7 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char *sSFB0 = sSFA + kWScales;            // [S][4][512 B] activation scale atoms
   uint64_t *full = reinterpret_cast<uint64_t *>(sSFB0 + S * 4 * kSFAtom);
   uint64_t *empty = full + S;
-  uint64_t *tfull = empty + S;
+  uint64_t *sready = empty + S;  // [S] the stage's activation scales are in TMEM (4 warp arrivals)
+  uint64_t *tfull = sready + S;
   uint64_t *tempty = tfull + 2;
   uint64_t *afull = tempty + 2;
   uint64_t *afree = afull + 1;
@@ -685,6 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
+      mbar_init(sready + s, 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
@@ -760,35 +776,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (i >= 2 && !mbar_wait(tempty + b, (uint32_t)(((i >> 1) - 1) & 1))) { ok = false; break; }
         tc_fence_after();
-        // kWCpBatch ring stages at a time: their scale copies, then their MMAs
-        for (int kt = 0; kt < kWKt; kt += kWCpBatch, g += kWCpBatch) {
-#pragma unroll
-          for (int p = 0; p < kWCpBatch; ++p)
-            if (ok && !mbar_wait(full + (g + p) % S, (uint32_t)(((g + p) / S) & 1))) ok = false;
-          if (!ok) break;
+        for (int kt = 0; kt < kWKt; ++kt, ++g) {
+          const int s = g % S, r = g / S;
+          if (!mbar_wait(full + s, (uint32_t)(r & 1)) || !mbar_wait(sready + s, (uint32_t)(r & 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
+          const uint32_t sfb = tmem + 384 + 16 * s;
+          const uint64_t ad = desc_sw128(smem_u32(sA + kt * kATile)), bd = desc_sw128(smem_u32(sB0 + s * 128 * 128));
 #pragma unroll
-          for (int p = 0; p < kWCpBatch; ++p) {
-            const int s = (g + p) % S;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tc_cp_scales(tmem + 384 + 16 * s + 4 * j, desc_scales(smem_u32(sSFB0 + s * 4 * kSFAtom) + j * kSFAtom));
-          }
-#pragma unroll
-          for (int p = 0; p < kWCpBatch; ++p) {
-            const int s = (g + p) % S, k = kt + p;
-            const uint32_t sfb = tmem + 384 + 16 * s;
-            const uint64_t ad = desc_sw128(smem_u32(sA + k * kATile)), bd = desc_sw128(smem_u32(sB0 + s * 128 * 128));
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tc_mma_nvf4(tmem + 128 + b * 128, ad + 2 * j, bd + 2 * j, idesc, tmem + 4 * (k * 4 + j), sfb + 4 * j,
-                          (k | j) != 0);
-            tc_commit(empty + s);
-          }
+          for (int j = 0; j < 4; ++j)
+            tc_mma_nvf4(tmem + 128 + b * 128, ad + 2 * j, bd + 2 * j, idesc, tmem + 4 * (kt * 4 + j), sfb + 4 * j,
+                        (kt | j) != 0);
+          tc_commit(empty + s);
         }
         if (!ok) break;
         tc_commit(tfull + b);
       }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------ activation scales -> TMEM (warps 6..9)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int nst = (u1 - u0) * kWKt;
+    for (int g = 0; g < nst; ++g) {
+      const int s = g % S, r = g / S;
+      // lane 0 waits and the warp follows it, so the collective TMEM store
+      // below always runs with all 32 lanes (or none)
+      const int got = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(full + s, (uint32_t)(r & 1)) : 0, 0);
+      __syncwarp();
+      if (!got) { ok = false; break; }
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // K step j: scale row `lane` of the stage's atom j
+        const uint4 x = *reinterpret_cast<const uint4 *>(sSFB0 + s * 4 * kSFAtom + j * kSFAtom + lane * 16);
+        v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+      }
+      tmem_st16(tmem + ((uint32_t)(q * 32) << 16) + 384 + 16 * s, v);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sready + s);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
@@ -928,7 +956,7 @@ cudaError_t launch_wstat(const TcGemm &g, const LaunchCtx &lc) {
   const int ntiles = ((g.args.Ma + 127) / 128) * ((g.args.Nb + 127) / 128);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(min(ntiles, lc.num_sms), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kWThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = lc.stream;
   cudaLaunchAttribute attr[1];

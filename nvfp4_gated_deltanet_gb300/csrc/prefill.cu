@@ -20,7 +20,8 @@
 //               and the state slice, kept in shared memory across chunks
 //   gnorm       (token)             z-gated RMSNorm + NVFP4 quantisation of y
 //   conv_tail   (channel)           the slot's conv state after the last token
-// The chunk products run in FP32 on the CUDA cores.
+// The chunk products run on warp-level tensor-core MMA in split TF32 (d = 128;
+// FP32 on the CUDA cores for the smaller head sizes and on request).
 #include "common.cuh"
 
 namespace gdn {
@@ -40,7 +41,7 @@ constexpr int kPrepTT = 32;
 template <int D>
 __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
   __shared__ __align__(16) uint16_t win[kPrepTT + 3][D];
-  __shared__ float outv[kPrepTT][D + 1];
+  __shared__ __align__(16) float outv[kPrepTT][D + 4];  // rows 16-byte aligned for vector reads
   const int t0 = blockIdx.x * kPrepTT, grp = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ngrp = 2 * a.Hk + a.Hv;
@@ -109,15 +110,24 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
       for (int e = 0; e < EPL; ++e) p = fmaf(outv[i][lane * EPL + e], outv[i][lane * EPL + e], p);
       p = warp_sum(p);
       const float r = isq ? (1.0f / sqrtf(p + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(p + a.l2_eps);
-      if (t < a.T)
+      if (t < a.T) {
+        if constexpr (EPL == 4) {  // one 16-byte store per lane
+          const float4 o4 = *reinterpret_cast<const float4 *>(&outv[i][lane * 4]);
+          *reinterpret_cast<float4 *>(dst + (size_t)t * D + lane * 4) = make_float4(o4.x * r, o4.y * r, o4.z * r, o4.w * r);
+        } else {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) dst[(size_t)t * D + lane * EPL + e] = outv[i][lane * EPL + e] * r;
+          for (int e = 0; e < EPL; ++e) dst[(size_t)t * D + lane * EPL + e] = outv[i][lane * EPL + e] * r;
+        }
+      }
     }
   } else {
     const int h = grp - 2 * nq;
-    for (int e = tid; e < kPrepTT * D; e += blockDim.x) {
-      const int i = e / D, c = e % D;
-      if (t0 + i < a.T) a.v[((size_t)h * a.Tp + t0 + i) * D + c] = outv[i][c];
+    constexpr int V4 = D / 4;
+    for (int e = tid; e < kPrepTT * V4; e += blockDim.x) {
+      const int i = e / V4, c = 4 * (e % V4);
+      if (t0 + i < a.T)
+        *reinterpret_cast<float4 *>(a.v + ((size_t)h * a.Tp + t0 + i) * D + c) =
+            *reinterpret_cast<const float4 *>(&outv[i][c]);
     }
   }
 }
@@ -650,13 +660,32 @@ __global__ void gnorm_kernel(PrefillArgs a) {
   const int h = i / per_head, e0 = (i % per_head) * 16;
   const float *op = a.o + ((size_t)t * a.Hv + h) * D + e0;
   const uint16_t *zp = a.proj + (size_t)t * a.ld + 2 * a.Hk * D + vd + h * D + e0;
-  float ov[16];
+  float ov[16], zv[16], nw[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {  // o rows and the norm weight are 64-byte aligned per 16-block
+    const float4 o4 = reinterpret_cast<const float4 *>(op)[q];
+    const float4 w4 = reinterpret_cast<const float4 *>(a.norm_w + e0)[q];
+    ov[4 * q] = o4.x; ov[4 * q + 1] = o4.y; ov[4 * q + 2] = o4.z; ov[4 * q + 3] = o4.w;
+    nw[4 * q] = w4.x; nw[4 * q + 1] = w4.y; nw[4 * q + 2] = w4.z; nw[4 * q + 3] = w4.w;
+  }
+  if (a.ld % 8 == 0) {  // z rows 16-byte aligned
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 z4 = reinterpret_cast<const uint4 *>(zp)[q];
+      const uint32_t w[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        zv[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
+        zv[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) zv[k] = bf16_bits_to_f32(zp[k]);
+  }
   float p = 0.0f;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    ov[k] = op[k];
-    p = fmaf(ov[k], ov[k], p);
-  }
+  for (int k = 0; k < 16; ++k) p = fmaf(ov[k], ov[k], p);
   // the head's 16-element group sums added in group order (as in decode)
   const int first = (threadIdx.x & 31) & ~(per_head - 1);
   float tot = 0.0f;
@@ -665,7 +694,7 @@ __global__ void gnorm_kernel(PrefillArgs a) {
   const float rstd = 1.0f / sqrtf(p / (float)D + a.rms_eps);
   float y[16];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) y[k] = ov[k] * rstd * a.norm_w[e0 + k] * siluf_(bf16_bits_to_f32(zp[k]));
+  for (int k = 0; k < 16; ++k) y[k] = ov[k] * rstd * nw[k] * siluf_(zv[k]);
   uint32_t lo, hi, s;
   const bool ok = quant_block16(y, a.ts_out, inv6ts_of(a.ts_out), lo, hi, s);
   if ((int)threadIdx.x >= nblk) return;
