@@ -321,6 +321,44 @@ def time_prefill(pkg, synth, T, reps=3):
     return {"ms": round(ms, 3), "tokens_per_s": round(T / (ms * 1e-3))}
 
 
+def fp4_peak():
+    """Dense FP4 tensor peak: the measured BF16 GEMM burst x the nominal FP4 / BF16
+    ratio (13.5 / 2.25 PFLOP/s dense)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]) * 6.0, "measured bf16 burst x 6 (nominal fp4/bf16 ratio)"
+    except Exception:
+        return 1900.0 * 6.0, "fallback bf16 x 6 (nominal fp4/bf16 ratio)"
+
+
+def time_in_proj(pkg, synth, T, reps=20):
+    """The prefill in-projection alone (NVFP4 quantisation of x, then the W4A4
+    q|k|v|z|b|a GEMM on tcgen05) over T tokens, through gdn_in_proj."""
+    import numpy as np
+    import torch
+    w = synth.layer_weights(synth.FULL, 1)
+    L = pkg.layer_from_synth(w, max_batch=1, max_prefill_tokens=T)
+    x = torch.from_numpy(synth.x_tokens(synth.FULL, 7, T).view(np.int16)).cuda()
+    nin = 2 * L.Hk * L.D + 2 * L.Hv * L.D + 2 * L.Hv
+    out = torch.empty(T, nin, dtype=torch.int16, device="cuda")
+    for _ in range(3):
+        L.in_proj(x, None, out)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        L.in_proj(x, None, out)
+    e1.record(st)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    tflops = 2.0 * nin * T * L.H / (us * 1e-6) / 1e12
+    peak, kind = fp4_peak()
+    return {"us": round(us, 2), "tflops": round(tflops, 1), "fp4_peak_tflops": round(peak, 1),
+            "frac_of_fp4_peak": round(tflops / peak, 4), "peak_kind": kind,
+            "note": "quantisation kernel + persistent tcgen05 GEMM; operands L2-resident"}
+
+
 def cpu_baseline_leg(seconds_budget=15.0):
     """The oracle, single-threaded, on config-1 decode steps: a bounded sample."""
     code = (
@@ -524,6 +562,9 @@ def main():
                 torch.cuda.empty_cache()
         for T in (1024, 4096, 16384):
             extra[f"prefill{T}"] = time_prefill(pkg, synth, T)
+            torch.cuda.empty_cache()
+        for T in (4096, 16384):
+            extra[f"prefill{T}_in_proj"] = time_in_proj(pkg, synth, T)
             torch.cuda.empty_cache()
 
     cpu = None if (args.no_cpu or rank != 0) else cpu_baseline_leg()

@@ -159,12 +159,13 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
                            uint16_t *out, uint16_t *conv_state, void *ssm_state, int num_slots,
                            void *stream);
 
-/* The in-projection stage of gdn_decode_step alone (for stage-wise checks and
- * timing): x BF16 [B][H] -> proj BF16 [B][2*Hk*d_k + 2*Hv*d_v + 2*Hv], each
- * row q | k | v | z | b | a; rows whose slot_ids entry is negative are zero
- * (slot_ids: device int32 [B], or NULL for none). Same kernels and results as
- * inside gdn_decode_step. Errors: GDN_E_NULL, GDN_E_ALIGN, GDN_E_SHAPE
- * (B < 1 or > max_batch), GDN_E_CUDA. */
+/* The in-projection stage of gdn_decode_step (B <= max_batch) or gdn_prefill
+ * (B tokens) alone, for stage-wise checks and timing: x BF16 [B][H] -> proj
+ * BF16 [B][2*Hk*d_k + 2*Hv*d_v + 2*Hv], each row q | k | v | z | b | a; rows
+ * whose slot_ids entry is negative are zero (slot_ids: device int32 [B], or
+ * NULL for none). Same kernels and results as inside those calls for the same
+ * row count. Errors: GDN_E_NULL, GDN_E_ALIGN, GDN_E_SHAPE (B < 1 or more than
+ * max(max_batch, max_prefill_tokens)), GDN_E_CUDA. */
 gdn_status gdn_in_proj(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *proj,
                        void *stream);
 
@@ -295,11 +296,11 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * tile overlaps the MMAs of the next. Two forms: streaming (both operands
  * through one shared-memory ring that runs across tiles) and, for a reduction
  * length of 2048, weight-stationary (a CTA keeps a 128-row weight tile and its
- * scales resident and streams only activation tiles). 0 = automatic, the
- * default: weight-stationary with at least 16 token tiles and two output tiles
- * per SM, else streaming from two output tiles per SM, else one tile per CTA;
- * 1 = one tile per CTA; 2 = streaming whenever the form allows; 3 =
- * weight-stationary whenever the form allows.
+ * scales resident and streams only activation tiles; measured slower than
+ * streaming on GB300). 0 = automatic, the default: streaming from two output
+ * tiles per SM, else one tile per CTA; 1 = one tile per CTA; 2 = streaming
+ * whenever the form allows; 3 = weight-stationary whenever the form allows
+ * (else as 2).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

@@ -719,7 +719,7 @@ gdn_status gdn_in_proj(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids,
                        void *stream) {
   if (!ctx || !x || !proj) return GDN_E_NULL;
   if (!aligned16(x) || !aligned16(proj) || (slot_ids && !aligned16(slot_ids))) return GDN_E_ALIGN;
-  if (B < 1 || B > ctx->cfg.max_batch) return GDN_E_SHAPE;
+  if (B < 1 || B > ctx->prow) return GDN_E_SHAPE;  // up to max(max_batch, max_prefill_tokens) rows
   LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, false};
   // a row is zero when its slot id is negative (no slot range to check here)
   return cuda_status(run_in_proj(ctx, x, B, slot_ids, 0x7fffffff, lc, true, proj));

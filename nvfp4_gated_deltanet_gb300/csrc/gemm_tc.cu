@@ -454,8 +454,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // boundaries -- the producer fetches the next tile's operands while the MMAs of
 // this one drain -- and two TMEM accumulators (columns 0 and 128) let the
 // epilogue of tile i overlap the MMAs of tile i + 1. Scales of stage s sit at
-// TMEM column 256 + 32 s. Same warp roles as gemm_nvf4_kernel; the epilogue
-// stages each tile as [128 tokens][128 rows] BF16 in a buffer of its own.
+// TMEM column 256 + 32 s, written by four scale warps with tcgen05.st, so the
+// MMA thread issues only MMAs. Warps: 0 producer, 1 MMA, 2..5 epilogue (each
+// tile staged as [128 tokens][128 rows] BF16 in a buffer of its own), 6..9
+// scales.
+constexpr int kWThreads = 320;  // persistent forms: producer, MMA, 4 epilogue and 4 scale warps
 constexpr int kPStage = kATile + 128 * 128 + 2 * 4 * kSFAtom;  // A codes | B codes | A atoms | B atoms
 constexpr int kPStaging = 128 * 128 * 2;
 constexpr int kPTmemCols = 512;
@@ -463,11 +466,11 @@ static_assert(kPStage % 1024 == 0, "stages stay 1024-byte aligned");
 
 template <int S>
 constexpr size_t persist_smem_bytes() {
-  return 1024 + (size_t)S * kPStage + kPStaging + (2 * S + 4) * 8 + 16;
+  return 1024 + (size_t)S * kPStage + kPStaging + (3 * S + 4) * 8 + 16;
 }
 
 template <int S>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kWThreads, 1)
     gemm_nvf4_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              TcArgs a) {
   static_assert(256 + 32 * S <= kPTmemCols, "scale columns exceed the allocation");
@@ -477,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char *staging = sm + (size_t)S * kPStage;
   uint64_t *full = reinterpret_cast<uint64_t *>(staging + kPStaging);
   uint64_t *empty = full + S;
-  uint64_t *tfull = empty + S;   // [2] accumulator b complete (tcgen05.commit)
+  uint64_t *sready = empty + S;  // [S] the stage's scales are in TMEM (4 warp arrivals)
+  uint64_t *tfull = sready + S;  // [2] accumulator b complete (tcgen05.commit)
   uint64_t *tempty = tfull + 2;  // [2] accumulator b drained by the epilogue (128 arrivals)
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(tempty + 2);
   auto stA = [&](int s) { return sm + (size_t)s * kPStage; };
@@ -496,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
+      mbar_init(sready + s, 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
@@ -561,14 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kt = 0; kt < nkt; ++kt, ++g) {
           const int s = g % S, u = g / S;
-          if (!mbar_wait(full + s, (uint32_t)(u & 1))) { ok = false; break; }
+          if (!mbar_wait(full + s, (uint32_t)(u & 1)) || !mbar_wait(sready + s, (uint32_t)(u & 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sfa = tmem + 256 + 32 * s, sfb = sfa + 16;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_scales(sfa + 4 * j, desc_scales(smem_u32(stAtA(s)) + j * kSFAtom));
-            tc_cp_scales(sfb + 4 * j, desc_scales(smem_u32(stAtB(s)) + j * kSFAtom));
-          }
           const uint64_t ad = desc_sw128(smem_u32(stA(s))), bd = desc_sw128(smem_u32(stB(s)));
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -578,6 +581,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_commit(tfull + b);
       }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------ scales -> TMEM (warps 6..9)
+    // Each warp writes its TMEM lane quarter with tcgen05.st: per 64-wide K
+    // step the 16-byte scale row `lane` of the stage's atom, for both
+    // operands (the layout tcgen05.cp.32x128b.warpx4 would give).
+    const int q = warp & 3;
+    int n_st = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) n_st += nkt;
+    for (int g = 0; g < n_st; ++g) {
+      const int s = g % S, u = g / S;
+      // lane 0 waits and the warp follows it, so the collective TMEM stores
+      // below always run with all 32 lanes (or none)
+      const int got = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(full + s, (uint32_t)(u & 1)) : 0, 0);
+      __syncwarp();
+      if (!got) { ok = false; break; }
+      uint32_t va[16], vb[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(stAtA(s) + j * kSFAtom + lane * 16);
+        const uint4 y = *reinterpret_cast<const uint4 *>(stAtB(s) + j * kSFAtom + lane * 16);
+        va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+        vb[4 * j] = y.x; vb[4 * j + 1] = y.y; vb[4 * j + 2] = y.z; vb[4 * j + 3] = y.w;
+      }
+      const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + 256 + 32 * s;
+      tmem_st16(base, va);
+      tmem_st16(base + 16, vb);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sready + s);
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
@@ -656,7 +690,6 @@ constexpr int kWKt = kWK / 256;                 // 256-wide K tiles
 constexpr int kWCodes = kWKt * kATile;          // 128 KB
 constexpr int kWScales = (kWK / 64) * kSFAtom;  // 16 KB
 constexpr int kWStages = 4;
-constexpr int kWThreads = 320;
 
 constexpr size_t wstat_smem_bytes() {
   return 1024 + (size_t)kWCodes + (size_t)kWStages * (128 * 128) + kWScales + (size_t)kWStages * 4 * kSFAtom +
@@ -982,7 +1015,7 @@ cudaError_t launch_persist(const TcGemm &g, const LaunchCtx &lc) {
   const int ntiles = ((g.args.Ma + 127) / 128) * ((g.args.Nb + 127) / 128);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(min(ntiles, lc.num_sms), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kWThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = lc.stream;
   cudaLaunchAttribute attr[1];
@@ -1032,15 +1065,13 @@ cudaError_t launch_tc_gemm(const TcGemm &g, const LaunchCtx &lc) {
     if ((a.K / 256) % ks || (a.K / 256) / ks > 4) return cudaErrorInvalidValue;
   }
   // persistent forms: 128-token activation tiles, tiled scales, BF16 out.
-  // Weight-stationary for K = 2048 with at least 16 token tiles per weight
-  // tile; else the streaming persistent kernel from two output tiles per SM
-  // (measured on GB300: with 1.3 tiles per SM, batch 256, the tile-per-CTA
-  // kernel is faster).
+  // Automatically the streaming form, from two output tiles per SM (measured
+  // on GB300, prefill in-projection T = 16384: streaming 230 us, weight-
+  // stationary 276 us, one tile per CTA 588 us; with 1.3 tiles per SM, batch
+  // 256, the tile-per-CTA kernel was faster). Weight-stationary on request.
   if (!a.b_bf16 && a.sfa_tiled && a.sfb_tiled && a.c_is_bf16 && ks == 1 && bn == 128 && g.persist != 1) {
-    const bool wstat_ok = a.K == kWK && a.a_const;
-    if (g.persist == 3 ? wstat_ok : (g.persist == 0 && wstat_ok && n_tiles >= 16 && m_tiles * n_tiles >= 2 * lc.num_sms))
-      return launch_wstat(g, lc);
-    if (g.persist == 2 || m_tiles * n_tiles >= 2 * lc.num_sms) return launch_persist(g, lc);
+    if (g.persist == 3 && a.K == kWK && a.a_const) return launch_wstat(g, lc);
+    if (g.persist >= 2 || m_tiles * n_tiles >= 2 * lc.num_sms) return launch_persist(g, lc);
   }
   switch (bn) {
     case 16: return launch_bn<16>(g, ks, lc);

@@ -266,3 +266,23 @@ def test_in_proj_stage_matches_oracle_projections(api):
         assert np.mean(_bf16(got[live]) == want[live]) > 0.99
         if B > 1:
             assert not got[2].any()
+
+
+def test_in_proj_stage_at_prompt_size_matches_oracle_rows(api):
+    """gdn_in_proj over a prompt-sized block of rows (more than max_batch, up to
+    max_prefill_tokens: the persistent tensor-core GEMM with several output
+    tiles per CTA and a ragged last token tile) against the oracle's W4A4
+    product on sampled rows, and rows past the capacity refused."""
+    shape = synth.FULL
+    T = 1000
+    L = api.layer_from_synth(weights("FULL", 1), max_batch=4, max_prefill_tokens=T)
+    O = oracle_layer("FULL", 1)
+    x = synth.x_tokens(shape, 7, T)
+    got = to_host(L.in_proj(to_dev(x)))
+    rows = [0, 1, 127, 128, 555, 999]
+    qkvz, ba = O.projections(x[rows])
+    want = np.concatenate([qkvz, ba], axis=1)
+    assert rel_l2(_bf16(got[rows]), want) <= 1e-5
+    assert np.mean(_bf16(got[rows]) == want) > 0.99
+    with pytest.raises(api.GdnError):
+        L.in_proj(to_dev(synth.x_tokens(shape, 7, T + 1)))
