@@ -95,3 +95,19 @@ def test_python_binding_raises_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(g, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         g.lib()
+
+
+def test_tuning_knob_ranges(L):
+    """Every knob takes its documented values and refuses the rest (GDN_E_RANGE
+    = 6); each is put back to its default (0) afterwards."""
+    valid = {0: (0, 1, 2), 1: (0, 1, 2, 4, 8), 2: (0, 1, 2, 4, 8), 3: (0, 1, 2), 4: (0, 1, 2), 5: (0, 1, 2),
+             6: (0, 1, 2), 7: (0, 1, 2, 4), 8: (0, 1, 2), 9: (0, 1, 2), 10: (0, 1, 2), 11: (0, 1, 2, 3)}
+    try:
+        for knob, values in valid.items():
+            for v in range(-1, 10):
+                assert L.gdn_set_tuning(knob, v) == (0 if v in values else 6), (knob, v)
+        assert L.gdn_set_tuning(12, 0) == 6
+        assert L.gdn_set_tuning(-1, 0) == 6
+    finally:
+        for knob in valid:
+            L.gdn_set_tuning(knob, 0)
