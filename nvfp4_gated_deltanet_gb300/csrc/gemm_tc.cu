@@ -10,13 +10,16 @@
 //
 // Per CTA (6 warps):
 //   warp 0      TMA producer: code tiles (128 B x rows, 128-byte swizzle) and
-//               the row-major scale rows of this K tile, into a ring of S stages
-//   warp 1      tensor-memory allocation, then one thread issues tcgen05.cp
-//               (scales -> TMEM) and tcgen05.mma, committing each stage back
-//               to the producer
-//   warps 2..5  rearrange each stage's scale rows into the 32x16-byte layout
-//               tcgen05.cp reads (row r: byte (r%32)*16 + (r/32)*4 + k-block),
-//               then the epilogue: TMEM -> registers -> scaled BF16/FP32 stores
+//               the scales of this K tile (tiled atoms, or row-major rows),
+//               into a ring of S stages
+//   warp 1      tensor-memory allocation, then one thread issues tcgen05.mma,
+//               committing each stage back to the producer
+//   warps 2..5  put each stage's scales into TMEM with tcgen05.st (each warp
+//               its lane quarter; row-major scale rows are first rearranged
+//               into 512-byte atoms, row r at byte (r%32)*16 + (r/32)*4 +
+//               k-block, the layout tcgen05.cp.32x128b.warpx4 would copy), so
+//               the MMA thread issues nothing but MMAs; then the epilogue:
+//               TMEM -> registers -> scaled BF16/FP32 stores
 // Split-K over a thread-block cluster of KS CTAs: ranks != 0 push their FP32
 // partial tile into rank 0's shared memory before one cluster barrier; rank 0
 // adds them in rank order (deterministic, no atomics).
@@ -151,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char *stage0 = sm;
   float *part = reinterpret_cast<float *>(sm + (size_t)S * L::kStage);
   uint64_t *full = reinterpret_cast<uint64_t *>(part + (KS > 1 ? (KS - 1) * 128 * BN : 0));
-  uint64_t *sfready = full + S;
+  uint64_t *sfready = full + S;  // [S] the stage's scales are in TMEM (one arrival per warp 2..5)
   uint64_t *empty = sfready + S;
   uint64_t *accum = empty + S;
   uint64_t *bready = accum + 1;  // decode form: the quantised B tiles are in place
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(sfready + s, 128);
+      mbar_init(sfready + s, 4);
       mbar_init(empty + s, 1);
     }
     mbar_init(accum, 1);
@@ -245,17 +248,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (bq && !mbar_wait(bready, 0)) ok = false;
       for (int i = 0; i < (ok ? nkt : 0); ++i) {
         const int s = i % S, u = i / S;
-        if (!mbar_wait(full + s, (uint32_t)(u & 1)) || (!tiled && !mbar_wait(sfready + s, (uint32_t)(u & 1)))) {
+        if (!mbar_wait(full + s, (uint32_t)(u & 1)) || !mbar_wait(sfready + s, (uint32_t)(u & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sfa = tmem + 128 + 32 * s, sfb = sfa + 16;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          tc_cp_scales(sfa + 4 * j, desc_scales(smem_u32(stAtA(s)) + j * kSFAtom));
-          tc_cp_scales(sfb + 4 * j, desc_scales(smem_u32(stAtB(s)) + j * kSFAtom));
-        }
         const uint64_t ad = desc_sw128(smem_u32(stA(s))), bd = desc_sw128(smem_u32(stB(s)));
 #pragma unroll
         for (int j = 0; j < 4; ++j) {  // K = 64 per MMA: 32 bytes further along the swizzled rows
@@ -270,6 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int t = threadIdx.x - 64;  // 0..127
+    const int qw = warp & 3;         // TMEM lane quarter this warp may access
+    // this warp's lane quarter of stage s's scales, from the stage's atoms:
+    // per 64-wide K step the 16-byte atom row `lane` (the layout
+    // tcgen05.cp.32x128b.warpx4 would give), A at column 128 + 32 s, B 16 on
+    auto put_scales = [&](int s) {
+      uint32_t va[16], vb[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(stAtA(s) + j * kSFAtom + lane * 16);
+        const uint4 y = *reinterpret_cast<const uint4 *>(stAtB(s) + j * kSFAtom + lane * 16);
+        va[4 * j] = x.x; va[4 * j + 1] = x.y; va[4 * j + 2] = x.z; va[4 * j + 3] = x.w;
+        vb[4 * j] = y.x; vb[4 * j + 1] = y.y; vb[4 * j + 2] = y.z; vb[4 * j + 3] = y.w;
+      }
+      const uint32_t base = tmem + ((uint32_t)(qw * 32) << 16) + 128 + 32 * s;
+      tmem_st16(base, va);
+      tmem_st16(base + 16, vb);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfready + s);
+    };
     // ------------------------------------------------ decode form: quantise B
     if constexpr (BN == 16) if (bq) {
       pdl_wait();  // the activation rows come from the preceding kernel
@@ -333,10 +352,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_shared();  // generic-proxy writes -> visible to tcgen05.mma / tcgen05.cp
       mbar_arrive(bready);
     }
-    // ------------------------------------------------ scale rearrangement
-    for (int i = 0; i < (tiled ? 0 : nkt); ++i) {
+    // ------------------------------------------------ scales -> TMEM
+    if (tiled) {  // atoms copied in by the producer (and, decode form, B's written above)
+      if (bq) asm volatile("bar.sync 1, 128;" ::: "memory");  // every warp's B atoms are in place
+      for (int i = 0; i < nkt; ++i) {
+        const int s = i % S, u = i / S;
+        // lane 0 waits and the warp follows it: the collective TMEM stores run
+        // with all 32 lanes (or none)
+        const int got = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(full + s, (uint32_t)(u & 1)) : 0, 0);
+        __syncwarp();
+        if (!got) { ok = false; break; }
+        put_scales(s);
+      }
+    }
+    volatile uint32_t *sflag = tmem_holder + 1;
+    for (int i = 0; i < (tiled ? 0 : nkt); ++i) {  // row-major scales: rearrange into atoms first
       const int s = i % S, u = i / S;
-      if (!mbar_wait(full + s, (uint32_t)(u & 1))) { ok = false; break; }
+      // one thread waits, the four warps follow it (the named barriers stay matched)
+      if (t == 0) *sflag = mbar_wait(full + s, (uint32_t)(u & 1)) ? 1u : 0u;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (*sflag == 0) { ok = false; break; }
       const uint4 va = *reinterpret_cast<const uint4 *>(stSA(s) + t * 16);
       uint32_t *atA = reinterpret_cast<uint32_t *>(stAtA(s) + (t & 31) * 16 + (t >> 5) * 4);
       atA[0 * kSFAtom / 4] = va.x;
@@ -351,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         atB[2 * kSFAtom / 4] = vb.z;
         atB[3 * kSFAtom / 4] = vb.w;
       }
-      fence_async_shared();  // generic-proxy writes -> visible to tcgen05.cp
-      mbar_arrive(sfready + s);
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // the stage's atoms are complete
+      put_scales(s);
     }
     // ------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
