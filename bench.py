@@ -376,6 +376,47 @@ def cpu_baseline_leg(seconds_budget=15.0):
             "sample": f"{d['n']} config-1 decode c1 layer-steps (full width), single thread, float64/int64 exact"}
 
 
+def cpu_all_cores_leg(seconds_budget=10.0):
+    """The oracle on every host core: one single-threaded process per core, each
+    running config-1 decode steps of its own sequence for the same window;
+    aggregate throughput as us per layer-step. Workers are capped by the host
+    memory (about 2 GB each while the oracle layer is built)."""
+    cores = os.cpu_count() or 1
+    try:
+        with open("/proc/meminfo") as f:
+            avail_kb = next(int(ln.split()[1]) for ln in f if ln.startswith("MemAvailable"))
+        cores = max(1, min(cores, avail_kb // (2 * 1024 * 1024)))
+    except Exception:
+        pass
+    start_at = time.time() + 20.0  # every worker builds its layer first, then all measure together
+    code = (
+        "import os,sys,time,json;sys.path.insert(0,%r);"
+        "from nvfp4_gated_deltanet_gb300 import synth;from oracle import gdn;import numpy as np;"
+        "seed=int(sys.argv[1]);w=synth.layer_weights(synth.FULL,1);L=gdn.Layer(w);"
+        "x=synth.x_tokens(synth.FULL,seed,1000);"
+        "c=synth.conv_state(synth.FULL,seed)[None].copy();s=synth.ssm_state(synth.FULL,seed)[None].copy();"
+        "L.decode_step(x[0:1],[0],c,s)\n"
+        "while time.time()<%f: time.sleep(0.01)\n"
+        "t=time.time();n=0\n"
+        "while time.time()-t<%f and n<999:\n n+=1;L.decode_step(x[n:n+1],[0],c,s)\n"
+        "print(json.dumps({'n':n,'t0':t,'t1':time.time()}))" % (ROOT, start_at, seconds_budget))
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    procs = [subprocess.Popen([sys.executable, "-c", code, str(100 + i)], stdout=subprocess.PIPE,
+                              stderr=subprocess.DEVNULL, text=True, env=env) for i in range(cores)]
+    res = []
+    for p in procs:
+        out, _ = p.communicate(timeout=600)
+        if p.returncode == 0 and out.strip():
+            res.append(json.loads(out.strip().splitlines()[-1]))
+    if not res:
+        return None
+    n = sum(d["n"] for d in res)
+    wall = max(d["t1"] for d in res) - min(d["t0"] for d in res)
+    return {"value": wall / n * 1e6, "unit": UNIT, "cores": len(res), "kind": "oracle",
+            "sample": f"{n} config-1 decode c1 layer-steps over {len(res)} single-threaded processes "
+                      f"(one sequence each) in a {wall:.1f} s window; aggregate throughput"}
+
+
 def reference_arm(args):
     """--impl reference: the CPU oracle on the same workload and metric."""
     rank = int(os.environ.get("RANK", "0"))
@@ -568,6 +609,8 @@ def main():
             torch.cuda.empty_cache()
 
     cpu = None if (args.no_cpu or rank != 0) else cpu_baseline_leg()
+    if cpu is not None:
+        cpu["all_cores"] = cpu_all_cores_leg()
     line = {
         "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False, "scaling": "weak",
