@@ -6,7 +6,7 @@
  * an NVFP4 checkpoint -- W4A4 QKVZ/BA projections, a BF16 causal convolution,
  * an FP32 recurrent state updated by the gated delta rule (state laid out
  * [v][k], the "pretranspose" decode layout), a z-gated RMSNorm and a W4A4
- * output projection. NVFP4 (bloomery issue #565, Round 1, #489/#687): packed
+ * output projection. NVFP4 (bloomery issue #565, §4, #489/#687): packed
  * E2M1 pairs, one E4M3 scale per 16 values, one FP32 scale per tensor; W4A4
  * quantises the activations to NVFP4 as well.
  *
@@ -115,7 +115,7 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
  * work of the context's own allocations (cudaFree). */
 gdn_status gdn_destroy(gdn_ctx *ctx);
 
-/* NVFP4 quantisation of x[rows][cols] (bloomery issue #565, Round 1, #687:
+/* NVFP4 quantisation of x[rows][cols] (bloomery issue #565, §4, #687:
  * "4-bit activations"). x is BF16 bits (x_is_f32 = 0) or FP32 (x_is_f32 = 1);
  * cols % 16 == 0. For every 16-block, in FP32 with round-to-nearest-even:
  *   inv6ts = 1 / (6 * tensor_scale); amax = max |x|; s = E4M3_satfinite(amax * inv6ts);
@@ -180,7 +180,7 @@ gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba,
 
 /* Prefill of T tokens of one sequence held in slot `slot` (host int): the same
  * arithmetic as T successive decode steps of that sequence (bloomery issue #565,
- * Round 1, #812: the delta rule of a prompt runs on tensor cores in chunks).
+ * §4, #812: the delta rule of a prompt runs on tensor cores in chunks).
  * x BF16 [T][H] -> out BF16 [T][H]; init_zero != 0 starts from zero conv and
  * recurrent state (the slot's state is overwritten), else from the slot's
  * state. The slot's state is left as after the last token. Errors: GDN_E_NULL,

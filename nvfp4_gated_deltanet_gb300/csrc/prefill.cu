@@ -1,5 +1,5 @@
 // Prefill of one sequence: the decode arithmetic over T tokens, with the gated
-// delta rule in 64-token chunks (the WY / UT form; bloomery issue #565, Round 1,
+// delta rule in 64-token chunks (the WY / UT form; bloomery issue #565, §4,
 // #812: the delta rule of a prompt runs in chunks on tensor cores).
 //
 // Within a chunk with start state S0 and rows i = 1..64 (per value head):

@@ -1,4 +1,4 @@
-// NVFP4 activation quantiser (bloomery issue #565, Round 1, #687: W4A4 runs
+// NVFP4 activation quantiser (bloomery issue #565, §4, #687: W4A4 runs
 // with 4-bit activations): one thread per 16-element block.
 #include "common.cuh"
 

@@ -20,7 +20,7 @@ What it follows, by page:
   projections, a BF16 causal convolution and an FP32 recurrent state; the
   recurrence follows vLLM's fused_recurrent gated delta rule, the decode state
   layout follows FlashInfer's "pretranspose" decode (state stored [v][k]).
-* bloomery issue #565, Round 1 (#489/#687): NVFP4 is U8-packed E2M1 pairs with
+* bloomery issue #565, §4 (#489/#687): NVFP4 is U8-packed E2M1 pairs with
   one F8_E4M3 scale per 16 values and an FP32 per-tensor scale; W4A4 means the
   activations are quantised to NVFP4 too.
 * Rocket blog, "Moving the KDA state tile out of shared memory is 4.6x at M=8",

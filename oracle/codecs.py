@@ -13,7 +13,7 @@ Encoders round to nearest, ties to the code with an even mantissa (RNE), and
 saturate finite values beyond the largest magnitude to it ("satfinite"). The
 sign is kept, so a negative value that rounds to zero encodes as -0.
 
-NVFP4 packing (bloomery issue #565, Round 1, #489: "U8-packed E2M1 pairs"):
+NVFP4 packing (bloomery issue #565, §4, #489: "U8-packed E2M1 pairs"):
 element 2i sits in the low nibble of byte i, element 2i+1 in the high nibble.
 """
 from __future__ import annotations

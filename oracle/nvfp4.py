@@ -1,6 +1,6 @@
 """NVFP4 quantisation and the block-scaled W4A4 product.
 
-Format (bloomery issue #565, Round 1, #489 and #687; Rocket blog, "FP8 and
+Format (bloomery issue #565, §4, #489 and #687; Rocket blog, "FP8 and
 NVFP4 serving maps": ModelOpt block-16 packing): a value is
     x_hat = e2m1(code) * e4m3(block scale) * tensor_scale,
 one unsigned E4M3 scale per 16 consecutive elements of a row, one FP32 scale
