@@ -321,6 +321,18 @@ def time_prefill(pkg, synth, T, reps=3):
     return {"ms": round(ms, 3), "tokens_per_s": round(T / (ms * 1e-3))}
 
 
+def max_over_ranks(x: float, dist=None) -> float:
+    """The largest x over all ranks (every rank gets it); x itself without a
+    process group. NCCL reduces a device tensor, other backends a host one."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def fp4_peak():
     """Dense FP4 tensor peak: the measured BF16 GEMM burst x the nominal FP4 / BF16
     ratio (13.5 / 2.25 PFLOP/s dense)."""
@@ -517,10 +529,7 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ms = time_graph(g1, args.steps, args.warmup)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist)
     us_layer = ms * 1e3 / n_layers
     hbm_peak, peak_kind = peaks()
     gbs_step = step_bytes(1) / (us_layer * 1e-6) / 1e9
