@@ -429,6 +429,13 @@ def cpu_all_cores_leg(seconds_budget=10.0):
                       f"(one sequence each) in a {wall:.1f} s window; aggregate throughput"}
 
 
+def headline_config(world: int) -> dict:
+    """The workload of the headline line, identical in both arms."""
+    return {"workload": "gdn-decode-c1", "hidden": 2048, "k_heads": 16, "v_heads": 32, "d": 128, "conv": 4,
+            "batch": 1, "l2_defeat": "distinct layer instances, footprint > 4x L2",
+            "graph": "one CUDA graph per bucket over the stack", "parallelism": f"replicas x{world}"}
+
+
 def reference_arm(args):
     """--impl reference: the CPU oracle on the same workload and metric."""
     rank = int(os.environ.get("RANK", "0"))
@@ -456,7 +463,7 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "gdn-decode-c1 full width (H2048 Hk16 Hv32 d128 K4), 1 layer-step per step"},
+            "config": headline_config(args.gpus),
             "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} config-1 decode c1 layer-steps"},
             "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -624,11 +631,10 @@ def main():
         "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4-w4a4 (fp32 accum) + f32 state", "data": "synthetic",
-        "config": {"workload": "gdn-decode-c1", "hidden": 2048, "k_heads": 16, "v_heads": 32, "d": 128,
-                   "conv": 4, "batch": 1, "layers_per_step": n_layers,
-                   "l2_defeat": f"{n_layers} distinct layer instances, {n_layers * per_layer / 1e6:.0f} MB > 4x L2 "
-                                f"({l2 / 1e6:.0f} MB)", "graph": "one CUDA graph per bucket over the stack",
-                   "parallelism": f"replicas x{world}"},
+        "config": headline_config(world),
+        "stack": {"layers_per_step": n_layers,
+                  "l2_defeat": f"{n_layers} distinct layer instances, {n_layers * per_layer / 1e6:.0f} MB > 4x L2 "
+                               f"({l2 / 1e6:.0f} MB)"},
         "hbm_gbs_step": round(gbs_step, 1), "hbm_frac_step": round(gbs_step / hbm_peak, 4),
         "roofline": {"bound": "hbm", "kernel": "gemv_mma_kernel (one-row W4A4 q|k|v|z|b|a projection, warp-MMA block products)",
                      "achieved": round(gemv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",

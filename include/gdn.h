@@ -2,7 +2,8 @@
  * gdn.h -- C ABI of one NVFP4 W4A4 Gated DeltaNet (GDN) layer step on one GPU.
  *
  * The operation (Rocket blog, "A reduction barrier makes Qwen GDN graph replay
- * bit exact", setup table): one GDN linear-attention layer as it is served from
+ * bit exact", setup table; "the Rocket GDN entry" below): one GDN
+ * linear-attention layer as it is served from
  * an NVFP4 checkpoint -- W4A4 QKVZ/BA projections, a BF16 causal convolution,
  * an FP32 recurrent state updated by the gated delta rule (state laid out
  * [v][k], the "pretranspose" decode layout), a z-gated RMSNorm and a W4A4
@@ -104,7 +105,11 @@ typedef struct {
 typedef struct gdn_ctx gdn_ctx;
 
 /* Validate the config and weights, copy the weights into the kernels' layouts
- * and allocate the context's workspace on the current device. Synchronises
+ * and allocate the context's workspace on the current device. The pages define
+ * no such call (an interface choice of this library): it holds what the Rocket
+ * GDN entry's setup table fixes for a served layer -- the W4A4 NVFP4 QKVZ/BA
+ * and output projection weights, the BF16 causal-convolution taps and the
+ * gate parameters -- in the layouts the kernels stream. Synchronises
  * `stream` once (the only call that does besides gdn_check). On failure *out is
  * NULL and nothing stays allocated. Errors: GDN_E_NULL, GDN_E_SHAPE,
  * GDN_E_NONFINITE (eps/scales), GDN_E_BAD_SCALE (scale <= 0 or an E4M3 weight
@@ -112,7 +117,8 @@ typedef struct gdn_ctx gdn_ctx;
 gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream, gdn_ctx **out);
 
 /* Free everything the context owns. NULL is accepted. Synchronises the device
- * work of the context's own allocations (cudaFree). */
+ * work of the context's own allocations (cudaFree). No counterpart on the
+ * pages: an interface choice of this library, the inverse of gdn_create. */
 gdn_status gdn_destroy(gdn_ctx *ctx);
 
 /* NVFP4 quantisation of x[rows][cols] (bloomery issue #565, §4, #687:
@@ -129,7 +135,10 @@ gdn_status nvfp4_quantize(const void *x, int x_is_f32, int rows, int cols, float
                           uint8_t *codes, uint8_t *scales, int32_t *dev_status, void *stream);
 
 /* Block-scaled W4A4 product C[M][N] = sum_k A_hat[m][k] * B_hat[n][k], FP32
- * accumulation, written as BF16 (c_is_bf16 = 1, round to nearest even) or FP32.
+ * accumulation, written as BF16 (c_is_bf16 = 1, round to nearest even) or FP32
+ * (bloomery issue #565, §4, #687: W4A4 means both the 4-bit weights and the
+ * activations enter the product as NVFP4; the Rocket GDN entry's setup table
+ * runs the QKVZ/BA and output projections of the layer this way).
  * A is [M][K], B is [N][K], both NVFP4 (struct fields are device pointers,
  * the struct itself is host memory). K % 64 == 0, M, N >= 0 (0 is a no-op).
  * Errors: GDN_E_NULL, GDN_E_SHAPE, GDN_E_ALIGN, GDN_E_BAD_SCALE (tensor
@@ -137,7 +146,10 @@ gdn_status nvfp4_quantize(const void *x, int x_is_f32, int rows, int cols, float
 gdn_status nvfp4_gemm(const gdn_nvfp4 *A, int M, const gdn_nvfp4 *B, int N, int K,
                       void *C, int c_is_bf16, void *stream);
 
-/* One decode step of B sequences (c1..c16 buckets and larger batches).
+/* One decode step of B sequences (c1..c16 buckets and larger batches): the
+ * layer step of the Rocket GDN entry (setup table and decode table: W4A4 QKVZ/BA projections, a
+ * BF16 causal convolution, the FP32 recurrent state in the pretranspose [v][k]
+ * layout, the output projection; buckets c1, c2, c4, c8, c16).
  *   x:          BF16 [B][H]
  *   slot_ids:   int32 [B] (device), the state slot of each row; -1 marks a padding
  *               row, whose output row is written as zeros and which touches no state.
@@ -300,7 +312,13 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * streaming on GB300). 0 = automatic, the default: streaming from two output
  * tiles per SM, else one tile per CTA; 1 = one tile per CTA; 2 = streaming
  * whenever the form allows; 3 = weight-stationary whenever the form allows
- * (else as 2).
+ * (else as 2). knob 12: the budget, in SM cycles, of each grid-barrier wait of
+ * the persistent single-kernel step (knob 3): 0 = the default, 2^31 (about
+ * one second); any positive value sets it. A wait that runs out records
+ * GDN_E_TIMEOUT in the status word and the kernel finishes without it (that
+ * step's results are then meaningless); the barrier words are cleared before
+ * every launch, so the next call starts clean. A short budget exists to test
+ * that path: these waits guard no copy in flight.
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

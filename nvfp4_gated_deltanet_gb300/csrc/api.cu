@@ -62,6 +62,7 @@ struct Tuning {
   int scan_tc = 0;         // prefill chunk scan products on warp-level tensor cores: 0 auto (on), 1 off, 2 on
   int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto, 1 off, 2 streaming
                            // form whenever allowed, 3 weight-stationary form whenever allowed
+  long long barrier_wait = 0;  // grid-barrier wait budget in SM cycles (0 = kWaitCycles)
 };
 Tuning g_tune;
 
@@ -313,6 +314,7 @@ FusedArgs fused_args(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, i
   f.y_codes = ctx->y_codes;
   f.y_scales = ctx->y_scales;
   f.bar = ctx->grid_bar;
+  f.wait_cycles = g_tune.barrier_wait > 0 ? g_tune.barrier_wait : kWaitCycles;
   f.status = ctx->status;
   return f;
 }
@@ -361,6 +363,10 @@ gdn_status gdn_set_tuning(int knob, int value) {
     case 11:
       if (value < 0 || value > 3) return GDN_E_RANGE;
       g_tune.persist_gemm = value;
+      return GDN_OK;
+    case 12:
+      if (value < 0) return GDN_E_RANGE;
+      g_tune.barrier_wait = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;
@@ -594,7 +600,13 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   // ~2.5 us, more than a PDL kernel boundary), so it runs only on request.
   if (g_tune.fused == 2 && g_tune.decode_gemm != 2 && B <= 2 && !ctx->cfg.state_bf16) {
     FusedArgs f = fused_args(ctx, x, slot_ids, B, out, conv_state, static_cast<float *>(ssm_state), num_slots);
-    if (fused_plan(f, ctx->num_sms)) return cuda_status(launch_fused(f, lc));
+    if (fused_plan(f, ctx->num_sms)) {
+      // fresh barrier words for every launch: a launch whose barrier gave up
+      // leaves nothing behind for the next one
+      cudaError_t e = cudaMemsetAsync(ctx->grid_bar, 0, 16, lc.stream);
+      if (e != cudaSuccess) return cuda_status(e);
+      return cuda_status(launch_fused(f, lc));
+    }
   }
   cudaError_t e = run_in_proj(ctx, x, B, slot_ids, num_slots, lc, true);
   if (e != cudaSuccess) return cuda_status(e);

@@ -484,7 +484,8 @@ struct FusedArgs {
   float *ssm_state;
   uint16_t *proj;                 // scratch [B][Nin]
   uint8_t *y_codes, *y_scales;    // scratch [B][Vd/2], [B][Vd/16] row-major
-  unsigned int *bar;              // grid barrier words (2), zero before the first launch
+  unsigned int *bar;              // grid barrier words (2), zeroed before every launch
+  long long wait_cycles;          // budget of each grid-barrier wait, SM cycles
   int32_t *status;
   int rows_in, rows_out;          // weight rows per CTA (set by fused_plan)
 };

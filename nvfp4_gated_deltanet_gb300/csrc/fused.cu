@@ -31,10 +31,11 @@ constexpr int kThreadsF = 512;   // 16 warps
 constexpr int kDF = 128;         // head size of this kernel
 
 // Grid barrier over all CTAs of a cooperative launch: arrival counter + a
-// generation word, both in global memory (bar[0], bar[1]), reusable across
-// launches (the last arriver resets the counter before releasing). The wait
-// is bounded; on timeout the caller records GDN_E_TIMEOUT.
-GDN_DEV bool grid_barrier(unsigned int *bar, unsigned int nblocks) {
+// generation word, both in global memory (bar[0], bar[1]; the host zeroes them
+// before every launch), reusable within the launch (the last arriver resets
+// the counter before releasing). The wait is bounded by `budget` SM cycles;
+// a CTA that gives up records GDN_E_TIMEOUT at once and returns false.
+GDN_DEV bool grid_barrier(unsigned int *bar, unsigned int nblocks, long long budget, int32_t *status) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -50,7 +51,11 @@ GDN_DEV bool grid_barrier(unsigned int *bar, unsigned int nblocks) {
     } else {
       const long long t0 = clock64();
       while (*vgen == gen) {
-        if (clock64() - t0 > kWaitCycles) { ok = 0; break; }
+        if (clock64() - t0 > budget) {
+          ok = 0;
+          flag_status(status, GDN_E_TIMEOUT);
+          break;
+        }
         __nanosleep(20);
       }
       __threadfence();
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(FusedArgs a)
       }
     }
   }
-  if (!grid_barrier(a.bar, gridDim.x)) ok = false;
+  if (!grid_barrier(a.bar, gridDim.x, a.wait_cycles, a.status)) ok = false;
 
   // ---------------------------------------------------------------- phase B
   const int kh = uh / G;
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(kThreadsF, 1) decode_fused_kernel(FusedArgs a)
       a.y_scales[e0 >> 4] = uint8_t(s);
     }
   }
-  if (!grid_barrier(a.bar, gridDim.x)) ok = false;
+  if (!grid_barrier(a.bar, gridDim.x, a.wait_cycles, a.status)) ok = false;
 
   // ---------------------------------------------------------------- phase C
   if (ulive && uh % G == 0) {  // every reader of this key head's q/k conv state is done

@@ -106,8 +106,11 @@ def test_tuning_knob_ranges(L):
         for knob, values in valid.items():
             for v in range(-1, 10):
                 assert L.gdn_set_tuning(knob, v) == (0 if v in values else 6), (knob, v)
-        assert L.gdn_set_tuning(12, 0) == 6
+        for v in (0, 1, 1000, 2 ** 31 - 1):                    # knob 12: a wait budget in cycles
+            assert L.gdn_set_tuning(12, v) == 0, v
+        assert L.gdn_set_tuning(12, -1) == 6
+        assert L.gdn_set_tuning(13, 0) == 6
         assert L.gdn_set_tuning(-1, 0) == 6
     finally:
-        for knob in valid:
+        for knob in list(valid) + [12]:
             L.gdn_set_tuning(knob, 0)

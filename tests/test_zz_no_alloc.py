@@ -2,18 +2,19 @@
 device memory or keep a context -- gives the same results as gdn_decode_step.
 
 Both entry points are called through the C ABI on the same weights and the
-same inputs, two steps in a row, for one row (CUDA-core projections) and four
-rows (tensor-core projections). The static entry point keeps its
-intermediates in a fixed device array shared by all its calls, so the second
-call also checks that nothing left behind by the first one leaks into it.
-This file is collected last on purpose."""
+same inputs, two steps in a row, for one, two and four rows. The static entry
+point keeps its intermediates in a fixed device array shared by all its calls,
+so the second call also checks that nothing left behind by the first one leaks
+into it. The first step is also compared with the oracle, and the calls after
+the first must leave the device's allocated and free memory unchanged. This
+file is collected last on purpose."""
 import ctypes
 
 import numpy as np
 import pytest
 
 from conftest import rel_l2
-from helpers import slot_inputs, to_dev, to_host, weights
+from helpers import oracle_layer, slot_inputs, to_dev, to_host, weights
 from nvfp4_gated_deltanet_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -24,7 +25,7 @@ def _bf(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-@pytest.mark.parametrize("B", [1, 4])
+@pytest.mark.parametrize("B", [1, 2, 4])
 def test_static_step_matches_context_step(B):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
@@ -50,19 +51,31 @@ def test_static_step_matches_context_step(B):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     L = pkg.lib()
+    xs = [to_dev(x[step]) for step in range(2)]
+    outs = [torch.empty(B, sh.hidden, dtype=torch.int16, device="cuda") for _ in range(2)]
+    conv_o, ssm_o = conv0.copy(), ssm0.copy()     # the oracle's first step
+    want0 = oracle_layer("FULL", 1).decode_step(x[0], slots, conv_o, ssm_o)
+    mem = None
     for step in range(2):                          # two calls in a row
-        xd = to_dev(x[step])
-        want = layer.decode_step(xd, ids, conv_a, ssm_a)
-        got = torch.empty(B, sh.hidden, dtype=torch.int16, device="cuda")
-        st = L.gdn_decode_step_static(ctypes.byref(cfg), ctypes.byref(gw), xd.data_ptr(), ids.data_ptr(), B,
+        want = layer.decode_step(xs[step], ids, conv_a, ssm_a)
+        got = outs[step]
+        torch.cuda.synchronize()
+        before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        st = L.gdn_decode_step_static(ctypes.byref(cfg), ctypes.byref(gw), xs[step].data_ptr(), ids.data_ptr(), B,
                                       got.data_ptr(), conv_b.data_ptr(), ssm_b.data_ptr(), B, status.data_ptr(),
                                       stream)
         assert st == 0, pkg.STATUS_NAMES[st]
         torch.cuda.synchronize()
+        after = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
+        if step > 0:                               # the first call may set up the array's address
+            assert after == before, (before, after)
         assert int(status.item()) == 0
         assert rel_l2(_bf(to_host(got)), _bf(to_host(want))) <= 4e-3
         assert rel_l2(to_host(ssm_b), to_host(ssm_a)) <= 1e-4
         assert rel_l2(_bf(to_host(conv_b)), _bf(to_host(conv_a))) <= 4e-3
+        if step == 0:                              # against the oracle, on its own
+            assert rel_l2(_bf(to_host(got)), _bf(want0)) <= 4e-3
+            assert rel_l2(to_host(ssm_b), ssm_o) <= 1e-4
     assert layer.check() == 0
 
 
