@@ -319,6 +319,13 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * step's results are then meaningless); the barrier words are cleared before
  * every launch, so the next call starts clean. A short budget exists to test
  * that path: these waits guard no copy in flight.
+ * knob 13: decode of up to 8 rows (d_k = 128, Hv / Hk of 1 or 2, H <= 2048)
+ * as two kernels: the in-projection rows of each key head computed inside the
+ * cluster that mixes that head (conv, norms, gates, delta rule, gated norm,
+ * quantisation), then the warp-MMA out-projection, which lets the next kernel
+ * start at once (0 = automatic, the default: on where the shape allows and
+ * knob 0 is not 2; 1 = off; 2 = on where the shape allows). Bit-identical to
+ * the three-kernel step on the CUDA-core projections (knob 0 = 1).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

@@ -63,6 +63,8 @@ struct Tuning {
   int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto, 1 off, 2 streaming
                            // form whenever allowed, 3 weight-stationary form whenever allowed
   long long barrier_wait = 0;  // grid-barrier wait budget in SM cycles (0 = kWaitCycles)
+  int proj_mix = 0;        // decode of up to 8 rows with the in-projection inside the mixing kernel: 0 auto (on),
+                           // 1 off, 2 on
 };
 Tuning g_tune;
 
@@ -368,6 +370,10 @@ gdn_status gdn_set_tuning(int knob, int value) {
       if (value < 0) return GDN_E_RANGE;
       g_tune.barrier_wait = value;
       return GDN_OK;
+    case 13:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      g_tune.proj_mix = value;
+      return GDN_OK;
     default:
       return GDN_E_RANGE;
   }
@@ -607,6 +613,64 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
       if (e != cudaSuccess) return cuda_status(e);
       return cuda_status(launch_fused(f, lc));
     }
+  }
+  const gdn_config &c = ctx->cfg;
+  if (g_tune.proj_mix != 1 && g_tune.decode_gemm != 2 && ctx->w_in_mma && ctx->w_out_mma &&
+      proj_mix_ok(c.hidden, c.n_k_heads, c.n_v_heads, c.d_k, c.conv_kernel, B)) {
+    // projections + mixing as one cluster kernel, then the warp-MMA out-projection
+    PmArgs p{};
+    p.x = x;
+    p.slot_ids = slot_ids;
+    p.B = B;
+    p.num_slots = num_slots;
+    p.w_mma = ctx->w_in_mma;
+    p.w_codes = ctx->w_in_codes;
+    p.w_scales = ctx->w_in_scales;
+    p.ts_in = c.act_scale_in;
+    p.ts_qkvz = ctx->ts_qkvz;
+    p.ts_ba = ctx->ts_ba;
+    p.H = c.hidden;
+    p.Hk = c.n_k_heads;
+    p.Hv = c.n_v_heads;
+    p.Nqkvz = ctx->Nqkvz;
+    p.C = ctx->C;
+    p.Kc = c.conv_kernel;
+    p.conv_w = ctx->conv_w;
+    p.A_log = ctx->A_log;
+    p.dt_bias = ctx->dt_bias;
+    p.norm_w = ctx->norm_w;
+    p.l2_eps = c.l2_eps;
+    p.rms_eps = c.rms_eps;
+    p.ts_out = c.act_scale_out;
+    p.conv_state = conv_state;
+    p.ssm_state = ssm_state;
+    p.state_bf16 = c.state_bf16;
+    p.y_codes = ctx->y_codes;
+    p.y_scales = ctx->y_scales;
+    p.status = ctx->status;
+    cudaError_t e = launch_proj_mix(p, lc);
+    if (e != cudaSuccess) return cuda_status(e);
+    GemvArgs o{};
+    o.a_codes = ctx->y_codes;
+    o.a_scales = ctx->y_scales;
+    o.ts_a = c.act_scale_out;
+    o.w_codes = ctx->w_out_codes;
+    o.w_scales = ctx->w_out_scales;
+    o.ts_w0 = o.ts_w1 = ctx->ts_wout;
+    o.n_split = c.hidden;
+    o.c = out;
+    o.c_is_bf16 = 1;
+    o.ldc = c.hidden;
+    o.M = B;
+    o.N = c.hidden;
+    o.K = ctx->Vd;
+    o.status = ctx->status;
+    o.w_mma = ctx->w_out_mma;
+    // the step's last kernel lets the next one start at once: every kernel of
+    // this library that can follow reads only weights (and slot ids) before
+    // its own dependency wait
+    o.early_trigger = g_tune.early_trigger != 1;
+    return cuda_status(launch_gemv_mma(o, lc));
   }
   cudaError_t e = run_in_proj(ctx, x, B, slot_ids, num_slots, lc, true);
   if (e != cudaSuccess) return cuda_status(e);

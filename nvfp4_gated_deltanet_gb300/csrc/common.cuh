@@ -129,6 +129,60 @@ GDN_DEV bool quant_block16(const float (&v)[16], float ts, float inv6ts, uint32_
 
 GDN_DEV float inv6ts_of(float ts) { return __frcp_rn(__fmul_rn(6.0f, ts)); }
 
+// Warp-level m16n8k16 MMA, FP16 inputs, FP32 accumulation starting from zero:
+// d = A (16 x 16, row) * B (16 x 8, col). Lane (g = lane / 4, t = lane % 4)
+// holds d[0], d[1] = rows g, columns 2t, 2t+1 and d[2], d[3] = row g + 8.
+GDN_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Four E4M3 bytes -> four floats (exact).
+GDN_DEV void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
+  uint32_t lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+  f[0] = __half2float(__ushort_as_half(uint16_t(lo & 0xFFFFu)));
+  f[1] = __half2float(__ushort_as_half(uint16_t(lo >> 16)));
+  f[2] = __half2float(__ushort_as_half(uint16_t(hi & 0xFFFFu)));
+  f[3] = __half2float(__ushort_as_half(uint16_t(hi >> 16)));
+}
+
+// One NVFP4 block (codes lo/hi, scale byte) as x_hat = e2m1 * e4m3 in FP16,
+// exact (|x_hat| <= 6 * 448 and >= 2^-10), written as 16 halves.
+GDN_DEV void store_xhat_block(__half *dst, uint32_t lo, uint32_t hi, uint32_t s) {
+  __half2 h[8];
+  e2m1x8_to_h2x4(lo, *reinterpret_cast<__half2(*)[4]>(&h[0]));
+  e2m1x8_to_h2x4(hi, *reinterpret_cast<__half2(*)[4]>(&h[4]));
+  const __half2 sc = __float2half2_rn(e4m3_to_f32(s));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = __hmul2(h[i], sc);
+  reinterpret_cast<uint4 *>(dst)[0] = *reinterpret_cast<const uint4 *>(&h[0]);
+  reinterpret_cast<uint4 *>(dst)[1] = *reinterpret_cast<const uint4 *>(&h[4]);
+}
+
+// 16 BF16 values (two 16-byte loads) -> FP32.
+GDN_DEV void load_bf16x16(const uint16_t *p, float (&v)[16]) {
+  const uint4 *q = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 w4 = q[i];
+    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
+      v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+}
+
 // Tiled scale layout read by tcgen05.cp .32x128b.warpx4 for one operand of the
 // block-scaled MMA: the scales of 128 rows x one 64-wide K step form a 512-byte
 // atom, row r at byte (r % 32) * 16 + ((r % 128) / 32) * 4 + k-block; atoms are
@@ -362,6 +416,28 @@ struct MixArgs {
   size_t ssm_row_stride, conv_row_stride;
 };
 cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc);
+
+// In-projection + token mixing of a decode step in one cluster kernel
+// (proj_mix.cu), B <= 8 rows; y goes out NVFP4 with row-major scales.
+struct PmArgs {
+  const uint16_t *x;                  // [B][H] BF16
+  const int32_t *slot_ids;            // [B]
+  int B, num_slots;
+  const uint8_t *w_mma;               // [qkvz; ba] in the warp-MMA group layout (launch_mma_tiles)
+  const uint8_t *w_codes, *w_scales;  // [qkvz; ba] row-major (the b and a rows are read from here)
+  float ts_in, ts_qkvz, ts_ba;
+  int H, Hk, Hv, Nqkvz, C, Kc;
+  const uint16_t *conv_w;
+  const float *A_log, *dt_bias, *norm_w;
+  float l2_eps, rms_eps, ts_out;
+  uint16_t *conv_state;               // [S][K-1][C]
+  void *ssm_state;                    // [S][Hv][dv][dk], FP32 or BF16 bits
+  int state_bf16;
+  uint8_t *y_codes, *y_scales;        // [B][Hv*dv/2], [B][Hv*dv/16]
+  int32_t *status;
+};
+bool proj_mix_ok(int H, int Hk, int Hv, int D, int Kc, int B);
+cudaError_t launch_proj_mix(const PmArgs &a, const LaunchCtx &lc);
 
 // Large-batch token mixing split in three kernels (batch.cu), bit-identical
 // to launch_mix; the workspace holds the per-row intermediates.

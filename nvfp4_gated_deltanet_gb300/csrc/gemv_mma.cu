@@ -27,44 +27,22 @@ namespace {
 
 constexpr int kMmaWarps = 8;  // 2 row groups x 4 K quarters per CTA
 
-GDN_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%10, %10, %10, %10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
-}
-
-// Four E4M3 bytes -> four floats (exact).
-GDN_DEV void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
-  uint32_t lo, hi;
-  asm("{\n\t.reg .b16 l, h;\n\t"
-      "mov.b32 {l, h}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
-  f[0] = __half2float(__ushort_as_half(uint16_t(lo & 0xFFFFu)));
-  f[1] = __half2float(__ushort_as_half(uint16_t(lo >> 16)));
-  f[2] = __half2float(__ushort_as_half(uint16_t(hi & 0xFFFFu)));
-  f[3] = __half2float(__ushort_as_half(uint16_t(hi >> 16)));
-}
-
 __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   if (a.early_trigger) pdl_launch_dependents();
   const int K = a.K, nkb4 = K >> 6, qkb4 = nkb4 >> 2;  // 64-K steps: all, per quarter
+  const int M = a.M;                                    // activation rows = MMA columns, 1..8
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rgl = warp >> 2, q = warp & 3;                // row group in CTA, K quarter
   const int rg = blockIdx.x * 2 + rgl;
   const int ngroups = (a.N + 15) >> 4;
   const size_t group_bytes = (size_t)nkb4 * 576;
   const uint32_t cbytes = (uint32_t)qkb4 * 512, sbytes = (uint32_t)qkb4 * 64;
-  // smem: [barriers 8 x 8][per warp: codes cbytes | scales sbytes][x_hat K halves][partials 2 x 4 x 16 floats]
+  // smem: [barriers 8 x 8][per warp: codes cbytes | scales sbytes][x_hat M x K halves][partials 2 x 4 x 16 x M floats]
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
   unsigned char *mine = smem + 64 + (size_t)warp * (cbytes + sbytes);
   __half *xh = reinterpret_cast<__half *>(smem + 64 + (size_t)kMmaWarps * (cbytes + sbytes));
-  float *part = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(xh) + (size_t)K * 2);
+  float *part = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(xh) + (size_t)M * K * 2);
   const bool have = rg < ngroups;
 
   if (lane == 0 && have) {  // this warp's quarter of its row group: codes, then scales
@@ -77,59 +55,42 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
   }
   __syncwarp();
 
-  pdl_wait();  // the activation row comes from the preceding kernel
+  pdl_wait();  // the activation rows come from the preceding kernel
 
   // ---- prologue: x_hat = e2m1(code) * e4m3(scale) in FP16, block by block
   {
     const int nblk = K >> 4;
     const float inv6ts = inv6ts_of(a.ts_a);
-    bool live = a.M > 0;
-    if (live && a.row_slot) {
-      const int slot = a.row_slot[0];
-      live = slot >= 0 && slot < a.num_slots;
-    }
-    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+    for (int jm = threadIdx.x; jm < M * nblk; jm += blockDim.x) {
+      const int m = jm / nblk, j = jm - m * nblk;
+      bool live = true;
+      if (a.row_slot) {
+        const int slot = a.row_slot[m];
+        live = slot >= 0 && slot < a.num_slots;
+      }
       uint32_t lo = 0, hi = 0, s = 0;
       if (live) {
         if (a.a_bf16) {
-          const uint4 *p = reinterpret_cast<const uint4 *>(a.a_bf16 + (size_t)j * 16);
           float v[16];
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const uint4 w4 = p[i];
-            const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
-              v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-            }
-          }
+          load_bf16x16(a.a_bf16 + (size_t)m * K + (size_t)j * 16, v);
           if (!quant_block16(v, a.ts_a, inv6ts, lo, hi, s) && blockIdx.x == 0)
             flag_status(a.status, GDN_E_NONFINITE);
         } else {
-          const uint2 c = *reinterpret_cast<const uint2 *>(a.a_codes + (size_t)j * 8);
+          const uint2 c = *reinterpret_cast<const uint2 *>(a.a_codes + (size_t)m * (K >> 1) + (size_t)j * 8);
           lo = c.x;
           hi = c.y;
-          s = a.a_scales[j];
+          s = a.a_scales[(size_t)m * nblk + j];
         }
       }
-      __half2 h[8];
-      e2m1x8_to_h2x4(lo, *reinterpret_cast<__half2(*)[4]>(&h[0]));
-      e2m1x8_to_h2x4(hi, *reinterpret_cast<__half2(*)[4]>(&h[4]));
-      const __half2 sc = __float2half2_rn(e4m3_to_f32(s));  // exact: an E4M3 value
-#pragma unroll
-      for (int i = 0; i < 8; ++i) h[i] = __hmul2(h[i], sc);  // exact: see above
-      uint4 *dst = reinterpret_cast<uint4 *>(xh + (size_t)j * 16);
-      dst[0] = *reinterpret_cast<const uint4 *>(&h[0]);
-      dst[1] = *reinterpret_cast<const uint4 *>(&h[4]);
+      store_xhat_block(xh + (size_t)m * K + (size_t)j * 16, lo, hi, s);
     }
   }
   __syncthreads();
   if (!a.early_trigger) pdl_launch_dependents();
 
-  // ---- the quarter's block dot products
+  // ---- the quarter's block dot products: rows g, g+8 of the group x columns 2t, 2t+1
   const int g = lane >> 2, t = lane & 3;
-  float acc0 = 0.0f, acc1 = 0.0f;  // rows g and g+8 (column 0 lives in lanes t == 0)
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   bool ok = true;
   if (have) {
     if (!mbar_wait(bars + warp, 0)) {
@@ -137,6 +98,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
     } else {
       const uint4 *codes = reinterpret_cast<const uint4 *>(mine);
       const uint32_t *scl = reinterpret_cast<const uint32_t *>(mine + cbytes);
+      const __half *xrow = xh + (size_t)(g < M ? g : 0) * K + 4 * t;  // column g = activation row g
       for (int s = 0; s < qkb4; ++s) {
         const uint4 c4 = codes[s * 32 + lane];
         float swg[4], swg8[4];
@@ -151,35 +113,46 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
           const uint32_t af[4] = {*reinterpret_cast<uint32_t *>(&hv[0]), *reinterpret_cast<uint32_t *>(&hv[2]),
                                   *reinterpret_cast<uint32_t *>(&hv[1]), *reinterpret_cast<uint32_t *>(&hv[3])};
           uint32_t b0 = 0, b1 = 0;
-          if (g == 0) {  // column 0 = the activation row; columns 1..7 are zero
-            const uint2 xv = *reinterpret_cast<const uint2 *>(xh + (size_t)(kb0 + j) * 16 + 4 * t);
+          if (g < M) {  // columns M..7 are zero
+            const uint2 xv = *reinterpret_cast<const uint2 *>(xrow + (size_t)(kb0 + j) * 16);
             b0 = xv.x;
             b1 = xv.y;
           }
           float d[4];
           mma16816(d, af, b0, b1);
-          acc0 = fmaf(d[0], swg[j], acc0);
-          acc1 = fmaf(d[2], swg8[j], acc1);
+          acc[0] = fmaf(d[0], swg[j], acc[0]);
+          acc[1] = fmaf(d[1], swg[j], acc[1]);
+          acc[2] = fmaf(d[2], swg8[j], acc[2]);
+          acc[3] = fmaf(d[3], swg8[j], acc[3]);
         }
       }
     }
   }
-  if (t == 0) {
-    part[(rgl * 4 + q) * 16 + g] = acc0;
-    part[(rgl * 4 + q) * 16 + g + 8] = acc1;
+  {
+    float *pq = part + (size_t)(rgl * 4 + q) * 16 * M;  // [16 rows][M columns]
+    const int c0 = 2 * t, c1 = 2 * t + 1;
+    if (c0 < M) {
+      pq[g * M + c0] = acc[0];
+      pq[(g + 8) * M + c0] = acc[2];
+    }
+    if (c1 < M) {
+      pq[g * M + c1] = acc[1];
+      pq[(g + 8) * M + c1] = acc[3];
+    }
   }
   __syncthreads();
-  if (threadIdx.x < 32) {  // 2 groups x 16 rows: quarters added in order
-    const int gl = threadIdx.x >> 4, r = threadIdx.x & 15;
+  for (int i = threadIdx.x; i < 32 * M; i += blockDim.x) {  // 2 groups x 16 rows x M: quarters added in order
+    const int m = i % M, rr = i / M, gl = rr >> 4, r = rr & 15;
     const int n = (blockIdx.x * 2 + gl) * 16 + r;
     if (n < a.N) {
-      const float sum = ((part[(gl * 4 + 0) * 16 + r] + part[(gl * 4 + 1) * 16 + r]) + part[(gl * 4 + 2) * 16 + r]) +
-                        part[(gl * 4 + 3) * 16 + r];
+      const float *p0 = part + (size_t)(gl * 4) * 16 * M + r * M + m;
+      const size_t qs = (size_t)16 * M;
+      const float sum = ((p0[0] + p0[qs]) + p0[2 * qs]) + p0[3 * qs];
       const float y = sum * (a.ts_a * (n < a.n_split ? a.ts_w0 : a.ts_w1));
       if (a.c_is_bf16)
-        static_cast<uint16_t *>(a.c)[n] = f32_to_bf16_bits(y);
+        static_cast<uint16_t *>(a.c)[(size_t)m * a.ldc + n] = f32_to_bf16_bits(y);
       else
-        static_cast<float *>(a.c)[n] = y;
+        static_cast<float *>(a.c)[(size_t)m * a.ldc + n] = y;
     }
   }
   if (!ok && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
@@ -222,12 +195,12 @@ cudaError_t launch_mma_tiles(const uint8_t *codes, const uint8_t *scales, int ro
   return cudaGetLastError();
 }
 
-bool gemv_mma_ok(const GemvArgs &a) { return a.w_mma && a.M == 1 && a.K % 256 == 0 && a.K <= 8192; }
+bool gemv_mma_ok(const GemvArgs &a) { return a.w_mma && a.M >= 1 && a.M <= 8 && a.K % 256 == 0 && a.K <= 8192; }
 
 cudaError_t launch_gemv_mma(const GemvArgs &a, const LaunchCtx &lc) {
   const int ngroups = (a.N + 15) / 16;
   const size_t per_warp = (size_t)(a.K / 256) * 576;
-  const size_t smem = 64 + kMmaWarps * per_warp + (size_t)a.K * 2 + 2 * 4 * 16 * 4;
+  const size_t smem = 64 + kMmaWarps * per_warp + (size_t)a.M * a.K * 2 + 2 * 4 * 16 * 4 * (size_t)a.M;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);

@@ -64,6 +64,7 @@ def _case(B):
     return w, codecs.f32_to_bf16(qkvz), codecs.f32_to_bf16(ba), conv, ssm, onehot
 
 
+@pytest.mark.filterwarnings("ignore:overflow encountered in exp")   # the oracle's sigmoid(-1e4) = 0
 @pytest.mark.parametrize("B", [1, 3])
 def test_gate_extremes_match_oracle_and_closed_forms(api, B):
     from oracle import codecs, gdn
