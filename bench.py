@@ -436,6 +436,101 @@ def headline_config(world: int) -> dict:
             "graph": "one CUDA graph per bucket over the stack", "parallelism": f"replicas x{world}"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model string (x86 'model name', else lscpu's 'Model name')."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+_CPU_SINGLE = r"""
+import json, sys, time
+sys.path.insert(0, %r)
+import numpy as np
+from nvfp4_gated_deltanet_gb300 import synth
+from oracle import gdn
+sh = synth.FULL
+w = synth.layer_weights(sh, 1)
+L = gdn.Layer(w)
+res = {}
+def decode(B, steps):
+    x = np.stack([synth.x_tokens(sh, synth.slot_seed(s), steps) for s in range(B)], axis=1)
+    c = np.stack([synth.conv_state(sh, synth.slot_seed(s)) for s in range(B)])
+    m = np.stack([synth.ssm_state(sh, synth.slot_seed(s)) for s in range(B)])
+    t = time.perf_counter()
+    for i in range(steps):
+        L.decode_step(x[i], list(range(B)), c, m)
+    return (time.perf_counter() - t) / steps
+for B, steps in ((1, 3), (2, 1), (4, 1), (8, 1), (16, 1), (64, 1)):
+    res["c%%d" %% B if B <= 16 else "batch%%d" %% B] = {"value": decode(B, steps) * 1e6, "unit": "us/step",
+                                                     "sample": "%%d step(s)" %% steps}
+T = 64
+x = synth.x_tokens(sh, 7, T)
+c, m = synth.conv_state(sh, 7, True), synth.ssm_state(sh, 7, True)
+t = time.perf_counter()
+L.prefill(x, c, m, init_zero=True)
+el = time.perf_counter() - t
+res["prefill"] = {"value": T / el, "unit": "tokens/s", "sample": "the first %%d tokens of the 1024-token prompt "
+                  "(token-by-token recurrence: the cost per token does not depend on T)" %% T}
+print(json.dumps(res))
+"""
+
+
+def cpu_configs_leg():
+    """The oracle on the host cores for every configuration: single-threaded
+    (one process, BLAS pinned to one thread) on a few steps of each decode
+    bucket and batch 64 and on a prefill sample; on all cores (oracle.parallel:
+    worker processes over rows or key-head groups, bit-identical to the
+    single-thread oracle) on one step of c16 and batch 64/128/256 and on whole
+    prefills of 1024/4096/16384 tokens. Workers are warmed (weights built)
+    before anything is timed."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", _CPU_SINGLE % ROOT], capture_output=True, text=True, env=env,
+                       timeout=900)
+    single = json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else {"error": r.stderr[-300:]}
+    import numpy as np
+    from nvfp4_gated_deltanet_gb300 import synth
+    from oracle import parallel
+    sh = synth.FULL
+    w = synth.layer_weights(sh, 1)
+    pool, n = parallel.make_pool(w)
+    allc = {}
+    try:
+        x1 = synth.x_tokens(sh, 7, 64)
+        parallel.prefill(w, x1, synth.conv_state(sh, 7, True), synth.ssm_state(sh, 7, True), True, n, pool)
+        for B in (16, 64, 128, 256):
+            x = np.stack([synth.x_tokens(sh, synth.slot_seed(s), 1)[0] for s in range(B)])
+            c = np.stack([synth.conv_state(sh, synth.slot_seed(s)) for s in range(B)])
+            m = np.stack([synth.ssm_state(sh, synth.slot_seed(s)) for s in range(B)])
+            t = time.perf_counter()
+            parallel.decode_step(w, x, list(range(B)), c, m, n, pool)
+            allc["c16" if B == 16 else f"batch{B}"] = {"value": (time.perf_counter() - t) * 1e6, "unit": "us/step",
+                                                      "sample": "1 step"}
+        for T in (1024, 4096, 16384):
+            x = synth.x_tokens(sh, 7, T)
+            t = time.perf_counter()
+            parallel.prefill(w, x, synth.conv_state(sh, 7, True), synth.ssm_state(sh, 7, True), True, n, pool)
+            allc[f"prefill{T}"] = {"value": T / (time.perf_counter() - t), "unit": "tokens/s",
+                                   "sample": f"the whole {T}-token prompt"}
+    finally:
+        pool.close()
+        pool.join()
+    return {"single_thread": single, "all_cores": allc, "cores_all": n, "cpu_model": cpu_model(),
+            "nproc": os.cpu_count()}
+
+
 def reference_arm(args):
     """--impl reference: the CPU oracle on the same workload and metric."""
     rank = int(os.environ.get("RANK", "0"))
@@ -482,6 +577,16 @@ def single_case(args):
     if args.case == "prefill":
         r = time_prefill(pkg, synth, args.T, reps=args.steps)
         line = {"case": f"prefill{args.T}", **r}
+    elif args.case == "bucket":
+        l2 = torch.cuda.get_device_properties(0).L2_cache_size
+        B = args.batch
+        n_layers = args.layers or max(4, -(-4 * l2 // step_bytes(B)) + 1)
+        _, layers, states, xd = make_stack(pkg, synth, n_layers, B, max(16, B))
+        g, _ = capture_stack(layers, states, xd, B)
+        us = time_graph(g, args.steps, args.warmup) * 1e3 / n_layers
+        gbs = step_bytes(B) / (us * 1e-6) / 1e9
+        line = {"case": f"c{B}", "us_per_layer_step": round(us, 3), "hbm_gbs": round(gbs, 1),
+                "frac_of_peak": round(gbs / hbm_peak, 4), "layers": n_layers}
     else:
         r = time_batch(pkg, synth, args.batch, hbm_peak, steps=args.steps)
         line = {"case": f"batch{args.batch}", **r}
@@ -498,9 +603,9 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="layer instances in the stack (0: > 4x L2)")
     ap.add_argument("--no-extra", action="store_true", help="skip the c2..c16 / batch / prefill extras")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
-    ap.add_argument("--case", default="decode", choices=["decode", "prefill", "batch"],
-                    help="decode: the headline (default); prefill / batch: only that workload, one JSON line "
-                         "(for profiling)")
+    ap.add_argument("--case", default="decode", choices=["decode", "prefill", "batch", "bucket"],
+                    help="decode: the headline (default); prefill / batch / bucket (a decode stack at --batch "
+                         "rows): only that workload, one JSON line (for profiling)")
     ap.add_argument("--T", type=int, default=4096, help="prompt length for --case prefill")
     ap.add_argument("--batch", type=int, default=256, help="rows for --case batch")
     args = ap.parse_args()
@@ -627,6 +732,7 @@ def main():
     cpu = None if (args.no_cpu or rank != 0) else cpu_baseline_leg()
     if cpu is not None:
         cpu["all_cores"] = cpu_all_cores_leg()
+        cpu["configs"] = cpu_configs_leg()
     line = {
         "metric": METRIC, "value": round(us_layer, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": False, "scaling": "weak",

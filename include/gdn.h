@@ -190,6 +190,26 @@ gdn_status gdn_mix_step(gdn_ctx *ctx, const uint16_t *qkvz, const uint16_t *ba,
                         const int32_t *slot_ids, int B, float *y, uint16_t *conv_state,
                         void *ssm_state, int num_slots, void *stream);
 
+/* The in-projection and token-mixing stages of gdn_decode_step as the one
+ * kernel that step runs for up to 8 rows (tuning knob 13), for stage-wise
+ * checks and timing: x BF16 [B][H] -> y, the gated-norm output as NVFP4 with
+ * tensor scale act_scale_out: codes [B][Hv*d_v/2] and row-major scales
+ * [B][Hv*d_v/16] (zeros for padding rows); conv_state and ssm_state as in
+ * gdn_decode_step, updated in place. Not launched early: it starts after the
+ * preceding work in the stream has finished. Errors: as gdn_decode_step,
+ * GDN_E_SHAPE when B > 8 or the shape is outside what the kernel covers
+ * (d_k = 128, Hv / Hk of 1 or 2, H a multiple of 256 up to 2048). */
+gdn_status gdn_in_mix(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint8_t *y_codes,
+                      uint8_t *y_scales, uint16_t *conv_state, void *ssm_state, int num_slots, void *stream);
+
+/* The out-projection stage alone on the warp-MMA kernel gdn_decode_step runs
+ * for up to 8 rows: y NVFP4 (codes [B][Hv*d_v/2], row-major scales
+ * [B][Hv*d_v/16], tensor scale act_scale_out) -> out BF16 [B][H]. Errors:
+ * GDN_E_NULL, GDN_E_ALIGN, GDN_E_SHAPE (B outside 1..8, or Hv*d_v not a
+ * multiple of 256), GDN_E_CUDA. */
+gdn_status gdn_out_proj(gdn_ctx *ctx, const uint8_t *y_codes, const uint8_t *y_scales, int B, uint16_t *out,
+                        void *stream);
+
 /* Prefill of T tokens of one sequence held in slot `slot` (host int): the same
  * arithmetic as T successive decode steps of that sequence (bloomery issue #565,
  * §4, #812: the delta rule of a prompt runs on tensor cores in chunks).

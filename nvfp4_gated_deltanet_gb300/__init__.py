@@ -50,6 +50,8 @@ SIGNATURES = {
     "gdn_verify_commit": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _vp]),
     "kda_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "gdn_in_proj": (_i, [_vp, _vp, _vp, _i, _vp, _vp]),
+    "gdn_in_mix": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp]),
+    "gdn_out_proj": (_i, [_vp, _vp, _vp, _i, _vp, _vp]),
     "gdn_check": (_i, [_vp, _i, _vp]),
     "gdn_set_tuning": (_i, [_i, _i]),
     "gdn_decode_step_static": (_i, [ctypes.POINTER(GdnConfig), ctypes.POINTER(GdnWeights), _vp, _vp, _i, _vp, _vp,

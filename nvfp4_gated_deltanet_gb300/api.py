@@ -151,6 +151,31 @@ class GatedDeltaNetLayer:
         _check(st, "gdn_in_proj")
         return out
 
+    def in_mix(self, x, slot_ids, conv_state, ssm_state, y_codes=None, y_scales=None, stream=None):
+        """In-projection + mixing of B <= 8 rows as one kernel: x [B][H] -> y as
+        NVFP4 (codes uint8 [B][Hv*D/2], row-major scales uint8 [B][Hv*D/16])."""
+        B = x.shape[0]
+        vd = self.Hv * self.D
+        if y_codes is None:
+            y_codes = torch.empty(B, vd // 2, dtype=torch.uint8, device=x.device)
+        if y_scales is None:
+            y_scales = torch.empty(B, vd // 16, dtype=torch.uint8, device=x.device)
+        st = lib().gdn_in_mix(self._ctx, _ptr(_dev(x)), _ptr(_dev(slot_ids)), B, _ptr(_dev(y_codes)),
+                              _ptr(_dev(y_scales)), _ptr(_dev(conv_state)), _ptr(self._state(ssm_state)),
+                              conv_state.shape[0], _stream(stream))
+        _check(st, "gdn_in_mix")
+        return y_codes, y_scales
+
+    def out_proj(self, y_codes, y_scales, out=None, stream=None):
+        """The out-projection of B <= 8 NVFP4 rows -> out [B][H] BF16 bits."""
+        B = y_codes.shape[0]
+        if out is None:
+            out = torch.empty(B, self.H, dtype=torch.int16, device=y_codes.device)
+        st = lib().gdn_out_proj(self._ctx, _ptr(_dev(y_codes)), _ptr(_dev(y_scales)), B, _ptr(_dev(out)),
+                                _stream(stream))
+        _check(st, "gdn_out_proj")
+        return out
+
     def new_snapshots(self, B: int, r: int, device="cuda"):
         """Snapshot buffers of a verify pass: conv [B][r][K-1][C] BF16 bits and
         recurrent [B][r][Hv][dv][dk] in the layer's state type."""

@@ -277,6 +277,72 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
   return run_gemv(o, lc, rows);
 }
 
+// The fused in-projection + mixing kernel's arguments (y row-major NVFP4).
+PmArgs pm_args(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *conv_state, void *ssm_state,
+               int num_slots, uint8_t *y_codes, uint8_t *y_scales) {
+  const gdn_config &c = ctx->cfg;
+  PmArgs p{};
+  p.x = x;
+  p.slot_ids = slot_ids;
+  p.B = B;
+  p.num_slots = num_slots;
+  p.w_mma = ctx->w_in_mma;
+  p.w_codes = ctx->w_in_codes;
+  p.w_scales = ctx->w_in_scales;
+  p.ts_in = c.act_scale_in;
+  p.ts_qkvz = ctx->ts_qkvz;
+  p.ts_ba = ctx->ts_ba;
+  p.H = c.hidden;
+  p.Hk = c.n_k_heads;
+  p.Hv = c.n_v_heads;
+  p.Nqkvz = ctx->Nqkvz;
+  p.C = ctx->C;
+  p.Kc = c.conv_kernel;
+  p.conv_w = ctx->conv_w;
+  p.A_log = ctx->A_log;
+  p.dt_bias = ctx->dt_bias;
+  p.norm_w = ctx->norm_w;
+  p.l2_eps = c.l2_eps;
+  p.rms_eps = c.rms_eps;
+  p.ts_out = c.act_scale_out;
+  p.conv_state = conv_state;
+  p.ssm_state = ssm_state;
+  p.state_bf16 = c.state_bf16;
+  p.y_codes = y_codes;
+  p.y_scales = y_scales;
+  p.status = ctx->status;
+  return p;
+}
+
+// The warp-MMA out-projection of B <= 8 NVFP4 rows (row-major scales).
+GemvArgs out_gemv_args(gdn_ctx *ctx, const uint8_t *y_codes, const uint8_t *y_scales, int B, uint16_t *out,
+                       bool early) {
+  const gdn_config &c = ctx->cfg;
+  GemvArgs o{};
+  o.a_codes = y_codes;
+  o.a_scales = y_scales;
+  o.ts_a = c.act_scale_out;
+  o.w_codes = ctx->w_out_codes;
+  o.w_scales = ctx->w_out_scales;
+  o.ts_w0 = o.ts_w1 = ctx->ts_wout;
+  o.n_split = c.hidden;
+  o.c = out;
+  o.c_is_bf16 = 1;
+  o.ldc = c.hidden;
+  o.M = B;
+  o.N = c.hidden;
+  o.K = ctx->Vd;
+  o.status = ctx->status;
+  o.w_mma = ctx->w_out_mma;
+  o.early_trigger = early ? 1 : 0;
+  return o;
+}
+
+bool pm_path(const gdn_ctx *ctx, int B) {
+  const gdn_config &c = ctx->cfg;
+  return ctx->w_in_mma && ctx->w_out_mma && proj_mix_ok(c.hidden, c.n_k_heads, c.n_v_heads, c.d_k, c.conv_kernel, B);
+}
+
 FusedArgs fused_args(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint16_t *out,
                      uint16_t *conv_state, float *ssm_state, int num_slots) {
   const gdn_config &c = ctx->cfg;
@@ -614,63 +680,16 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
       return cuda_status(launch_fused(f, lc));
     }
   }
-  const gdn_config &c = ctx->cfg;
-  if (g_tune.proj_mix != 1 && g_tune.decode_gemm != 2 && ctx->w_in_mma && ctx->w_out_mma &&
-      proj_mix_ok(c.hidden, c.n_k_heads, c.n_v_heads, c.d_k, c.conv_kernel, B)) {
+  if (g_tune.proj_mix != 1 && g_tune.decode_gemm != 2 && pm_path(ctx, B)) {
     // projections + mixing as one cluster kernel, then the warp-MMA out-projection
-    PmArgs p{};
-    p.x = x;
-    p.slot_ids = slot_ids;
-    p.B = B;
-    p.num_slots = num_slots;
-    p.w_mma = ctx->w_in_mma;
-    p.w_codes = ctx->w_in_codes;
-    p.w_scales = ctx->w_in_scales;
-    p.ts_in = c.act_scale_in;
-    p.ts_qkvz = ctx->ts_qkvz;
-    p.ts_ba = ctx->ts_ba;
-    p.H = c.hidden;
-    p.Hk = c.n_k_heads;
-    p.Hv = c.n_v_heads;
-    p.Nqkvz = ctx->Nqkvz;
-    p.C = ctx->C;
-    p.Kc = c.conv_kernel;
-    p.conv_w = ctx->conv_w;
-    p.A_log = ctx->A_log;
-    p.dt_bias = ctx->dt_bias;
-    p.norm_w = ctx->norm_w;
-    p.l2_eps = c.l2_eps;
-    p.rms_eps = c.rms_eps;
-    p.ts_out = c.act_scale_out;
-    p.conv_state = conv_state;
-    p.ssm_state = ssm_state;
-    p.state_bf16 = c.state_bf16;
-    p.y_codes = ctx->y_codes;
-    p.y_scales = ctx->y_scales;
-    p.status = ctx->status;
-    cudaError_t e = launch_proj_mix(p, lc);
+    cudaError_t e = launch_proj_mix(pm_args(ctx, x, slot_ids, B, conv_state, ssm_state, num_slots, ctx->y_codes,
+                                            ctx->y_scales), lc);
     if (e != cudaSuccess) return cuda_status(e);
-    GemvArgs o{};
-    o.a_codes = ctx->y_codes;
-    o.a_scales = ctx->y_scales;
-    o.ts_a = c.act_scale_out;
-    o.w_codes = ctx->w_out_codes;
-    o.w_scales = ctx->w_out_scales;
-    o.ts_w0 = o.ts_w1 = ctx->ts_wout;
-    o.n_split = c.hidden;
-    o.c = out;
-    o.c_is_bf16 = 1;
-    o.ldc = c.hidden;
-    o.M = B;
-    o.N = c.hidden;
-    o.K = ctx->Vd;
-    o.status = ctx->status;
-    o.w_mma = ctx->w_out_mma;
     // the step's last kernel lets the next one start at once: every kernel of
     // this library that can follow reads only weights (and slot ids) before
     // its own dependency wait
-    o.early_trigger = g_tune.early_trigger != 1;
-    return cuda_status(launch_gemv_mma(o, lc));
+    return cuda_status(launch_gemv_mma(out_gemv_args(ctx, ctx->y_codes, ctx->y_scales, B, out,
+                                                     g_tune.early_trigger != 1), lc));
   }
   cudaError_t e = run_in_proj(ctx, x, B, slot_ids, num_slots, lc, true);
   if (e != cudaSuccess) return cuda_status(e);
@@ -886,6 +905,29 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   e = launch_prefill_mix(p, ctx->conv_tmp, lc);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(run_out_proj(ctx, out, T, lc, true));
+}
+
+gdn_status gdn_in_mix(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_ids, int B, uint8_t *y_codes,
+                      uint8_t *y_scales, uint16_t *conv_state, void *ssm_state, int num_slots, void *stream) {
+  gdn_status st = check_state_args(ctx, x, y_codes, conv_state, ssm_state, num_slots);
+  if (st != GDN_OK) return st;
+  if (!slot_ids || !y_scales) return GDN_E_NULL;
+  if (!aligned16(slot_ids) || !aligned16(y_scales)) return GDN_E_ALIGN;
+  if (B < 1 || B > ctx->cfg.max_batch || !pm_path(ctx, B)) return GDN_E_SHAPE;
+  // no programmatic launch: the state must not be read before a preceding
+  // kernel that writes it has finished
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, false};
+  return cuda_status(
+      launch_proj_mix(pm_args(ctx, x, slot_ids, B, conv_state, ssm_state, num_slots, y_codes, y_scales), lc));
+}
+
+gdn_status gdn_out_proj(gdn_ctx *ctx, const uint8_t *y_codes, const uint8_t *y_scales, int B, uint16_t *out,
+                        void *stream) {
+  if (!ctx || !y_codes || !y_scales || !out) return GDN_E_NULL;
+  if (!aligned16(y_codes) || !aligned16(y_scales) || !aligned16(out)) return GDN_E_ALIGN;
+  if (B < 1 || B > 8 || !ctx->w_out_mma || ctx->Vd % 256) return GDN_E_SHAPE;
+  LaunchCtx lc{static_cast<cudaStream_t>(stream), ctx->num_sms, false};
+  return cuda_status(launch_gemv_mma(out_gemv_args(ctx, y_codes, y_scales, B, out, false), lc));
 }
 
 gdn_status gdn_check(gdn_ctx *ctx, int clear, void *stream) {

@@ -59,7 +59,7 @@ struct PmSmem {
     xh = up(ba + 2 * (size_t)(K / 2 + K / 16));
     part = up(xh + (size_t)MB * K * 2);
     bsum = up(part + (size_t)NG * 4 * 16 * MB * 4);
-    proj = up(bsum + (size_t)2 * MB * (K / 16) * 4);
+    proj = up(bsum + (size_t)2 * MB * (K / 16) * 4 + (size_t)2 * MB * 4 * 4);
     q = up(proj + (size_t)MB * (32 + 2 * R + 2) * 4);
     k = up(q + (size_t)MB * kPmD * 4);
     v = up(k + (size_t)MB * kPmD * 4);
@@ -279,6 +279,28 @@ __global__ void __launch_bounds__(kPmThreads, 1) proj_mix_kernel(PmArgs a) {
     }
   }
   __syncthreads();
+  // the b and a rows' quarter chains: one thread per (row, m, quarter), its
+  // block sums and scales in registers, then the FMAs in block order
+  float *bpart = bsum + (size_t)2 * MB * nblk;  // [2][MB][4], after the block sums
+  if (tid < 2 * B * 4) {
+    const int r = tid / (B * 4), rem = tid - r * B * 4, m = rem >> 2, q = rem & 3;
+    const int nq = nblk >> 2;  // blocks per quarter, a multiple of 4
+    const float4 *bs = reinterpret_cast<const float4 *>(bsum + (size_t)(r * MB + m) * nblk + q * nq);
+    const uint32_t *scw = reinterpret_cast<const uint32_t *>(bas + r * (K / 2 + K / 16) + K / 2 + q * nq);
+    float acc = 0.0f;
+#pragma unroll 4
+    for (int j4 = 0; j4 < nq / 4; ++j4) {
+      const float4 b4 = bs[j4];
+      float sw[4];
+      e4m3x4_to_f32(scw[j4], sw);
+      acc = fmaf(b4.x, sw[0], acc);
+      acc = fmaf(b4.y, sw[1], acc);
+      acc = fmaf(b4.z, sw[2], acc);
+      acc = fmaf(b4.w, sw[3], acc);
+    }
+    bpart[(r * MB + m) * 4 + q] = acc;
+  }
+  __syncthreads();
   // combine: projection value n of row m = ((q0 + q1) + q2) + q3, scaled, BF16
   {
     const float tsq = a.ts_in * a.ts_qkvz;
@@ -290,16 +312,8 @@ __global__ void __launch_bounds__(kPmThreads, 1) proj_mix_kernel(PmArgs a) {
         const float *p0 = part + (size_t)(g * 4) * 16 * MB + r * MB + m;
         const size_t qs = (size_t)16 * MB;
         y = (((p0[0] + p0[qs]) + p0[2 * qs]) + p0[3 * qs]) * tsq;
-      } else {  // b (n = NG*16) or a: the quarter chains, then the sum
-        const int r = n - NG * 16;
-        const float *bs = bsum + (size_t)(r * MB + m) * nblk;
-        const unsigned char *scl = bas + r * (K / 2 + K / 16) + K / 2;
-        float qv[4];
-        for (int q = 0; q < 4; ++q) {
-          float acc = 0.0f;
-          for (int j = q * (nblk / 4); j < (q + 1) * (nblk / 4); ++j) acc = fmaf(bs[j], e4m3_to_f32(scl[j]), acc);
-          qv[q] = acc;
-        }
+      } else {  // b (n = NG*16) or a: the quarter sums in order
+        const float *qv = bpart + ((n - NG * 16) * MB + m) * 4;
         y = (((qv[0] + qv[1]) + qv[2]) + qv[3]) * (a.ts_in * a.ts_ba);
       }
       proj[m * NP + n] = bf16_bits_to_f32(f32_to_bf16_bits(y));

@@ -1,4 +1,4 @@
-"""The oracle's token-by-token prefill on every host core.
+"""The oracle's token-by-token prefill and decode steps on every host core.
 
 TEST INFRASTRUCTURE, like the rest of ``oracle/``. This module adds no
 arithmetic: it runs the layer's own stages (``gdn.Layer.projections``,
@@ -14,7 +14,8 @@ CPU by comparing the two):
   Rocket blog's GDN entry: value head h reads key head h / (Hv / Hk));
 * the NVFP4 quantisers and the W4A4 products treat every token row on its own
   (one tensor scale per site, set in advance), so token ranges of the
-  projections and of the out-projection can run apart.
+  projections and of the out-projection can run apart, and the rows of a
+  decode batch (each with its own state) can too.
 
 Workers are started with the ``spawn`` method (safe in a process that already
 uses a GPU) and import numpy and the oracle only. BLAS threads are pinned to
@@ -138,26 +139,95 @@ def _init_worker(w: Weights):
     _W, _L = w, None
 
 
-def _task(job):
+def _layer():
     global _L
+    if _L is None:
+        _L = gdn.Layer(_W)
+    return _L
+
+
+def _task(job):
     kind = job[0]
     if kind == "group":
         _, kh, x_bits, conv_g, ssm_g = job
         return group_recurrence(group_weights(_W, kh), x_bits, conv_g, ssm_g)
     if kind == "out":
-        if _L is None:
-            _L = gdn.Layer(_W)
-        return _L.out_proj(job[1])
+        return _layer().out_proj(job[1])
+    if kind == "rows":   # decode rows with their own states (slots 0..n-1 of the job)
+        _, x_bits, ids, conv, ssm = job
+        out = _layer().decode_step(x_bits, ids, conv, ssm)
+        return out, conv, ssm
     raise ValueError(kind)
 
 
+def _pool(n: int, w: Weights):
+    saved = {v: os.environ.get(v) for v in _THREAD_VARS}
+    for v in _THREAD_VARS:
+        os.environ[v] = "1"
+    try:
+        return mp.get_context("spawn").Pool(n, initializer=_init_worker, initargs=(w,))
+    finally:
+        for v, val in saved.items():
+            if val is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = val
+
+
+def make_pool(weights, workers: int | None = None):
+    """A worker pool holding ``weights`` for repeated calls (pass it as
+    ``pool=``; the caller closes it). Its size is the core count used."""
+    n = (os.cpu_count() or 1) if workers is None else workers
+    return _pool(n, plain(weights)), n
+
+
+def decode_step(weights, x_bits: np.ndarray, slot_ids, conv_state: np.ndarray, ssm_state: np.ndarray,
+                workers: int | None = None, pool=None) -> np.ndarray:
+    """Same contract and result as ``gdn.Layer(weights).decode_step``: the rows
+    are split over ``workers`` processes (rows are independent: per-row
+    quantisation, products, state). 0 runs in this process; ``pool`` (from
+    make_pool with the same weights, and its size as ``workers``) is reused."""
+    w = plain(weights)
+    x_bits = np.asarray(x_bits, dtype=np.uint16).reshape(len(slot_ids), w.shape.hidden)
+    n = (os.cpu_count() or 1) if workers is None else workers
+    rows = list(range(len(slot_ids)))
+    parts = [rows[i::max(1, n)] for i in range(max(1, n))]
+    jobs, index = [], []
+    for part in parts:
+        if not part:
+            continue
+        live = [r for r in part if slot_ids[r] >= 0]
+        ids = [live.index(r) if slot_ids[r] >= 0 else -1 for r in part]
+        sl = [slot_ids[r] for r in live]
+        jobs.append(("rows", x_bits[part], ids, conv_state[sl].copy(), ssm_state[sl].copy()))
+        index.append((part, sl))
+    if n <= 0:
+        _init_worker(w)
+        res = [_task(j) for j in jobs]
+    elif pool is not None:
+        res = pool.map(_task, jobs, chunksize=1)
+    else:
+        own = _pool(n, w)
+        try:
+            res = own.map(_task, jobs, chunksize=1)
+        finally:
+            own.close()
+            own.join()
+    out = np.zeros((len(slot_ids), w.shape.hidden), np.uint16)
+    for (part, sl), (o, c, s) in zip(index, res):
+        out[part] = o
+        conv_state[sl] = c
+        ssm_state[sl] = s
+    return out
+
+
 def prefill(weights, x_bits: np.ndarray, conv_state: np.ndarray, ssm_state: np.ndarray, init_zero: bool,
-            workers: int | None = None) -> np.ndarray:
+            workers: int | None = None, pool=None) -> np.ndarray:
     """Same contract and result as ``gdn.Layer(weights).prefill`` for an FP32
     state: x_bits BF16 [T][H]; conv_state [K-1][C] and ssm_state [Hv][dv][dk]
     updated in place; returns out BF16 bits [T][H]. ``workers`` processes (by
     default one per host core, at most one per key head for the recurrence);
-    0 runs every task in this process."""
+    0 runs every task in this process; ``pool`` as for decode_step."""
     w = plain(weights)
     s = w.shape
     if init_zero:
@@ -170,25 +240,15 @@ def prefill(weights, x_bits: np.ndarray, conv_state: np.ndarray, ssm_state: np.n
         _, _, chans, heads = group_rows(s, kh)
         groups.append(("group", kh, x_bits, conv_state[:, chans].copy(), ssm_state[heads].copy()))
     n = (os.cpu_count() or 1) if workers is None else workers
+    own = None
     if n <= 0:
         _init_worker(w)
-        res = [_task(j) for j in groups]
         run = lambda jobs: [_task(j) for j in jobs]
-        pool = None
     else:
-        saved = {v: os.environ.get(v) for v in _THREAD_VARS}
-        for v in _THREAD_VARS:
-            os.environ[v] = "1"
-        try:
-            pool = mp.get_context("spawn").Pool(n, initializer=_init_worker, initargs=(w,))
-        finally:
-            for v, val in saved.items():
-                if val is None:
-                    os.environ.pop(v, None)
-                else:
-                    os.environ[v] = val
-        res = pool.map(_task, groups, chunksize=1)
+        if pool is None:
+            pool = own = _pool(n, w)
         run = lambda jobs: pool.map(_task, jobs, chunksize=1)
+    res = run(groups)
     try:
         y = np.empty((T, s.value_dim), dtype=np.float64)
         for (_, kh, _, _, _), (yg, cg, sg) in zip(groups, res):
@@ -200,7 +260,7 @@ def prefill(weights, x_bits: np.ndarray, conv_state: np.ndarray, ssm_state: np.n
         bounds = np.linspace(0, T, parts + 1).astype(int)
         outs = run([("out", y[a:b]) for a, b in zip(bounds[:-1], bounds[1:]) if b > a])
     finally:
-        if pool is not None:
-            pool.close()
-            pool.join()
+        if own is not None:
+            own.close()
+            own.join()
     return np.concatenate(outs, axis=0) if outs else np.zeros((0, s.hidden), np.uint16)

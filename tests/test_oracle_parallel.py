@@ -43,3 +43,21 @@ def test_parallel_prefill_crosses_token_chunks(monkeypatch):
     """Token chunks of 16 inside a worker: the states carry across them."""
     monkeypatch.setattr(parallel, "_TOKEN_CHUNK", 16)
     _both("TINY", 0, 53, workers=0)
+
+
+@pytest.mark.parametrize("workers", [0, 2])
+def test_parallel_decode_step_equals_oracle_decode_step(workers):
+    """Rows split over workers, with padding rows and slots out of row order."""
+    shape = synth.TINY
+    w = synth.layer_weights(shape, 0)
+    ids = [3, -1, 0, 5, 1]
+    S = 6
+    x = np.stack([synth.x_tokens(shape, 40 + r, 1)[0] for r in range(len(ids))])
+    c1 = np.stack([synth.conv_state(shape, 50 + s) for s in range(S)])
+    s1 = np.stack([synth.ssm_state(shape, 50 + s) for s in range(S)])
+    c2, s2 = c1.copy(), s1.copy()
+    want = gdn.Layer(w).decode_step(x, ids, c1, s1)
+    got = parallel.decode_step(w, x, ids, c2, s2, workers=workers)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(c2, c1)
+    np.testing.assert_array_equal(s2, s1)
