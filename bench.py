@@ -608,8 +608,15 @@ def main():
                          "rows): only that workload, one JSON line (for profiling)")
     ap.add_argument("--T", type=int, default=4096, help="prompt length for --case prefill")
     ap.add_argument("--batch", type=int, default=256, help="rows for --case batch")
+    ap.add_argument("--tune", default="", help="tuning knobs of gdn_set_tuning to set first, e.g. 13=1,0=1")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.tune and args.impl != "reference":
+        import nvfp4_gated_deltanet_gb300 as pkg
+        for kv in args.tune.split(","):
+            k, v = (int(t) for t in kv.split("="))
+            if pkg.lib().gdn_set_tuning(k, v) != 0:
+                raise SystemExit(f"bad tuning knob {kv}")
     if args.impl == "reference":
         return reference_arm(args)
     if args.case != "decode":
