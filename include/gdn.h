@@ -291,8 +291,9 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
 
 /* Process-wide tuning knobs (they change speed, never results beyond FP32
  * summation order). knob 0: projection kernel of decode and prefill:
- * 0 = automatic (more than 2 activation rows and a reduction length that is a
- * multiple of 256: tcgen05 block-scaled MMA; else the CUDA-core kernel),
+ * 0 = automatic (more than 4 activation rows and a reduction length that is a
+ * multiple of 256: tcgen05 block-scaled MMA; else the CUDA-core kernels, the
+ * warp-MMA one for up to 8 rows),
  * 1 = CUDA-core kernel (also for nvfp4_gemm with M <= 16), 2 = tensor cores
  * where the reduction length allows. knob 1 / knob 2: split-K of the in- /
  * out-projection on tensor cores, 0 = automatic, or 1, 2, 4, 8 (reduced to
@@ -343,9 +344,16 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * as two kernels: the in-projection rows of each key head computed inside the
  * cluster that mixes that head (conv, norms, gates, delta rule, gated norm,
  * quantisation), then the warp-MMA out-projection, which lets the next kernel
- * start at once (0 = automatic, the default: on where the shape allows and
- * knob 0 is not 2; 1 = off; 2 = on where the shape allows). Bit-identical to
- * the three-kernel step on the CUDA-core projections (knob 0 = 1).
+ * start at once (0 and 1 = off, the default: measured slower on GB300, only
+ * 15 of its 16 eight-CTA clusters fit at once; 2 = on where the shape allows
+ * and knob 0 is not 2). Bit-identical to the three-kernel step on the warp-MMA
+ * projections with four K slices (knob 0 = 1, knob 14 = 1).
+ * knob 14 / knob 15: tile of the warp-MMA in- / out-projection: 0 = automatic
+ * (in: one row 1, 2..4 rows 3; out: 2), 1 = two 16-row groups per CTA x four K
+ * slices, 2 = one group x eight K slices (reduction length a multiple of 512,
+ * else as 1), 3 = four groups x two K slices. knob 16: the warp-MMA kernels
+ * bring their activation rows into shared memory with one bulk copy per CTA
+ * (0 and 2 = yes, the default; 1 = per-thread loads).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

@@ -63,20 +63,32 @@ struct Tuning {
   int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto, 1 off, 2 streaming
                            // form whenever allowed, 3 weight-stationary form whenever allowed
   long long barrier_wait = 0;  // grid-barrier wait budget in SM cycles (0 = kWaitCycles)
-  int proj_mix = 0;        // decode of up to 8 rows with the in-projection inside the mixing kernel: 0 auto (on),
+  int proj_mix = 0;        // decode of up to 8 rows with the in-projection inside the mixing kernel: 0 auto (off),
                            // 1 off, 2 on
+  int tile_in = 0;         // warp-MMA tile of the in- / out-projection (GemvArgs::mma_tile): 0 auto
+  int tile_out = 0;
+  int act_bulk = 0;        // warp-MMA activation rows by one bulk copy: 0 auto, 1 off, 2 on
 };
 Tuning g_tune;
 
-// Automatic choice, measured on GB300 (decode stack, us per layer-step):
-// one row streams the weights faster through the CUDA-core GEMV (c1: 14.9 vs
-// 18.3); from two rows on the tensor cores win (c2: 26.1 on the GEMV, c4: 20.3
-// vs 36.2, c16: 34.8 vs 97.9).
+// Automatic choice, measured on GB300 (decode stack, us per layer-step): up
+// to four rows on the warp-MMA kernel (c1 13.6 vs 18.3, c2 15.1 vs 18.8, c4
+// 17.2 vs 19.2), from five rows on the tensor cores (c8 22.0 vs 27.2, c16
+// 31.6 vs 97.9 on the CUDA-core GEMV).
 bool use_tensor_cores(int rows) {
   if (g_tune.decode_gemm == 1) return false;
   if (g_tune.decode_gemm == 2) return true;
-  return rows > 1;
+  return rows > 4;
 }
+// Warp-MMA tiles (GemvArgs::mma_tile), measured on GB300: the in-projection of
+// one row as two 16-row groups per CTA x four K slices (c1 13.6 vs 14.0 with
+// four groups x two slices), of 2..4 rows as four groups x two slices (c2 15.1
+// vs 17.2); the out-projection as one group x eight K slices (128 CTAs instead
+// of 64: its post-wait MMA phase 1.5 -> 0.9 us). Activation rows come in by one
+// bulk copy per CTA.
+int tile_in(int rows) { return g_tune.tile_in ? g_tune.tile_in : (rows == 1 ? 1 : 3); }
+int tile_out() { return g_tune.tile_out ? g_tune.tile_out : 2; }
+bool act_bulk() { return g_tune.act_bulk != 1; }
 // Split-K for few activation rows: spreads the K loop of the 97 (in) or 16
 // (out) weight tiles over 2 or 4 CTAs of a cluster (measured best at B 1..16).
 int split_for(int knob_value, int rows, int dflt) {
@@ -220,6 +232,8 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
   g.K = c.hidden;
   g.status = ctx->status;
   g.w_mma = g_tune.gemv_mma != 1 ? ctx->w_in_mma : nullptr;
+  g.mma_tile = tile_in(rows);
+  g.mma_bulk = act_bulk();
   return run_gemv(g, lc, rows);
 }
 
@@ -271,6 +285,8 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
   o.K = ctx->Vd;
   o.status = ctx->status;
   o.w_mma = g_tune.gemv_mma != 1 ? ctx->w_out_mma : nullptr;
+  o.mma_tile = tile_out();
+  o.mma_bulk = act_bulk();
   // measured slower for the one-row GEMV chain (its weight prefetch then
   // competes with the mixing kernel), so only on request
   o.early_trigger = early && g_tune.early_trigger == 2 && rows <= 16;  // one launch, the step's last
@@ -334,6 +350,8 @@ GemvArgs out_gemv_args(gdn_ctx *ctx, const uint8_t *y_codes, const uint8_t *y_sc
   o.K = ctx->Vd;
   o.status = ctx->status;
   o.w_mma = ctx->w_out_mma;
+  o.mma_tile = tile_out();
+  o.mma_bulk = act_bulk();
   o.early_trigger = early ? 1 : 0;
   return o;
 }
@@ -439,6 +457,15 @@ gdn_status gdn_set_tuning(int knob, int value) {
     case 13:
       if (value < 0 || value > 2) return GDN_E_RANGE;
       g_tune.proj_mix = value;
+      return GDN_OK;
+    case 14:
+    case 15:
+      if (value < 0 || value > 3) return GDN_E_RANGE;
+      (knob == 14 ? g_tune.tile_in : g_tune.tile_out) = value;
+      return GDN_OK;
+    case 16:
+      if (value < 0 || value > 2) return GDN_E_RANGE;
+      g_tune.act_bulk = value;
       return GDN_OK;
     default:
       return GDN_E_RANGE;
@@ -680,7 +707,7 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
       return cuda_status(launch_fused(f, lc));
     }
   }
-  if (g_tune.proj_mix != 1 && g_tune.decode_gemm != 2 && pm_path(ctx, B)) {
+  if (g_tune.proj_mix == 2 && g_tune.decode_gemm != 2 && pm_path(ctx, B)) {
     // projections + mixing as one cluster kernel, then the warp-MMA out-projection
     cudaError_t e = launch_proj_mix(pm_args(ctx, x, slot_ids, B, conv_state, ssm_state, num_slots, ctx->y_codes,
                                             ctx->y_scales), lc);

@@ -372,9 +372,13 @@ struct GemvArgs {
   int M, N, K;
   int32_t *status;
   int early_trigger;  // as TcArgs::early_trigger
-  // Optional: the weights repacked for the warp-MMA one-row kernel
-  // (launch_mma_tiles); used when M == 1 and K % 256 == 0.
+  // Optional: the weights repacked for the warp-MMA kernel (launch_mma_tiles);
+  // used for 1..8 rows when K % 512 == 0.
   const uint8_t *w_mma;
+  // Warp-MMA tile: 1 (or 0) = two 16-row groups per CTA x four K slices, 2 = one
+  // group x eight K slices, 3 = four groups x two K slices. mma_bulk: the
+  // activation rows are bulk-copied into shared memory first.
+  int mma_tile, mma_bulk;
 };
 cudaError_t launch_gemv(const GemvArgs &a, const LaunchCtx &lc);
 // Warp-MMA one-row product (gemv_mma.cu) and its weight layout.

@@ -25,33 +25,44 @@ namespace gdn {
 
 namespace {
 
-constexpr int kMmaWarps = 8;  // 2 row groups x 4 K quarters per CTA
+constexpr int kMmaWarps = 8;  // GPC row groups x KS K slices per CTA
 
+// GPC 16-row groups per CTA, each split over KS warps by K slice (GPC * KS =
+// 8). BULK: the activation rows come into shared memory with one bulk copy
+// instead of per-thread loads (fewer requests on the L2 lines every CTA reads).
+template <int GPC, int KS, bool BULK>
 __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
+  static_assert(GPC * KS == kMmaWarps, "eight warps");
   extern __shared__ __align__(128) unsigned char smem[];
   if (a.early_trigger) pdl_launch_dependents();
-  const int K = a.K, nkb4 = K >> 6, qkb4 = nkb4 >> 2;  // 64-K steps: all, per quarter
+  const int K = a.K, nkb4 = K >> 6, qkb4 = nkb4 / KS;   // 64-K steps: all, per K slice
   const int M = a.M;                                    // activation rows = MMA columns, 1..8
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rgl = warp >> 2, q = warp & 3;                // row group in CTA, K quarter
-  const int rg = blockIdx.x * 2 + rgl;
+  const int rgl = warp / KS, q = warp % KS;             // row group in CTA, K slice
+  const int rg = blockIdx.x * GPC + rgl;
   const int ngroups = (a.N + 15) >> 4;
   const size_t group_bytes = (size_t)nkb4 * 576;
   const uint32_t cbytes = (uint32_t)qkb4 * 512, sbytes = (uint32_t)qkb4 * 64;
-  // smem: [barriers 8 x 8][per warp: codes cbytes | scales sbytes][x_hat M x K halves][partials 2 x 4 x 16 x M floats]
+  // smem: [barriers 8 x 8 + 1][per warp: codes cbytes | scales sbytes][x_hat M x K halves]
+  //       [partials GPC x KS x 16 x M floats][staged activation rows (BULK)]
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-  unsigned char *mine = smem + 64 + (size_t)warp * (cbytes + sbytes);
-  __half *xh = reinterpret_cast<__half *>(smem + 64 + (size_t)kMmaWarps * (cbytes + sbytes));
+  unsigned char *mine = smem + 128 + (size_t)warp * (cbytes + sbytes);
+  __half *xh = reinterpret_cast<__half *>(smem + 128 + (size_t)kMmaWarps * (cbytes + sbytes));
   float *part = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(xh) + (size_t)M * K * 2);
+  unsigned char *stage = reinterpret_cast<unsigned char *>(part) + (size_t)GPC * KS * 16 * M * 4;
   const bool have = rg < ngroups;
 
-  if (lane == 0 && have) {  // this warp's quarter of its row group: codes, then scales
+  if (lane == 0 && have) {  // this warp's K slice of its row group: codes, then scales
     mbar_init(bars + warp, 1);
+    if (BULK && warp == 0) mbar_init(bars + 8, 1);
     fence_barrier_init();
     const unsigned char *g = a.w_mma + (size_t)rg * group_bytes;
     mbar_arrive_expect_tx(bars + warp, cbytes + sbytes);
     bulk_g2s(mine, g + (size_t)q * cbytes, cbytes, bars + warp);
     bulk_g2s(mine + cbytes, g + (size_t)nkb4 * 512 + (size_t)q * sbytes, sbytes, bars + warp);
+  } else if (BULK && threadIdx.x == 0) {
+    mbar_init(bars + 8, 1);
+    fence_barrier_init();
   }
   __syncwarp();
 
@@ -61,6 +72,31 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
   {
     const int nblk = K >> 4;
     const float inv6ts = inv6ts_of(a.ts_a);
+    const uint16_t *xb = a.a_bf16;
+    const uint8_t *xc = a.a_codes, *xs = a.a_scales;
+    bool staged = false;
+    if (BULK) {
+      __syncthreads();  // barrier 8 initialised
+      const uint32_t nb = a.a_bf16 ? (uint32_t)M * K * 2 : (uint32_t)M * (K / 2 + K / 16);
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bars + 8, nb);
+        if (a.a_bf16) {
+          bulk_g2s(stage, a.a_bf16, (uint32_t)M * K * 2, bars + 8);
+        } else {
+          bulk_g2s(stage, a.a_codes, (uint32_t)M * K / 2, bars + 8);
+          bulk_g2s(stage + (size_t)M * K / 2, a.a_scales, (uint32_t)M * K / 16, bars + 8);
+        }
+      }
+      staged = mbar_wait(bars + 8, 0);
+      if (staged) {
+        if (a.a_bf16) {
+          xb = reinterpret_cast<const uint16_t *>(stage);
+        } else {
+          xc = stage;
+          xs = stage + (size_t)M * K / 2;
+        }
+      }
+    }
     for (int jm = threadIdx.x; jm < M * nblk; jm += blockDim.x) {
       const int m = jm / nblk, j = jm - m * nblk;
       bool live = true;
@@ -70,16 +106,16 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
       }
       uint32_t lo = 0, hi = 0, s = 0;
       if (live) {
-        if (a.a_bf16) {
+        if (xb) {
           float v[16];
-          load_bf16x16(a.a_bf16 + (size_t)m * K + (size_t)j * 16, v);
+          load_bf16x16(xb + (size_t)m * K + (size_t)j * 16, v);
           if (!quant_block16(v, a.ts_a, inv6ts, lo, hi, s) && blockIdx.x == 0)
             flag_status(a.status, GDN_E_NONFINITE);
         } else {
-          const uint2 c = *reinterpret_cast<const uint2 *>(a.a_codes + (size_t)m * (K >> 1) + (size_t)j * 8);
+          const uint2 c = *reinterpret_cast<const uint2 *>(xc + (size_t)m * (K >> 1) + (size_t)j * 8);
           lo = c.x;
           hi = c.y;
-          s = a.a_scales[(size_t)m * nblk + j];
+          s = xs[(size_t)m * nblk + j];
         }
       }
       store_xhat_block(xh + (size_t)m * K + (size_t)j * 16, lo, hi, s);
@@ -88,7 +124,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
   __syncthreads();
   if (!a.early_trigger) pdl_launch_dependents();
 
-  // ---- the quarter's block dot products: rows g, g+8 of the group x columns 2t, 2t+1
+  // ---- the slice's block dot products: rows g, g+8 of the group x columns 2t, 2t+1
   const int g = lane >> 2, t = lane & 3;
   float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   bool ok = true;
@@ -129,7 +165,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
     }
   }
   {
-    float *pq = part + (size_t)(rgl * 4 + q) * 16 * M;  // [16 rows][M columns]
+    float *pq = part + (size_t)(rgl * KS + q) * 16 * M;  // [16 rows][M columns]
     const int c0 = 2 * t, c1 = 2 * t + 1;
     if (c0 < M) {
       pq[g * M + c0] = acc[0];
@@ -141,13 +177,15 @@ __global__ void __launch_bounds__(kMmaWarps * 32) gemv_mma_kernel(GemvArgs a) {
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 32 * M; i += blockDim.x) {  // 2 groups x 16 rows x M: quarters added in order
+  for (int i = threadIdx.x; i < GPC * 16 * M; i += blockDim.x) {  // K slices added in order
     const int m = i % M, rr = i / M, gl = rr >> 4, r = rr & 15;
-    const int n = (blockIdx.x * 2 + gl) * 16 + r;
+    const int n = (blockIdx.x * GPC + gl) * 16 + r;
     if (n < a.N) {
-      const float *p0 = part + (size_t)(gl * 4) * 16 * M + r * M + m;
+      const float *p0 = part + (size_t)(gl * KS) * 16 * M + r * M + m;
       const size_t qs = (size_t)16 * M;
-      const float sum = ((p0[0] + p0[qs]) + p0[2 * qs]) + p0[3 * qs];
+      float sum = p0[0];
+#pragma unroll
+      for (int k = 1; k < KS; ++k) sum += p0[k * qs];
       const float y = sum * (a.ts_a * (n < a.n_split ? a.ts_w0 : a.ts_w1));
       if (a.c_is_bf16)
         static_cast<uint16_t *>(a.c)[(size_t)m * a.ldc + n] = f32_to_bf16_bits(y);
@@ -197,19 +235,23 @@ cudaError_t launch_mma_tiles(const uint8_t *codes, const uint8_t *scales, int ro
 
 bool gemv_mma_ok(const GemvArgs &a) { return a.w_mma && a.M >= 1 && a.M <= 8 && a.K % 256 == 0 && a.K <= 8192; }
 
-cudaError_t launch_gemv_mma(const GemvArgs &a, const LaunchCtx &lc) {
+namespace {
+template <int GPC, int KS, bool BULK>
+cudaError_t launch_gemv_mma_t(const GemvArgs &a, const LaunchCtx &lc) {
   const int ngroups = (a.N + 15) / 16;
-  const size_t per_warp = (size_t)(a.K / 256) * 576;
-  const size_t smem = 64 + kMmaWarps * per_warp + (size_t)a.M * a.K * 2 + 2 * 4 * 16 * 4 * (size_t)a.M;
+  const size_t per_warp = (size_t)(a.K / 64 / KS) * 576;
+  const size_t stage = BULK ? (a.a_bf16 ? (size_t)a.M * a.K * 2 : (size_t)a.M * (a.K / 2 + a.K / 16)) : 0;
+  const size_t smem = 128 + kMmaWarps * per_warp + (size_t)a.M * a.K * 2 + (size_t)GPC * KS * 16 * 4 * a.M + stage;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<GPC, KS, BULK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         200 * 1024);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((ngroups + 1) / 2, 1, 1);
+  cfg.gridDim = dim3((ngroups + GPC - 1) / GPC, 1, 1);
   cfg.blockDim = dim3(kMmaWarps * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = lc.stream;
@@ -218,7 +260,23 @@ cudaError_t launch_gemv_mma(const GemvArgs &a, const LaunchCtx &lc) {
   attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel, a);
+  return cudaLaunchKernelEx(&cfg, gemv_mma_kernel<GPC, KS, BULK>, a);
+}
+
+template <bool BULK>
+cudaError_t launch_gemv_mma_b(const GemvArgs &a, const LaunchCtx &lc) {
+  switch (a.mma_tile) {
+    case 2:
+      if (a.K % 512 == 0) return launch_gemv_mma_t<1, 8, BULK>(a, lc);
+      return launch_gemv_mma_t<2, 4, BULK>(a, lc);
+    case 3: return launch_gemv_mma_t<4, 2, BULK>(a, lc);
+    default: return launch_gemv_mma_t<2, 4, BULK>(a, lc);
+  }
+}
+}  // namespace
+
+cudaError_t launch_gemv_mma(const GemvArgs &a, const LaunchCtx &lc) {
+  return a.mma_bulk ? launch_gemv_mma_b<true>(a, lc) : launch_gemv_mma_b<false>(a, lc);
 }
 
 }  // namespace gdn

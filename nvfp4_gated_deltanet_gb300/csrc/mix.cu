@@ -28,13 +28,14 @@ namespace gdn {
 
 namespace {
 
-// State rows per warp: 8, or 16 when one CTA holds a whole head (the
-// per-warp work that does not scale with rows -- q/k norms, gates, the conv
-// share -- is then spread over twice the state). The row dot products reduce
-// over the lanes in the same butterfly order either way, so the results do
-// not depend on it.
+// State rows per warp: 16 when one CTA holds a whole head, 8 for half a head,
+// 4 for a quarter (eight warps per CTA at d = 128 whatever the slicing: the
+// smallest batches have the fewest CTAs, and their latency chain -- conv,
+// norms, the row reductions -- shortens with more warps in flight). The row
+// dot products reduce over the lanes in the same butterfly order whatever the
+// rows per warp, so the results do not depend on it.
 template <int NS>
-__host__ __device__ constexpr int rows_per_warp() { return NS == 1 ? 16 : 8; }
+__host__ __device__ constexpr int rows_per_warp() { return NS == 1 ? 16 : (NS == 2 ? 8 : 4); }
 
 
 template <int D, int NS, bool SB>
@@ -48,7 +49,7 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   constexpr int CPT = (NCH + THREADS - 1) / THREADS;    // channels per thread
   static_assert(R % 16 == 0 && WARPS >= 1 && R <= THREADS, "slice must hold whole quantisation blocks");
 
-  __shared__ float s_q[D], s_k[D], s_v[R], s_o[R], s_y[R];
+  __shared__ float s_q[D], s_k[D], s_v[R], s_o[R];
   __shared__ uint16_t s_qk_new[3][2 * D];  // new conv state of the q/k channels (K_conv <= 4)
   __shared__ float s_gsum[D / 16];         // sums of o^2 over the head's 16-row groups
 
@@ -167,6 +168,10 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   const uint16_t *bain = a.ba + (size_t)io * a.ld_ba;
   const float b_raw = bf16_bits_to_f32(bain[h]);
   const float a_raw = bf16_bits_to_f32(bain[a.Hv + h]);
+  // the gates need nothing else: start them before the conv
+  const float beta = sigmoidf_(b_raw);
+  const float g = -expf(A_log) * softplusf_(a_raw + dt_bias);
+  const float alpha = expf(g);
 
   // ---- conv + SiLU for q, k (key head kh, all D) and v (this slice)
 #pragma unroll
@@ -219,9 +224,6 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
     kq = fmaf(kr[e], qr[e], kq);
   }
   kq = warp_sum(kq);
-  const float beta = sigmoidf_(b_raw);
-  const float g = -expf(A_log) * softplusf_(a_raw + dt_bias);
-  const float alpha = expf(g);
 
   // ---- the delta rule on this warp's rows
   {
@@ -306,23 +308,45 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   for (int gi = 0; gi < D / 16; ++gi) sumsq += s_gsum[gi];
   const float rstd = 1.0f / sqrtf(sumsq / (float)D + a.rms_eps);
 
-  // ---- gated RMSNorm -> y (FP32), then NVFP4 blocks of 16 rows
+  // ---- gated RMSNorm -> y (FP32), then NVFP4 blocks of 16 rows, each block
+  // by 16 lanes: shuffle max, then every lane converts its own element -- the
+  // operations of quant_block16, so the same bits
+  float y = 0.0f;
   if (tid < R) {
-    const float y = s_o[tid] * rstd * nw * siluf_(zv);
-    s_y[tid] = y;
+    y = s_o[tid] * rstd * nw * siluf_(zv);
     if (a.y_f32) a.y_f32[(size_t)io * vd + h * D + row0 + tid] = y;
   }
-  __syncthreads();
-  if (a.y_codes && tid < R / 16) {
-    float v[16];
+  if (a.y_codes && warp < (R + 31) / 32) {  // whole warps (R is a multiple of 16)
+    float amax = fabsf(y);
+    int finite = amax <= 3.402823466e38f;  // false for NaN and +inf
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = s_y[tid * 16 + i];
-    uint32_t lo, hi, s;
-    if (!quant_block16(v, a.ts_out, inv6ts_of(a.ts_out), lo, hi, s)) flag_status(a.status, GDN_E_NONFINITE);
-    const size_t e0 = (size_t)io * vd + h * D + row0 + tid * 16;
-    *reinterpret_cast<uint2 *>(a.y_codes + (e0 >> 1)) = make_uint2(lo, hi);
-    const int blk = (h * D + row0 + tid * 16) >> 4;
-    a.y_scales[a.y_sf_tiled ? sf_tiled_offset(io, blk, vd >> 4) : (e0 >> 4)] = uint8_t(s);
+    for (int o = 8; o > 0; o >>= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o, 16));
+      finite &= __shfl_xor_sync(0xffffffffu, finite, o, 16);
+    }
+    uint32_t sc = 0, code2 = 0;
+    const float yn = __shfl_down_sync(0xffffffffu, y, 1, 16);
+    if (finite) {
+      sc = e4m3_from_f32(__fmul_rn(amax, inv6ts_of(a.ts_out)));
+      const float sv = e4m3_to_f32(sc);
+      if (sv != 0.0f) {
+        const float rr = __frcp_rn(__fmul_rn(sv, a.ts_out));
+        code2 = e2m1x2_from_f32(__fmul_rn(y, rr), __fmul_rn(yn, rr));
+      }
+    }
+    uint32_t lo = 0, hi = 0;  // the block's 8 code bytes (lanes 0, 2, .., 14 of the 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t b = __shfl_sync(0xffffffffu, code2, 2 * i, 16);
+      if (i < 4) lo |= b << (8 * i); else hi |= b << (8 * (i - 4));
+    }
+    if (tid < R && (tid & 15) == 0) {
+      if (!finite) flag_status(a.status, GDN_E_NONFINITE);
+      const size_t e0 = (size_t)io * vd + h * D + row0 + tid;
+      *reinterpret_cast<uint2 *>(a.y_codes + (e0 >> 1)) = make_uint2(lo, hi);
+      const int blk = (h * D + row0 + tid) >> 4;
+      a.y_scales[a.y_sf_tiled ? sf_tiled_offset(io, blk, vd >> 4) : (e0 >> 4)] = uint8_t(sc);
+    }
   }
 }
 

@@ -102,7 +102,7 @@ def test_tuning_knob_ranges(L):
     = 6); each is put back to its default (0) afterwards."""
     valid = {0: (0, 1, 2), 1: (0, 1, 2, 4, 8), 2: (0, 1, 2, 4, 8), 3: (0, 1, 2), 4: (0, 1, 2), 5: (0, 1, 2),
              6: (0, 1, 2), 7: (0, 1, 2, 4), 8: (0, 1, 2), 9: (0, 1, 2), 10: (0, 1, 2), 11: (0, 1, 2, 3),
-             13: (0, 1, 2)}
+             13: (0, 1, 2), 14: (0, 1, 2, 3), 15: (0, 1, 2, 3), 16: (0, 1, 2)}
     try:
         for knob, values in valid.items():
             for v in range(-1, 10):
@@ -110,7 +110,7 @@ def test_tuning_knob_ranges(L):
         for v in (0, 1, 1000, 2 ** 31 - 1):                    # knob 12: a wait budget in cycles
             assert L.gdn_set_tuning(12, v) == 0, v
         assert L.gdn_set_tuning(12, -1) == 6
-        assert L.gdn_set_tuning(14, 0) == 6
+        assert L.gdn_set_tuning(17, 0) == 6
         assert L.gdn_set_tuning(-1, 0) == 6
     finally:
         for knob in list(valid) + [12]:

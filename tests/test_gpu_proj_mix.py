@@ -1,6 +1,7 @@
 """The decode step with the in-projection inside the mixing kernel (up to 8
-rows, tuning knob 13) against the three-kernel step on the CUDA-core
-projections (knob 0 = 1, knob 13 = 1): the same arithmetic in the same order,
+rows, tuning knob 13) against the three-kernel step on the warp-MMA
+projections with four K slices (knob 0 = 1, knob 13 = 1, knob 14 = 1): the same
+arithmetic in the same order,
 so outputs, conv state and recurrent state must agree bit for bit, step after
 step -- with padding rows, a refused (repeated or out-of-range) slot, FP32 and
 BF16 state, and the two-way head-parallel shape. Both are also held to the
@@ -64,7 +65,7 @@ def test_fused_step_bit_identical_to_three_kernel_step(api, shape_name, ids, bf1
     ssm_all = np.stack([synth.ssm_state(shape, synth.slot_seed(s)) for s in range(S)])
     if bf16:
         ssm_all = synth.to_bf16_bits(ssm_all)
-    ref = _run(api, layer, {0: 1, 13: 1}, x, ids, conv_all, ssm_all, steps)
+    ref = _run(api, layer, {0: 1, 13: 1, 14: 1}, x, ids, conv_all, ssm_all, steps)
     got = _run(api, layer, {13: 2}, x, ids, conv_all, ssm_all, steps)
     assert ref[3] == 0 and got[3] == 0
     for a, b, what in zip(got[:3], ref[:3], ("out", "conv", "ssm")):
@@ -83,7 +84,7 @@ def test_fused_step_refuses_repeated_and_out_of_range_slots(api):
     layer = api.layer_from_synth(weights("FULL", 1), max_batch=16)
     x, conv0, ssm0 = slot_inputs(shape, [0, 1, 2], 1)
     for ids in ([1, 1, 0], [0, 9, 2]):
-        ref = _run(api, layer, {0: 1, 13: 1}, x, ids, conv0, ssm0, 1)
+        ref = _run(api, layer, {0: 1, 13: 1, 14: 1}, x, ids, conv0, ssm0, 1)
         got = _run(api, layer, {13: 2}, x, ids, conv0, ssm0, 1)
         assert ref[3] == 6 and got[3] == 6                  # GDN_E_RANGE
         for a, b in zip(got[:3], ref[:3]):

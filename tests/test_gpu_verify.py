@@ -1,9 +1,10 @@
 """Multi-token verify and its commit on the GPU (gdn_verify, gdn_verify_commit):
 outputs and per-token state snapshots against the oracle (BF16 outputs
 rel-L2 <= 4e-3, states rel-L2 <= 1e-4), bit-identity with the same number of
-gdn_decode_step calls on the same kernels (2+ rows: every projection runs on
-the tensor cores either way, and the mixing kernel's order does not depend on
-how many rows it serves), commits of 0, some and all tokens, and a padding row."""
+gdn_decode_step calls when both run their projections on the tensor cores
+(tuning knob 0 = 2; the mixing kernel's order does not depend on how many rows
+it serves) and agreement within tolerance under the automatic kernel choice,
+commits of 0, some and all tokens, and a padding row."""
 import numpy as np
 import pytest
 
@@ -78,19 +79,35 @@ def test_verify_commit_all_is_bitwise_r_decode_steps(api, state_bf16):
         from oracle import codecs
         ssm0 = codecs.f32_to_bf16(ssm0)
     ids = torch.arange(B, dtype=torch.int32, device="cuda")
-    # r decode steps
-    ca, sa = to_dev(conv0), to_dev(ssm0)
-    dec = np.stack([to_host(L.decode_step(to_dev(np.ascontiguousarray(x[:, t])), ids, ca, sa)) for t in range(r)],
-                   axis=1)
-    # verify + commit of every token
-    cb, sb = to_dev(conv0), to_dev(ssm0)
-    snap_c, snap_s = L.new_snapshots(B, r)
-    ver = to_host(L.verify(to_dev(x), ids, cb, sb, snap_c, snap_s))
-    L.verify_commit(ids, torch.full((B,), r, dtype=torch.int32, device="cuda"), snap_c, snap_s, cb, sb)
-    assert L.check() == 0
+
+    def run():
+        # r decode steps
+        ca, sa = to_dev(conv0), to_dev(ssm0)
+        dec = np.stack([to_host(L.decode_step(to_dev(np.ascontiguousarray(x[:, t])), ids, ca, sa))
+                        for t in range(r)], axis=1)
+        # verify + commit of every token
+        cb, sb = to_dev(conv0), to_dev(ssm0)
+        snap_c, snap_s = L.new_snapshots(B, r)
+        ver = to_host(L.verify(to_dev(x), ids, cb, sb, snap_c, snap_s))
+        L.verify_commit(ids, torch.full((B,), r, dtype=torch.int32, device="cuda"), snap_c, snap_s, cb, sb)
+        assert L.check() == 0
+        return ver, dec, (to_host(sb), to_host(sa)), (to_host(cb), to_host(ca))
+
+    # on the same projection kernels (tensor cores for B and for B * r rows): bit for bit
+    api.lib().gdn_set_tuning(0, 2)
+    try:
+        ver, dec, (sv, sd), (cv, cd) = run()
+    finally:
+        api.lib().gdn_set_tuning(0, 0)
     np.testing.assert_array_equal(ver, dec)
-    np.testing.assert_array_equal(to_host(sb), to_host(sa))
-    np.testing.assert_array_equal(to_host(cb), to_host(ca))
+    np.testing.assert_array_equal(sv, sd)
+    np.testing.assert_array_equal(cv, cd)
+    # with the automatic choice (B rows on the warp-MMA kernel, B * r on the tensor
+    # cores) the two differ only by FP32 summation order
+    ver, dec, (sv, sd), (cv, cd) = run()
+    assert rel_l2(_bf(ver), _bf(dec)) <= 4e-3
+    val = _bf if state_bf16 else (lambda a: a.astype(np.float64))
+    assert rel_l2(val(sv), val(sd)) <= 1e-4
 
 
 def test_verify_refuses_too_many_rows(api):
