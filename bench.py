@@ -35,9 +35,6 @@ UNIT = "us/step"
 W_BYTES = 14_155_776 + 73_728 + 4_718_592 + 65_536 + 256 + 512      # 19,014,400
 SEQ_BYTES = 4_194_304 + 98_304 + 4_096 + 4_096                       # 4,300,800
 GEMV_IN_BYTES = 12352 * (1024 + 128)                                  # qkvz+ba codes+scales
-# dram__bytes_read.sum + dram__bytes_write.sum of one in-projection GEMV launch
-# (ncu --set full capture of the decode c1 stack; summary in profiles/)
-GEMV_IN_TRAFFIC = 14_252_288
 
 
 def layer_bytes(sh, state_bf16=False):
@@ -179,29 +176,67 @@ def time_graph(g, steps, warmup):
     return e0.elapsed_time(e1) / steps  # ms per bench step
 
 
-def time_gemv(pkg, layers, xd, steps):
-    """The dominant kernel alone: the one-row W4A4 in-projection (q|k|v|z|b|a:
-    N = 12288 + 64 rows, K = 2048) of every layer instance of the stack, one
-    launch each through gdn_in_proj (the kernel gdn_decode_step runs for one
-    row), captured as one graph and timed with CUDA events on its stream."""
-    import torch
-    outs = [None] * len(layers)
-    x1 = xd[:1].contiguous()
+# Algorithmic bytes per launch of the c1 step's three kernels as the roofline leg
+# runs them (full-width layer, one row): the in-projection reads its weights
+# (q|k|v|z|b|a codes + scales) and x, writes the BF16 projections; the mixing
+# stage (gdn_mix_step) reads the projections, conv taps, gate parameters and
+# norm weight, reads and writes the FP32 recurrent state and the conv state,
+# writes y in FP32; the out-projection reads its weights and y (NVFP4), writes out.
+STAGE_KERNELS = {
+    "in_proj": "gemv_mma_kernel<2,4> (one-row W4A4 q|k|v|z|b|a projection, warp-MMA block products)",
+    "mix": "mix_kernel<128,4> (conv, norms, gates, gated delta rule, gated RMSNorm, NVFP4 y)",
+    "out_proj": "gemv_mma_kernel<1,8> (one-row W4A4 out-projection)",
+}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of
+# the current kernels (profiles/); a stage absent here has no capture yet
+STAGE_TRAFFIC = {}
+STAGE_BYTES = {
+    "in_proj": GEMV_IN_BYTES + 2048 * 2 + 12352 * 2,
+    "mix": 12352 * 2 + 8192 * 4 * 2 + 32 * 8 + 128 * 4 + 2 * 2_097_152 + 2 * 3 * 8192 * 2 + 4096 * 4,
+    "out_proj": 2048 * (2048 + 256) + 2048 + 256 + 2048 * 2,
+}
 
-    def one_pass():
-        for i, L in enumerate(layers):
-            outs[i] = L.in_proj(x1, out=outs[i])
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        one_pass()
-    torch.cuda.current_stream().wait_stream(s)
+
+def time_stages(pkg, layers, states, xd, steps):
+    """The c1 step's three kernels one at a time over the stack's layer
+    instances (each launch on its own layer's weights and state), each as one
+    CUDA graph timed with CUDA events on its stream: us per launch."""
+    import torch
+    L0 = layers[0]
+    x1 = xd[:1].contiguous()
+    ids = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nin = 2 * L0.Hk * L0.D + 2 * L0.Hv * L0.D + 2 * L0.Hv
+    proj = [torch.empty(1, nin, dtype=torch.int16, device="cuda") for _ in layers]
+    ycs = [torch.empty(1, L0.Hv * L0.D // 2, dtype=torch.uint8, device="cuda") for _ in layers]
+    yss = [torch.empty(1, L0.Hv * L0.D // 16, dtype=torch.uint8, device="cuda") for _ in layers]
+    yf = torch.empty(1, L0.Hv * L0.D, dtype=torch.float32, device="cuda")
+    out = torch.empty(1, L0.H, dtype=torch.int16, device="cuda")
+    for i, L in enumerate(layers):  # real projections and y for the later stages
+        L.in_proj(x1, None, proj[i])
+        ycs[i].zero_()
+        yss[i].fill_(0x38)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        one_pass()
-    ms = time_graph(g, steps, 3)
-    return ms / len(layers) * 1e3, len(layers)  # us per launch
+    nq = 2 * L0.Hk * L0.D + 2 * L0.Hv * L0.D
+    passes = {
+        "in_proj": lambda: [L.in_proj(x1, None, proj[i]) for i, L in enumerate(layers)],
+        "mix": lambda: [L.mix_step(proj[i][:, :nq], proj[i][:, nq:], ids, c, m, y=yf)
+                        for i, (L, (c, m)) in enumerate(zip(layers, states))],
+        "out_proj": lambda: [L.out_proj(ycs[i], yss[i], out=out) for i, L in enumerate(layers)],
+    }
+    res = {}
+    for name, fn in passes.items():
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        res[name] = time_graph(g, steps, 3) / len(layers) * 1e3
+        del g
+    return res
 
 
 def time_batch(pkg, synth, B, hbm_peak, n_layers=2, steps=10, state_bf16=False):
@@ -580,12 +615,14 @@ def single_case(args):
     elif args.case == "bucket":
         l2 = torch.cuda.get_device_properties(0).L2_cache_size
         B = args.batch
-        n_layers = args.layers or max(4, -(-4 * l2 // step_bytes(B)) + 1)
-        _, layers, states, xd = make_stack(pkg, synth, n_layers, B, max(16, B))
+        sh = synth.TP2 if args.shape == "tp2" else synth.FULL
+        n_layers = args.layers or max(4, -(-4 * l2 // step_bytes(B, sh)) + 1)
+        _, layers, states, xd = make_stack(pkg, synth, n_layers, B, max(16, B), shape=sh)
         g, _ = capture_stack(layers, states, xd, B)
         us = time_graph(g, args.steps, args.warmup) * 1e3 / n_layers
-        gbs = step_bytes(B) / (us * 1e-6) / 1e9
-        line = {"case": f"c{B}", "us_per_layer_step": round(us, 3), "hbm_gbs": round(gbs, 1),
+        gbs = step_bytes(B, sh) / (us * 1e-6) / 1e9
+        line = {"case": f"{'tp2_' if args.shape == 'tp2' else ''}c{B}", "us_per_layer_step": round(us, 3),
+                "hbm_gbs": round(gbs, 1),
                 "frac_of_peak": round(gbs / hbm_peak, 4), "layers": n_layers}
     else:
         r = time_batch(pkg, synth, args.batch, hbm_peak, steps=args.steps)
@@ -607,7 +644,8 @@ def main():
                     help="decode: the headline (default); prefill / batch / bucket (a decode stack at --batch "
                          "rows): only that workload, one JSON line (for profiling)")
     ap.add_argument("--T", type=int, default=4096, help="prompt length for --case prefill")
-    ap.add_argument("--batch", type=int, default=256, help="rows for --case batch")
+    ap.add_argument("--batch", type=int, default=256, help="rows for --case batch / bucket")
+    ap.add_argument("--shape", default="full", choices=["full", "tp2"], help="layer shape for --case bucket")
     ap.add_argument("--tune", default="", help="tuning knobs of gdn_set_tuning to set first, e.g. 13=1,0=1")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -653,9 +691,14 @@ def main():
     hbm_peak, peak_kind = peaks()
     gbs_step = step_bytes(1) / (us_layer * 1e-6) / 1e9
 
-    # ---- dominant kernel: the projection GEMV alone, live
-    us_gemv, _ = time_gemv(pkg, layers, xd, max(20, args.steps // 4))
-    gemv_gbs = GEMV_IN_BYTES / (us_gemv * 1e-6) / 1e9
+    # ---- the step's kernels one at a time, live: the dominant one by time
+    stages = time_stages(pkg, layers, states, xd, max(20, args.steps // 4))
+    kernels = {}
+    for name, us in stages.items():
+        gbs = STAGE_BYTES[name] / (us * 1e-6) / 1e9
+        kernels[name] = {"us_per_launch": round(us, 3), "bytes_per_launch": STAGE_BYTES[name],
+                         "achieved_gbs": round(gbs, 1), "frac": round(gbs / peaks()[0], 4)}
+    dom = max(stages, key=stages.get)
 
     # ---- e2e: the Python API with host buffers, copies inside the timed region
     import numpy as np
@@ -749,10 +792,11 @@ def main():
                   "l2_defeat": f"{n_layers} distinct layer instances, {n_layers * per_layer / 1e6:.0f} MB > 4x L2 "
                                f"({l2 / 1e6:.0f} MB)"},
         "hbm_gbs_step": round(gbs_step, 1), "hbm_frac_step": round(gbs_step / hbm_peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "gemv_mma_kernel (one-row W4A4 q|k|v|z|b|a projection, warp-MMA block products)",
-                     "achieved": round(gemv_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gemv_gbs / hbm_peak, 4), "peak_kind": peak_kind, "traffic": GEMV_IN_TRAFFIC,
-                     "us_per_launch": round(us_gemv, 3), "bytes_per_launch": GEMV_IN_BYTES},
+        "roofline": {"bound": "hbm", "kernel": STAGE_KERNELS[dom], "stage": dom,
+                     "achieved": kernels[dom]["achieved_gbs"], "peak": hbm_peak, "unit": "GB/s",
+                     "frac": kernels[dom]["frac"], "peak_kind": peak_kind, "traffic": STAGE_TRAFFIC.get(dom),
+                     "us_per_launch": kernels[dom]["us_per_launch"], "bytes_per_launch": STAGE_BYTES[dom],
+                     "kernels": kernels},
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(xh.numel() * 2),
                 "d2h_bytes_per_step": int(oh.numel() * 2),
                 "path": "GatedDeltaNetLayer.decode_step (ctypes -> C ABI), pinned host x in / out back, eager launches"},

@@ -313,7 +313,8 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * pre-swizzled copy made at gdn_create, one contiguous 16 KB bulk copy per
  * 128 x 256 tile (0 and 2 = yes, the default; 1 = tensor-map copies from the
  * row-major codes). knob 7: d_v slices per head in the decode mixing kernel
- * (0 = chosen from the batch, the default; 1, 2 or 4, reduced while the
+ * (0 = chosen from the batch and the value-head count, the default: 4 while
+ * Hv * B <= 16, else 2 up to 4 rows, else 1; or 1, 2 or 4, reduced while the
  * cluster of a key head would exceed 8 CTAs). knob 8: one-row projections
  * of a context on the CUDA cores take the block dot products with warp-level
  * MMA (mma.sync, FP16 in, FP32 out; weights repacked at create) instead of
@@ -349,11 +350,13 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * and knob 0 is not 2). Bit-identical to the three-kernel step on the warp-MMA
  * projections with four K slices (knob 0 = 1, knob 14 = 1).
  * knob 14 / knob 15: tile of the warp-MMA in- / out-projection: 0 = automatic
- * (in: one row 1, 2..4 rows 3; out: 2), 1 = two 16-row groups per CTA x four K
- * slices, 2 = one group x eight K slices (reduction length a multiple of 512,
- * else as 1), 3 = four groups x two K slices. knob 16: the warp-MMA kernels
- * bring their activation rows into shared memory with one bulk copy per CTA
- * (0 and 2 = yes, the default; 1 = per-thread loads).
+ * (in: one row 1, 2..4 rows 3; out: 2 when Hv*d_v >= 4096, else 1), 1 = two
+ * 16-row groups per CTA x four K slices, 2 = one group x eight K slices
+ * (reduction length a multiple of 512, else as 1), 3 = four groups x two K
+ * slices. knob 16: the warp-MMA kernels bring their activation rows into
+ * shared memory with one bulk copy per CTA (0 = automatic: for two or more
+ * rows, or one row in a launch of at least 256 CTAs; 1 = never, per-thread
+ * loads; 2 = always).
  * Returns GDN_E_RANGE for an unknown knob or value. Not thread-safe; set it
  * before launching work. */
 gdn_status gdn_set_tuning(int knob, int value);

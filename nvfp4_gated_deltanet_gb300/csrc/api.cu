@@ -83,12 +83,24 @@ bool use_tensor_cores(int rows) {
 // Warp-MMA tiles (GemvArgs::mma_tile), measured on GB300: the in-projection of
 // one row as two 16-row groups per CTA x four K slices (c1 13.6 vs 14.0 with
 // four groups x two slices), of 2..4 rows as four groups x two slices (c2 15.1
-// vs 17.2); the out-projection as one group x eight K slices (128 CTAs instead
-// of 64: its post-wait MMA phase 1.5 -> 0.9 us). Activation rows come in by one
-// bulk copy per CTA.
+// vs 17.2); the out-projection with K slices of 512 (K = 4096: one group x
+// eight slices, 128 CTAs, its post-wait MMA phase 1.5 -> 0.9 us; K = 2048: two
+// groups x four, the two-way head slice's c1 12.1 -> 10.4 us).
 int tile_in(int rows) { return g_tune.tile_in ? g_tune.tile_in : (rows == 1 ? 1 : 3); }
-int tile_out() { return g_tune.tile_out ? g_tune.tile_out : 2; }
-bool act_bulk() { return g_tune.act_bulk != 1; }
+int tile_out(int K) { return g_tune.tile_out ? g_tune.tile_out : (K >= 4096 ? 2 : 1); }
+// Activation rows by one bulk copy per CTA when there are several rows (c2
+// 16.1 -> 14.5 us, c4 18.1 -> 17.3) or many CTAs read the same row (the
+// full-width in-projection's 386: c1 15.6 -> 15.2 us); one row in a grid of a
+// few hundred CTAs or fewer is faster with per-thread loads (two-way slice
+// c1 10.4 -> 9.8).
+int mma_ctas(int tile, int N) {
+  const int gpc = tile == 2 ? 1 : (tile == 3 ? 4 : 2);
+  return ((N + 15) / 16 + gpc - 1) / gpc;
+}
+bool act_bulk(int tile, int N, int rows) {
+  if (g_tune.act_bulk) return g_tune.act_bulk == 2;
+  return rows > 1 || mma_ctas(tile, N) >= 256;
+}
 // Split-K for few activation rows: spreads the K loop of the 97 (in) or 16
 // (out) weight tiles over 2 or 4 CTAs of a cluster (measured best at B 1..16).
 int split_for(int knob_value, int rows, int dflt) {
@@ -233,7 +245,7 @@ cudaError_t run_in_proj(gdn_ctx *ctx, const uint16_t *x, int rows, const int32_t
   g.status = ctx->status;
   g.w_mma = g_tune.gemv_mma != 1 ? ctx->w_in_mma : nullptr;
   g.mma_tile = tile_in(rows);
-  g.mma_bulk = act_bulk();
+  g.mma_bulk = act_bulk(g.mma_tile, g.N, rows);
   return run_gemv(g, lc, rows);
 }
 
@@ -285,8 +297,8 @@ cudaError_t run_out_proj(gdn_ctx *ctx, uint16_t *out, int rows, const LaunchCtx 
   o.K = ctx->Vd;
   o.status = ctx->status;
   o.w_mma = g_tune.gemv_mma != 1 ? ctx->w_out_mma : nullptr;
-  o.mma_tile = tile_out();
-  o.mma_bulk = act_bulk();
+  o.mma_tile = tile_out(ctx->Vd);
+  o.mma_bulk = act_bulk(o.mma_tile, c.hidden, rows);
   // measured slower for the one-row GEMV chain (its weight prefetch then
   // competes with the mixing kernel), so only on request
   o.early_trigger = early && g_tune.early_trigger == 2 && rows <= 16;  // one launch, the step's last
@@ -350,8 +362,8 @@ GemvArgs out_gemv_args(gdn_ctx *ctx, const uint8_t *y_codes, const uint8_t *y_sc
   o.K = ctx->Vd;
   o.status = ctx->status;
   o.w_mma = ctx->w_out_mma;
-  o.mma_tile = tile_out();
-  o.mma_bulk = act_bulk();
+  o.mma_tile = tile_out(ctx->Vd);
+  o.mma_bulk = act_bulk(o.mma_tile, c.hidden, B);
   o.early_trigger = early ? 1 : 0;
   return o;
 }

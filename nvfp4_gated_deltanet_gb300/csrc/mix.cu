@@ -379,12 +379,14 @@ cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
 
 // Slices per head: more CTAs when the batch is small (the state traffic of one
 // row is spread over more SMs), bounded by the portable cluster size 8.
-// Measured on GB300 (us per layer-step): c4 20.5 with 2 slices vs 22.4 with
-// one; c8 24.5 with one vs 26.1 with two; batch 64 and 256 best with one.
+// Measured on GB300 (us per layer-step, full-width layer / two-way head
+// slice): c1 13.2 with two slices vs 13.6 with four and 14.6 with one; c2 14.5
+// vs 14.9 / 15.0; c4 equal for one and two; the two-way slice's c1 (16 value
+// heads) 12.1 with four vs 13.0 with two; c8 and larger batches best with one.
 cudaError_t launch_mix(const MixArgs &a, const LaunchCtx &lc) {
   if (a.B <= 0) return cudaSuccess;
   const int G = a.Hv / a.Hk;
-  int ns = a.slices > 0 ? a.slices : (a.B <= 2 ? 4 : (a.B <= 4 ? 2 : 1));
+  int ns = a.slices > 0 ? a.slices : (a.Hv * a.B <= 16 ? 4 : (a.B <= 4 ? 2 : 1));
   while (ns > 1 && G * ns > 8) ns >>= 1;
   if (G > 8) return cudaErrorInvalidValue;
   switch (a.D) {
