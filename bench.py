@@ -188,8 +188,9 @@ STAGE_KERNELS = {
     "out_proj": "gemv_mma_kernel<1,8> (one-row W4A4 out-projection)",
 }
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of
-# the current kernels (profiles/); a stage absent here has no capture yet
-STAGE_TRAFFIC = {}
+# the current kernels (profiles/decode_c1_inproj_mix_ncu.md); a stage absent
+# here has no capture of its current form
+STAGE_TRAFFIC = {"in_proj": 14_252_544, "mix": 2_278_912}
 STAGE_BYTES = {
     "in_proj": GEMV_IN_BYTES + 2048 * 2 + 12352 * 2,
     "mix": 12352 * 2 + 8192 * 4 * 2 + 32 * 8 + 128 * 4 + 2 * 2_097_152 + 2 * 3 * 8192 * 2 + 4096 * 4,
