@@ -38,8 +38,8 @@ template <int NS>
 __host__ __device__ constexpr int rows_per_warp() { return NS == 1 ? 16 : (NS == 2 ? 8 : 4); }
 
 
-template <int D, int NS, bool SB>
-__global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ? 2 : 0) mix_kernel(MixArgs a) {
+template <int D, int NS, bool SB, bool STR>
+__global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, STR ? 4 : (NS == 1 ? 2 : 0)) mix_kernel(MixArgs a) {
   constexpr int kRPW = rows_per_warp<NS>();
   constexpr int R = D / NS;
   constexpr int WARPS = R / kRPW;
@@ -111,36 +111,74 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
                           : static_cast<char *>(a.ssm_state) + s_slot) + s_rel;
   const float *S = reinterpret_cast<const float *>(s_rd);
   const uint16_t *Sb = reinterpret_cast<const uint16_t *>(s_rd);
-  float st[kRPW][EPL];
+  // STR: the state streams. This warp's rows are asked of L2 here and pass
+  // through registers 4 at a time after the wait, so the CTAs stay light
+  // enough (4 per SM) that a grid of more CTAs than two per SM is resident at
+  // once; with the rows held in registers from here such a grid ran as two
+  // waves (c16 31.0 -> 26.8 us per layer-step streamed; c8, whose grid fits,
+  // 21.9 held against 23.8 streamed).
+  constexpr bool STREAM = STR;
+  constexpr int RB = STREAM ? 4 : kRPW;  // state rows in registers at a time
+  float st[RB][EPL];
+  auto load_row = [&](int j, float (&dst)[EPL]) {
+    if (SB) {
+      uint16_t b[EPL];
+      if (EPL == 4) {
+        const uint2 t = *reinterpret_cast<const uint2 *>(Sb + (size_t)j * D);
+        b[0] = t.x & 0xFFFFu; b[1 % EPL] = t.x >> 16; b[2 % EPL] = t.y & 0xFFFFu; b[3 % EPL] = t.y >> 16;
+      } else if (EPL == 2) {
+        const uint32_t t = *reinterpret_cast<const uint32_t *>(Sb + (size_t)j * D);
+        b[0] = t & 0xFFFFu; b[1 % EPL] = t >> 16;
+      } else {
+        b[0] = Sb[(size_t)j * D];
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) dst[e] = bf16_bits_to_f32(b[e]);
+    } else if (EPL == 4) {
+      float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
+      dst[0] = t4.x; dst[1 % EPL] = t4.y; dst[2 % EPL] = t4.z; dst[3 % EPL] = t4.w;
+    } else if (EPL == 2) {
+      float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
+      dst[0] = t2.x; dst[1 % EPL] = t2.y;
+    } else {
+      dst[0] = S[(size_t)j * D];
+    }
+  };
   if (live) {
 #pragma unroll
     for (int c = 0; c < CPT; ++c)
 #pragma unroll
       for (int j = 0; j < 3; ++j)
         tap[c][j] = (tid + c * THREADS < NCH && j < Kc - 1) ? cst_rd[(size_t)j * C + ch[c]] : uint16_t(0);
+    if (STREAM) {
+      if (lane == 0)  // this warp's rows: one contiguous run (lane 0's offset is the row start)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(s_rd), "r"((uint32_t)(kRPW * D * kEs))
+                     : "memory");
+    } else {
 #pragma unroll
-    for (int j = 0; j < kRPW; ++j) {
-      if (SB) {
-        uint16_t b[EPL];
-        if (EPL == 4) {
-          const uint2 t = *reinterpret_cast<const uint2 *>(Sb + (size_t)j * D);
-          b[0] = t.x & 0xFFFFu; b[1 % EPL] = t.x >> 16; b[2 % EPL] = t.y & 0xFFFFu; b[3 % EPL] = t.y >> 16;
+      for (int j = 0; j < kRPW; ++j) {
+        if (SB) {
+          uint16_t b[EPL];
+          if (EPL == 4) {
+            const uint2 t = *reinterpret_cast<const uint2 *>(Sb + (size_t)j * D);
+            b[0] = t.x & 0xFFFFu; b[1 % EPL] = t.x >> 16; b[2 % EPL] = t.y & 0xFFFFu; b[3 % EPL] = t.y >> 16;
+          } else if (EPL == 2) {
+            const uint32_t t = *reinterpret_cast<const uint32_t *>(Sb + (size_t)j * D);
+            b[0] = t & 0xFFFFu; b[1 % EPL] = t >> 16;
+          } else {
+            b[0] = Sb[(size_t)j * D];
+          }
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) st[j][e] = bf16_bits_to_f32(b[e]);
+        } else if (EPL == 4) {
+          float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
+          st[j][0] = t4.x; st[j][1 % EPL] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
         } else if (EPL == 2) {
-          const uint32_t t = *reinterpret_cast<const uint32_t *>(Sb + (size_t)j * D);
-          b[0] = t & 0xFFFFu; b[1 % EPL] = t >> 16;
+          float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
+          st[j][0] = t2.x; st[j][1 % EPL] = t2.y;
         } else {
-          b[0] = Sb[(size_t)j * D];
+          st[j][0] = S[(size_t)j * D];
         }
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) st[j][e] = bf16_bits_to_f32(b[e]);
-      } else if (EPL == 4) {
-        float4 t4 = *reinterpret_cast<const float4 *>(S + (size_t)j * D);
-        st[j][0] = t4.x; st[j][1 % EPL] = t4.y; st[j][2 % EPL] = t4.z; st[j][3 % EPL] = t4.w;
-      } else if (EPL == 2) {
-        float2 t2 = *reinterpret_cast<const float2 *>(S + (size_t)j * D);
-        st[j][0] = t2.x; st[j][1 % EPL] = t2.y;
-      } else {
-        st[j][0] = S[(size_t)j * D];
       }
     }
   }
@@ -225,54 +263,115 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   }
   kq = warp_sum(kq);
 
-  // ---- the delta rule on this warp's rows
-  {
-    float vals[2 * kRPW];
-#pragma unroll
-    for (int j = 0; j < kRPW; ++j) {
-      float dk = 0.0f, dq = 0.0f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        dk = fmaf(st[j][e], kr[e], dk);
-        dq = fmaf(st[j][e], qr[e], dq);
-      }
-      vals[j] = dk;
-      vals[kRPW + j] = dq;
-    }
-    const float tot = warp_transpose_reduce<2 * kRPW>(vals, lane);
-#pragma unroll
-    for (int j = 0; j < kRPW; ++j) {
-      const float Sk = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(j));
-      const float Sq = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(kRPW + j));
-      // S <- alpha S; u = beta (v - S k); S <- S + u k^T; o = S q
-      //   => (alpha S) k = alpha Sk, o = alpha Sq + u (k . q)
-      const float u = beta * (s_v[lr0 + j] - alpha * Sk);
-      const float o = fmaf(u, kq, alpha * Sq);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) st[j][e] = fmaf(u, kr[e], alpha * st[j][e]);
-      if (lane == 0) s_o[lr0 + j] = o;
-    }
+  // ---- the delta rule on this warp's rows, RB at a time
+  auto store_row = [&](int j, const float (&src)[EPL]) {
     float *Sf = reinterpret_cast<float *>(s_wr);
     uint16_t *Sw = reinterpret_cast<uint16_t *>(s_wr);
+    if (SB) {
+      uint32_t b[EPL];
 #pragma unroll
-    for (int j = 0; j < kRPW; ++j) {
-      if (SB) {
-        uint32_t b[EPL];
+      for (int e = 0; e < EPL; ++e) b[e] = f32_to_bf16_bits(src[e]);
+      if (EPL == 4)
+        *reinterpret_cast<uint2 *>(Sw + (size_t)j * D) = make_uint2(b[0] | (b[1 % EPL] << 16), b[2 % EPL] | (b[3 % EPL] << 16));
+      else if (EPL == 2)
+        *reinterpret_cast<uint32_t *>(Sw + (size_t)j * D) = b[0] | (b[1 % EPL] << 16);
+      else
+        Sw[(size_t)j * D] = (uint16_t)b[0];
+    } else if (EPL == 4) {
+      *reinterpret_cast<float4 *>(Sf + (size_t)j * D) = make_float4(src[0], src[1 % EPL], src[2 % EPL], src[3 % EPL]);
+    } else if (EPL == 2) {
+      *reinterpret_cast<float2 *>(Sf + (size_t)j * D) = make_float2(src[0], src[1 % EPL]);
+    } else {
+      Sf[(size_t)j * D] = src[0];
+    }
+  };
+  if constexpr (STREAM) {
+  #pragma unroll 1
+    for (int j0 = 0; j0 < kRPW; j0 += RB) {
+      if (STREAM) {
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) b[e] = f32_to_bf16_bits(st[j][e]);
-        if (EPL == 4)
-          *reinterpret_cast<uint2 *>(Sw + (size_t)j * D) = make_uint2(b[0] | (b[1 % EPL] << 16), b[2 % EPL] | (b[3 % EPL] << 16));
-        else if (EPL == 2)
-          *reinterpret_cast<uint32_t *>(Sw + (size_t)j * D) = b[0] | (b[1 % EPL] << 16);
-        else
-          Sw[(size_t)j * D] = (uint16_t)b[0];
-      } else if (EPL == 4) {
-        *reinterpret_cast<float4 *>(Sf + (size_t)j * D) =
-            make_float4(st[j][0], st[j][1 % EPL], st[j][2 % EPL], st[j][3 % EPL]);
-      } else if (EPL == 2) {
-        *reinterpret_cast<float2 *>(Sf + (size_t)j * D) = make_float2(st[j][0], st[j][1 % EPL]);
-      } else {
-        Sf[(size_t)j * D] = st[j][0];
+        for (int jj = 0; jj < RB; ++jj) load_row(j0 + jj, st[jj]);
+      }
+      float vals[2 * RB];
+#pragma unroll
+      for (int jj = 0; jj < RB; ++jj) {
+        float dk = 0.0f, dq = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          dk = fmaf(st[jj][e], kr[e], dk);
+          dq = fmaf(st[jj][e], qr[e], dq);
+        }
+        vals[jj] = dk;
+        vals[RB + jj] = dq;
+      }
+      // the same lane butterfly for every value whatever RB is: each row's
+      // totals do not depend on how many rows are reduced together
+      const float tot = warp_transpose_reduce<2 * RB>(vals, lane);
+#pragma unroll
+      for (int jj = 0; jj < RB; ++jj) {
+        const float Sk = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * RB>(jj));
+        const float Sq = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * RB>(RB + jj));
+        // S <- alpha S; u = beta (v - S k); S <- S + u k^T; o = S q
+        //   => (alpha S) k = alpha Sk, o = alpha Sq + u (k . q)
+        const float u = beta * (s_v[lr0 + j0 + jj] - alpha * Sk);
+        const float o = fmaf(u, kq, alpha * Sq);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) st[jj][e] = fmaf(u, kr[e], alpha * st[jj][e]);
+        if (lane == 0) s_o[lr0 + j0 + jj] = o;
+      }
+#pragma unroll
+      for (int jj = 0; jj < RB; ++jj) store_row(j0 + jj, st[jj]);
+    }
+  } else {
+    // ---- the delta rule on this warp's rows
+    {
+      float vals[2 * kRPW];
+#pragma unroll
+      for (int j = 0; j < kRPW; ++j) {
+        float dk = 0.0f, dq = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          dk = fmaf(st[j][e], kr[e], dk);
+          dq = fmaf(st[j][e], qr[e], dq);
+        }
+        vals[j] = dk;
+        vals[kRPW + j] = dq;
+      }
+      const float tot = warp_transpose_reduce<2 * kRPW>(vals, lane);
+#pragma unroll
+      for (int j = 0; j < kRPW; ++j) {
+        const float Sk = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(j));
+        const float Sq = __shfl_sync(0xffffffffu, tot, reduce_owner<2 * kRPW>(kRPW + j));
+        // S <- alpha S; u = beta (v - S k); S <- S + u k^T; o = S q
+        //   => (alpha S) k = alpha Sk, o = alpha Sq + u (k . q)
+        const float u = beta * (s_v[lr0 + j] - alpha * Sk);
+        const float o = fmaf(u, kq, alpha * Sq);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) st[j][e] = fmaf(u, kr[e], alpha * st[j][e]);
+        if (lane == 0) s_o[lr0 + j] = o;
+      }
+      float *Sf = reinterpret_cast<float *>(s_wr);
+      uint16_t *Sw = reinterpret_cast<uint16_t *>(s_wr);
+#pragma unroll
+      for (int j = 0; j < kRPW; ++j) {
+        if (SB) {
+          uint32_t b[EPL];
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) b[e] = f32_to_bf16_bits(st[j][e]);
+          if (EPL == 4)
+            *reinterpret_cast<uint2 *>(Sw + (size_t)j * D) = make_uint2(b[0] | (b[1 % EPL] << 16), b[2 % EPL] | (b[3 % EPL] << 16));
+          else if (EPL == 2)
+            *reinterpret_cast<uint32_t *>(Sw + (size_t)j * D) = b[0] | (b[1 % EPL] << 16);
+          else
+            Sw[(size_t)j * D] = (uint16_t)b[0];
+        } else if (EPL == 4) {
+          *reinterpret_cast<float4 *>(Sf + (size_t)j * D) =
+              make_float4(st[j][0], st[j][1 % EPL], st[j][2 % EPL], st[j][3 % EPL]);
+        } else if (EPL == 2) {
+          *reinterpret_cast<float2 *>(Sf + (size_t)j * D) = make_float2(st[j][0], st[j][1 % EPL]);
+        } else {
+          Sf[(size_t)j * D] = st[j][0];
+        }
       }
     }
   }
@@ -350,7 +449,7 @@ __global__ void __launch_bounds__((D / NS / rows_per_warp<NS>()) * 32, NS == 1 ?
   }
 }
 
-template <int D, int NS, bool SB>
+template <int D, int NS, bool SB, bool STR>
 cudaError_t launch_dn_t(const MixArgs &a, const LaunchCtx &lc) {
   const int G = a.Hv / a.Hk;
   cudaLaunchConfig_t cfg = {};
@@ -367,12 +466,19 @@ cudaError_t launch_dn_t(const MixArgs &a, const LaunchCtx &lc) {
   attr[1].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, mix_kernel<D, NS, SB>, a);
+  return cudaLaunchKernelEx(&cfg, mix_kernel<D, NS, SB, STR>, a);
+}
+
+template <int D, int NS, bool STR>
+cudaError_t launch_dn_s(const MixArgs &a, const LaunchCtx &lc) {
+  return a.state_bf16 ? launch_dn_t<D, NS, true, STR>(a, lc) : launch_dn_t<D, NS, false, STR>(a, lc);
 }
 
 template <int D, int NS>
 cudaError_t launch_dn(const MixArgs &a, const LaunchCtx &lc) {
-  return a.state_bf16 ? launch_dn_t<D, NS, true>(a, lc) : launch_dn_t<D, NS, false>(a, lc);
+  if constexpr (NS == 1)
+    if ((long long)a.Hv * a.B > 2LL * lc.num_sms) return launch_dn_s<D, NS, true>(a, lc);
+  return launch_dn_s<D, NS, false>(a, lc);
 }
 
 }  // namespace
