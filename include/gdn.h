@@ -320,8 +320,10 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * MMA (mma.sync, FP16 in, FP32 out; weights repacked at create) instead of
  * FP16x2 chains (0 and 2 = yes, the default; 1 = no). knob 9: the decode
  * token mixing as three kernels -- conv/norms/gates, the delta rule alone,
- * gated norm + quantisation -- with bit-identical results (0 = from 96 rows,
- * the default; 1 = never; 2 = always). knob 10: the prefill chunk scan's
+ * gated norm + quantisation -- with bit-identical results (0 and 1 = never,
+ * the default: the one mixing kernel, whose state streams through registers
+ * when its grid exceeds two CTAs per SM, measured faster at every batch size;
+ * 2 = always). knob 10: the prefill chunk scan's
  * products (W S^T, Q S^T, A U, the state update) on warp-level tensor-core MMA
  * in split TF32 (hi.hi + hi.lo + lo.hi) for d = 128 (0 and 2 = yes, the
  * default; 1 = FP32 on the CUDA cores). knob 11: tensor-core projections with

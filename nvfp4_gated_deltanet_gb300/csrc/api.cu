@@ -58,7 +58,7 @@ struct Tuning {
   int swizzled_tiles = 0;  // tensor-core weights from the pre-swizzled tile copy: 0 auto (on), 1 off, 2 on
   int mix_slices = 0;      // d_v slices per head in the mixing kernel: 0 auto, 1, 2, 4
   int gemv_mma = 0;        // one-row projections with warp-level MMA block products: 0 auto (on), 1 off, 2 on
-  int batch_split = 0;     // decode mixing as prep / delta / gated-norm kernels: 0 auto (B >= 96), 1 off, 2 on
+  int batch_split = 0;     // decode mixing as prep / delta / gated-norm kernels: 0 and 1 off, 2 on
   int scan_tc = 0;         // prefill chunk scan products on warp-level tensor cores: 0 auto (on), 1 off, 2 on
   int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto, 1 off, 2 streaming
                            // form whenever allowed, 3 weight-stationary form whenever allowed
@@ -746,8 +746,10 @@ gdn_status gdn_decode_step(gdn_ctx *ctx, const uint16_t *x, const int32_t *slot_
   m.y_scales = ctx->y_scales;
   m.y_sf_tiled = out_proj_tiled(ctx, B) ? 1 : 0;
   m.y_f32 = nullptr;
-  // large batches: the state stream in a kernel of its own (bit-identical)
-  const bool split = g_tune.batch_split == 2 || (g_tune.batch_split == 0 && B >= 96);
+  // the mixing as three kernels (bit-identical) only on request: the fused
+  // kernel's streaming form measured faster at every batch (96: 91.4 against
+  // 100.6 us per layer-step, 128: 109.3 against 119.9, 256: 194.8 against 209.1)
+  const bool split = g_tune.batch_split == 2;
   e = split ? launch_batch_mix(m, ctx->bws, lc) : launch_mix(m, lc);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(run_out_proj(ctx, out, B, lc, true, true));
