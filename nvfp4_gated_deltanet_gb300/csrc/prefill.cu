@@ -176,6 +176,14 @@ GDN_DEV void mma3(float (&d)[4], const float (&af)[4], const float (&bf)[2]) {
 
 
 // ---------------------------------------------------------------- chunk_prep
+// 16-byte asynchronous copy global -> shared; zero-filled when !valid.
+GDN_DEV void cp_async16(void *dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+GDN_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+GDN_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // One CTA (256 threads) per (chunk, value head). Tokens past T count as zero
 // (k = q = v = 0, beta = 0, g = 0), which adds nothing to any product.
 template <int D>
@@ -187,6 +195,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
   float *Lm = QR + kC * XLD;      // [kC][kC]
   float *gam = Lm + kC * kC;      // [kC]
   float *bet = gam + kC;          // [kC]
+  float *bek = bet + kC;          // [kC]: beta_i e^Gamma_i
   const int c = blockIdx.x, h = blockIdx.y;
   const int kh = h / (a.Hv / a.Hk);
   const int t0 = c * kC;
@@ -267,6 +276,17 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
     }
   }
   __syncthreads();
+  // v of the chunk into Q's rows (Q is consumed), so that the substitution
+  // below reads every right-hand side from shared memory
+  float *VR = QR;
+  for (int e = tid; e < kC * D / 4; e += 256) {
+    const int i = (4 * e) / D, d = (4 * e) % D;
+    cp_async16(VR + i * XLD + d, a.v + ((size_t)h * a.Tp + t0 + i) * D + d, t0 + i < a.T);
+  }
+  cp_async_commit();
+  if (tid < kC) bek[tid] = bet[tid] * expf(gam[tid]);
+  cp_async_wait_all();
+  __syncthreads();
 
   // (I + L) X = R by forward substitution, one column per thread (no barriers):
   // columns 0..D-1 give W (R = beta e^Gamma k), D..2D-1 give Ut (R = beta v).
@@ -275,12 +295,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
     const int col = tid;
     float X[kC];
 #pragma unroll
-    for (int i = 0; i < kC; ++i) {
-      if (col < D)
-        X[i] = bet[i] * expf(gam[i]) * KR[i * XLD + col];
-      else
-        X[i] = (t0 + i < a.T) ? bet[i] * a.v[((size_t)h * a.Tp + t0 + i) * D + (col - D)] : 0.0f;
-    }
+    for (int i = 0; i < kC; ++i) X[i] = col < D ? bek[i] * KR[i * XLD + col] : bet[i] * VR[i * XLD + (col - D)];
 #pragma unroll
     for (int i = 1; i < kC; ++i) {
       // four independent partial sums shorten the dependent FMA chain 4x
@@ -304,12 +319,6 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- chunk_scan
-GDN_DEV void cp_async16(void *dst, const void *src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-GDN_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-GDN_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // One CTA (512 threads = 16 warps) per (value head, 32 rows of d_v). The state
 // slice S[32][D] stays in shared memory across all chunks; lane = row r of the
@@ -720,7 +729,7 @@ __global__ void copy_u16_kernel(uint16_t *dst, const uint16_t *src, int n) {
 
 template <int D>
 cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
-  const size_t sm_prep = (size_t)(2 * kC * (D + 4) + kC * kC + 2 * kC) * sizeof(float);
+  const size_t sm_prep = (size_t)(2 * kC * (D + 4) + kC * kC + 3 * kC) * sizeof(float);
   const size_t sm_scan =
       (size_t)(3 * kC * D + kC * 32 + kC * kC + kC + 32 * (D + 1) + 2 * kC * 33 + kC * 33) * sizeof(float);
   static bool configured = false;
