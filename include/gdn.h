@@ -323,10 +323,11 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * gated norm + quantisation -- with bit-identical results (0 and 1 = never,
  * the default: the one mixing kernel, whose state streams through registers
  * when its grid exceeds two CTAs per SM, measured faster at every batch size;
- * 2 = always). knob 10: the prefill chunk scan's
- * products (W S^T, Q S^T, A U, the state update) on warp-level tensor-core MMA
- * in split TF32 (hi.hi + hi.lo + lo.hi) for d = 128 (0 and 2 = yes, the
- * default; 1 = FP32 on the CUDA cores). knob 11: tensor-core projections with
+ * 2 = always). knob 10: the prefill chunk scan's products (W S^T, Q S^T,
+ * A U, the state update) in split TF32 (hi.hi + hi.lo + lo.hi): 0 = automatic
+ * (tcgen05 MMAs with TMEM accumulators for d = 128, else FP32 on the CUDA
+ * cores), 1 = FP32 on the CUDA cores, 2 = warp-level MMA (d = 128), 3 =
+ * tcgen05 (d = 128); the three tensor-core forms agree to FP32 rounding. knob 11: tensor-core projections with
  * 128-token activation tiles, tiled scales and BF16 output as one persistent
  * CTA per SM with two TMEM accumulators, so that the epilogue of one output
  * tile overlaps the MMAs of the next. Two forms: streaming (both operands

@@ -24,6 +24,7 @@ struct gdn_ctx {
   float *qn, *kn, *v, *beta, *gl, *o;     // prefill intermediates (head-major, chunk-padded)
   BatchWs bws;                          // large-batch decode intermediates, max_batch rows
   float *W, *Ut, *Am, *Gam;               // per (value head, 64-token chunk) products
+  float *KT = nullptr;                    // per (key head, chunk) K^T for the tcgen05 chunk scan
   uint16_t *conv_tmp;                   // [K-1][C]
   uint8_t *xq_codes, *xq_scales;        // [prow][H/2] and tiled scales: x as NVFP4 for the tensor-core GEMM
   uint8_t *w_in_sf_t, *w_out_sf_t;      // the weights' scales in the tiled layout tcgen05.cp reads
@@ -59,7 +60,7 @@ struct Tuning {
   int mix_slices = 0;      // d_v slices per head in the mixing kernel: 0 auto, 1, 2, 4
   int gemv_mma = 0;        // one-row projections with warp-level MMA block products: 0 auto (on), 1 off, 2 on
   int batch_split = 0;     // decode mixing as prep / delta / gated-norm kernels: 0 and 1 off, 2 on
-  int scan_tc = 0;         // prefill chunk scan products on warp-level tensor cores: 0 auto (on), 1 off, 2 on
+  int scan_tc = 0;         // prefill chunk scan: 0 auto (tcgen05 for d = 128), 1 FP32 CUDA cores, 2 warp MMA, 3 tcgen05
   int persist_gemm = 0;    // tensor-core projections as one persistent CTA per SM: 0 auto, 1 off, 2 streaming
                            // form whenever allowed, 3 weight-stationary form whenever allowed
   long long barrier_wait = 0;  // grid-barrier wait budget in SM cycles (0 = kWaitCycles)
@@ -455,7 +456,7 @@ gdn_status gdn_set_tuning(int knob, int value) {
       g_tune.batch_split = value;
       return GDN_OK;
     case 10:
-      if (value < 0 || value > 2) return GDN_E_RANGE;
+      if (value < 0 || value > 3) return GDN_E_RANGE;
       g_tune.scan_tc = value;
       return GDN_OK;
     case 11:
@@ -583,6 +584,7 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Ut, Tp * Hv * D);
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Am, Tp * Hv * 64);
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Gam, Tp * Hv);
+    if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->KT, Tp * Hk * D);
   }
   // weights into the kernels' layout: [qkvz; ba] as one matrix for one pass over x
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->w_in_codes, w->qkvz.codes, Nqkvz * H / 2, cudaMemcpyDeviceToDevice, s);
@@ -915,7 +917,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.conv_state = cst;
   p.ssm = S;
   p.state_bf16 = c.state_bf16;
-  p.scan_tc = g_tune.scan_tc != 1;
+  p.scan_tc = g_tune.scan_tc == 1 ? 0 : (g_tune.scan_tc == 2 || D != 128) ? 1 : 2;
   p.conv_w = ctx->conv_w;
   p.A_log = ctx->A_log;
   p.dt_bias = ctx->dt_bias;
@@ -938,6 +940,7 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.Ut = ctx->Ut;
   p.Am = ctx->Am;
   p.Gam = ctx->Gam;
+  p.KT = p.scan_tc == 2 ? ctx->KT : nullptr;
   p.o = ctx->o;
   p.y_codes = ctx->y_codes;
   p.y_scales = ctx->y_scales;

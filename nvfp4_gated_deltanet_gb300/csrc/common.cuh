@@ -484,7 +484,7 @@ struct PrefillArgs {
   uint16_t *conv_state;  // this slot's [K-1][C]
   void *ssm;             // this slot's [Hv][D][D], FP32 or BF16 bits (state_bf16)
   int state_bf16;
-  int scan_tc;           // chunk scan on warp-level tensor-core MMA (D = 128)
+  int scan_tc;           // chunk scan: 0 FP32 CUDA cores, 1 warp-level MMA, 2 tcgen05 (D = 128)
   const uint16_t *conv_w;
   const float *A_log, *dt_bias, *norm_w;
   int Hk, Hv, D, C, Kc;
@@ -495,12 +495,15 @@ struct PrefillArgs {
   float *W, *Ut;         // [Hv][nc][64][D]: per chunk T diag(beta e^Gamma) K and T diag(beta) V
   float *Am;             // [Hv][nc][64][64]: exp(Gamma_i - Gamma_j) q_i.k_j, j <= i
   float *Gam;            // [Hv][nc][64]: in-chunk cumulative log-decay
+  float *KT;             // [Hk][nc][D][64]: per chunk K^T (the tcgen05 chunk scan's operand), or null
   float *o;              // [T][Hv][D]
   uint8_t *y_codes;      // [T][Hv*D/2]
   uint8_t *y_scales;     // [T][Hv*D/16] row-major, or tiled when y_sf_tiled
   int y_sf_tiled;
   int32_t *status;
 };
+// The prefill chunk scan on tcgen05 (scan_tc.cu), d = 128; needs a.KT.
+cudaError_t launch_chunk_scan_umma(const PrefillArgs &a, cudaStream_t stream);
 // Block-scaled W4A4 GEMM on tcgen05: D[m][n] = W_hat[m][:] . X_hat[n][:],
 // stored C[n][m] (ldc). W = weights (A operand, M = 128 rows per tile), X =
 // activations (B operand). K % 256 == 0; row-major codes and scales.

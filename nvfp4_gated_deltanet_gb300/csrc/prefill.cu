@@ -220,6 +220,10 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
     gam[tid] = live ? a.gl[(size_t)h * a.Tp + t0 + tid] : 0.0f;
   }
   __syncthreads();
+  if (a.KT && h % (a.Hv / a.Hk) == 0) {  // K^T of the chunk, once per key head
+    float *kt = a.KT + ((size_t)kh * nc + c) * D * kC;
+    for (int e = tid; e < D * kC; e += 256) kt[e] = KR[(e % kC) * XLD + e / kC];
+  }
   if (tid == 0) {  // cumulative log-decay, in token order, from shared memory
     float acc = 0.0f;
     for (int i = 0; i < kC; ++i) {
@@ -742,7 +746,9 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
   }
   const int nc = a.Tp / kC;
   chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
-  if (D == 128 && a.scan_tc) {
+  if (D == 128 && a.scan_tc == 2) {
+    return launch_chunk_scan_umma(a, lc.stream);
+  } else if (D == 128 && a.scan_tc) {
     const size_t sm_tc = (size_t)(2 * kC * (D + 4) + kC * (D + 8) + kC * 40 + kC * (kC + 4) + kC + 32 * (D + 4) + 2 * kC * 33 +
                                   2 * kC * 40 + 2 * 32 * (D + 4)) * sizeof(float);
     static bool configured_tc = false;

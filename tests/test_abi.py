@@ -101,7 +101,7 @@ def test_tuning_knob_ranges(L):
     """Every knob takes its documented values and refuses the rest (GDN_E_RANGE
     = 6); each is put back to its default (0) afterwards."""
     valid = {0: (0, 1, 2), 1: (0, 1, 2, 4, 8), 2: (0, 1, 2, 4, 8), 3: (0, 1, 2), 4: (0, 1, 2), 5: (0, 1, 2),
-             6: (0, 1, 2), 7: (0, 1, 2, 4), 8: (0, 1, 2), 9: (0, 1, 2), 10: (0, 1, 2), 11: (0, 1, 2, 3),
+             6: (0, 1, 2), 7: (0, 1, 2, 4), 8: (0, 1, 2), 9: (0, 1, 2), 10: (0, 1, 2, 3), 11: (0, 1, 2, 3),
              13: (0, 1, 2), 14: (0, 1, 2, 3), 15: (0, 1, 2, 3), 16: (0, 1, 2)}
     try:
         for knob, values in valid.items():
