@@ -10,27 +10,30 @@
 //   U   = Ut - P_W,  Cf_j = e^(Gamma_64 - Gamma_j) u_j
 //   O   = diag(e^Gamma) P_Q + A U         M = 128 (rows past 64 unused), N = R, K = 64
 //   S^T <- e^Gamma_64 S^T + K^T Cf        M = 128 (d_k), N = R, K = 64
-// The state lives in the registers of the four epilogue warps, transposed:
-// thread e (TMEM lane e) holds S[r0 + r][e] for the slice's R rows, which is
-// exactly the lane of the update's accumulator, so no state element moves
-// between threads. Every product runs in split TF32: x = hi + lo and
-// a.b ~ lo.hi + hi.lo + hi.hi, accumulated in FP32, about 21 of FP32's 24
-// mantissa bits -- the arithmetic of the warp-level chunk scan, here as
-// tcgen05 MMAs reading both operands from shared memory (K-major, 128-byte
-// swizzle). For the operands the CTA computes (S, U, Cf), hi = TF32(x) and
-// lo = TF32(x - hi) by round-to-nearest; for the streamed chunk operands hi is
-// x itself read as TF32 (its low 13 bits dropped) and lo = x - trunc(x).
+// The state lives in the registers of the eight epilogue warps, transposed:
+// a thread of TMEM lane e holds S[r0 + r][e] for half of the slice's R rows,
+// exactly its lane and columns of the update's accumulator, so no state
+// element moves between threads. Every product runs in split TF32, x = hi + lo with
+// hi = TF32(x) and lo = TF32(x - hi) (round to nearest), as
+// a.b ~ hi.hi + lo.hi + hi.lo + lo.lo accumulated in FP32 -- at least the
+// 21-bit precision of the warp-level chunk scan. The A operand (the chunk's
+// 128-row tiles) sits in tensor memory as hi and lo columns; the B operand
+// (S, U, Cf: R rows) is [B_hi; B_lo], N = 2R, from shared memory (K-major,
+// 128-byte swizzle), so one K step is two MMAs (A_hi B'^T and A_lo B'^T) and
+// the epilogue adds the accumulator's two column halves.
 //
 // Warp roles (448 threads):
-//   warps 0..3   epilogue: TMEM -> registers, U / Cf / S operand tiles (split)
-//                into shared memory, outputs, the state
-//   warp 4       TMEM allocation; one thread issues the MMAs
-//   warp 5       one thread streams the chunk's [Q; W], A and K^T tiles by
-//                TMA (128-byte swizzle) into a ring of 32 KB slots, and asks
-//                L2 to prefetch the next chunk
-//   warps 6..13  write the lo part of each landed FP32 tile beside it (the
-//                tile itself is the hi part: the tensor core reads an FP32
-//                word as TF32 by dropping its 13 low mantissa bits)
+//   warps 0..7   epilogue (two per TMEM lane quarter, each half of the
+//                slice's rows): TMEM -> registers, U / Cf / S operand tiles
+//                (split) into shared memory, outputs, the state
+//   warp 8       TMEM allocation; one thread issues the MMAs
+//   warp 9       one thread streams the chunk's [Q; W], A and K^T tiles by
+//                TMA (128-byte swizzle) into a ring of 32 KB FP32 landing
+//                slots, and asks L2 to prefetch the next chunk
+//   warps 10..13 split each landed tile into hi and lo and store both into a
+//                tensor-memory slot (tcgen05.st), where the MMAs read their
+//                A operand: only the small B operands (S, U, Cf) are read from
+//                shared memory, once per MMA
 // Every mbarrier wait is bounded; a wait that gives up sets the status word
 // (GDN_E_TIMEOUT) and a shared abort flag that ends every role's loop.
 #include <cuda.h>
@@ -42,23 +45,28 @@ namespace gdn {
 namespace {
 
 constexpr int kC = 64, kD = 128;
-constexpr int kSlots = 5;                 // operand ring slots
-constexpr int kHalf = 128 * 128;          // bytes of one [128 rows][32 floats] tile
-constexpr int kSplitWarps = 8;
-constexpr int kScanThreads = 32 * (6 + kSplitWarps);
-constexpr int kUsesPerChunk = 7;          // ring uses: 4 of [Q; W], 1 of A (both halves), 2 of K^T
+constexpr int kLand = 5;                  // FP32 landing slots in shared memory
+constexpr int kLandBytes = 2 * 128 * 128; // two [128 rows][32 floats] sub-tiles
+constexpr int kTSlots = 2;                // A-operand slots in tensor memory
+constexpr int kTSlotCols = 128;           // hi: 64 columns (K = 64), lo: the next 64
+constexpr int kTSlot0 = 192;              // first slot column; accumulators below
+constexpr int kEpiWarps = 8;              // two per TMEM lane quarter
+constexpr int kSplitWarps = 4;            // one per TMEM lane quarter
+constexpr int kScanThreads = 32 * (kEpiWarps + 2 + kSplitWarps);
+constexpr int kUsesPerChunk = 4;          // [Q; W] d_k 0..63 and 64..127, A, K^T (K = 64 each)
 
 template <int R>
 struct ScanLayout {
   static constexpr int kSub = R * 128;                  // one [R][32 floats] sub-tile
-  static constexpr int kRing = kSlots * 2 * kHalf;      // hi + lo per slot
-  static constexpr int kS = 2 * 4 * kSub;               // S hi, lo: four d_k sub-tiles each
-  static constexpr int kU = 2 * 2 * kSub;               // U^T hi, lo: two token sub-tiles each
+  static constexpr int kRing = kLand * kLandBytes;
+  static constexpr int kS = 2 * 4 * kSub;               // S: per 32-wide d_k sub-tile, hi rows then lo rows
+  static constexpr int kU = 2 * 2 * kSub;               // U^T: per 32-token sub-tile, hi rows then lo rows
   static constexpr int kCf = kU;                        // Cf^T hi, lo
   static constexpr int kBars = 256;
   static constexpr int kBytes = 1024 + kRing + kS + kU + kCf + kBars;
   static_assert(kSub % 1024 == 0, "sub-tiles stay 1024-byte aligned");
   static_assert(kBytes <= 227 * 1024, "one CTA per SM");
+  static_assert(6 * R <= kTSlot0, "accumulators (2R columns each) below the A slots");
 };
 
 GDN_DEV uint32_t tf32_bits(float x) {
@@ -79,22 +87,37 @@ GDN_DEV uint32_t sw_off(int row, int col) {
 GDN_DEV uint32_t idesc_tf32(int n) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
-GDN_DEV void mma_tf32(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+GDN_DEV void mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// D (+)= A B^T in split precision over one 32-wide K sub-tile (four K = 8 steps):
-// lo.hi, hi.lo, hi.hi per step; `first` starts the accumulator.
-GDN_DEV void mma_split_sub(uint32_t d, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl, uint32_t idesc, bool first) {
+GDN_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+// D (+)= A B'^T over K = 64 (eight K = 8 steps) with A = hi + lo in tensor
+// memory (hi at column a, lo at a + 64) and B' = [B_hi; B_lo] from shared
+// memory (N = 2R rows: the hi rows, then the lo rows; b(j) gives the
+// descriptor of K step j): columns 0..R-1 of D collect hi.hi + lo.hi and
+// columns R..2R-1 hi.lo + lo.lo, which the epilogue adds -- the split
+// product in two MMAs per K step. `first` starts the accumulator.
+template <typename BD>
+GDN_DEV void mma_split_ts(uint32_t d, uint32_t a, BD b, uint32_t idesc, bool first) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    mma_tf32(d, al + 2 * k, bh + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
-    mma_tf32(d, ah + 2 * k, bl + 2 * k, idesc, 1u);
-    mma_tf32(d, ah + 2 * k, bh + 2 * k, idesc, 1u);
+  for (int j = 0; j < 8; ++j) {
+    const uint64_t bd = b(j);
+    mma_tf32_ts(d, a + 64 + 8 * j, bd, idesc, (first && j == 0) ? 0u : 1u);
+    mma_tf32_ts(d, a + 8 * j, bd, idesc, 1u);
   }
 }
 GDN_DEV void prefetch_l2(const void *p, uint32_t bytes) {
@@ -132,13 +155,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t *ring = sm;
-  uint8_t *sS = sm + L::kRing;           // S as [R][d_k]: hi sub-tiles 0..3, lo 4..7
-  uint8_t *sU = sS + L::kS;              // U^T as [R][token]: hi 0..1, lo 2..3
+  uint8_t *sS = sm + L::kRing;           // S as [R][d_k]: per d_k sub-tile q, hi at 2q, lo at 2q + 1
+  uint8_t *sU = sS + L::kS;              // U^T as [R][token]: per token sub-tile, hi then lo
   uint8_t *sCf = sU + L::kU;             // Cf^T, the same layout
   uint64_t *landed = reinterpret_cast<uint64_t *>(sCf + L::kCf);  // TMA -> splitters
-  uint64_t *full = landed + kSlots;                                  // splitters -> MMA
-  uint64_t *empty = full + kSlots;                                   // MMA -> TMA
-  uint64_t *s_ready = empty + kSlots, *p_done = s_ready + 1, *u_ready = s_ready + 2, *acc_done = s_ready + 3,
+  uint64_t *sfree = landed + kLand;                                  // splitters -> TMA
+  uint64_t *tfull = sfree + kLand;                                   // splitters -> MMA
+  uint64_t *tempty = tfull + kTSlots;                                // MMA -> splitters
+  uint64_t *s_ready = tempty + kTSlots, *p_done = s_ready + 1, *u_ready = s_ready + 2, *acc_done = s_ready + 3,
            *fin = s_ready + 4;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(s_ready + 5);
   volatile uint32_t *abort_flag = tmem_holder + 1;
@@ -149,26 +173,25 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int nc = a.Tp / kC;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // the second half of the A product reads 64 rows past its operand (rows
-  // whose products are never read); the ring starts zeroed so they are finite
-  for (int i = tid; i < L::kRing / 16; i += kScanThreads) reinterpret_cast<uint4 *>(ring)[i] = make_uint4(0, 0, 0, 0);
-  fence_async_shared();
   if (tid == 0) {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kLand; ++s) {
       mbar_init(landed + s, 1);
-      mbar_init(full + s, 32 * kSplitWarps);
-      mbar_init(empty + s, 1);
+      mbar_init(sfree + s, 32 * kSplitWarps);
     }
-    mbar_init(s_ready, 128);
+    for (int t = 0; t < kTSlots; ++t) {
+      mbar_init(tfull + t, 32 * kSplitWarps);
+      mbar_init(tempty + t, 1);
+    }
+    mbar_init(s_ready, 32 * kEpiWarps);
     mbar_init(p_done, 1);
-    mbar_init(u_ready, 128);
+    mbar_init(u_ready, 32 * kEpiWarps);
     mbar_init(acc_done, 1);
     mbar_init(fin, 1);
     *abort_flag = 0u;
     fence_barrier_init();
   }
-  if (warp == 4) {
-    tmem_alloc(tmem_holder, 128);
+  if (warp == kEpiWarps) {
+    tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -176,23 +199,27 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp < 4) {
-    // ------------------------------------------------ epilogue: thread e = TMEM lane e
-    const int e = tid;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float Sv[R];  // S[r0 + r][e]
+  if (warp < kEpiWarps) {
+    // ------------------------------------------------ epilogue: thread = TMEM lane e of its warp's
+    // quarter, and one half of the slice's rows (accumulator columns) hf
+    constexpr int RH = R / 2;
+    const int qt = warp & 3, hf = warp >> 2;
+    const int e = 32 * qt + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(qt * 32) << 16) + RH * hf;
+    float Sv[RH];  // S[r0 + RH hf + r][e]
 #pragma unroll
-    for (int r = 0; r < R; ++r) Sv[r] = state_load(a.ssm, a.state_bf16, ((size_t)h * kD + r0 + r) * kD + e);
+    for (int r = 0; r < RH; ++r)
+      Sv[r] = state_load(a.ssm, a.state_bf16, ((size_t)h * kD + r0 + RH * hf + r) * kD + e);
     bool ok = true;
     for (int c = 0; c < nc; ++c) {
-      // (a) S -> the B operand of P (thread e owns column e of every row)
+      // (a) S -> the B operand of P (thread e owns column e of its rows)
       {
-        uint8_t *hi = sS + warp * L::kSub, *lo = sS + (4 + warp) * L::kSub;
+        uint8_t *hi = sS + 2 * qt * L::kSub, *lo = hi + L::kSub;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
+        for (int r = 0; r < RH; ++r) {
           uint32_t vh, vl;
           split_hi_lo(Sv[r], vh, vl);
-          const uint32_t off = sw_off(r, lane);
+          const uint32_t off = sw_off(RH * hf + r, lane);
           *reinterpret_cast<uint32_t *>(hi + off) = vh;
           *reinterpret_cast<uint32_t *>(lo + off) = vl;
         }
@@ -205,10 +232,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       const float gi = gam[i], gC = gam[kC - 1];
       // (b) rows 64..127 of P are W S^T: U = Ut - W S^T and the update coefficients
       if (e >= 64) {
-        float ut[R];
-        const float4 *up = reinterpret_cast<const float4 *>(a.Ut + (((size_t)h * nc + c) * kC + i) * kD + r0);
+        float ut[RH];
+        const float4 *up = reinterpret_cast<const float4 *>(a.Ut + (((size_t)h * nc + c) * kC + i) * kD + r0 + RH * hf);
 #pragma unroll
-        for (int j = 0; j < R / 4; ++j) {
+        for (int j = 0; j < RH / 4; ++j) {
           const float4 v = up[j];
           ut[4 * j] = v.x; ut[4 * j + 1] = v.y; ut[4 * j + 2] = v.z; ut[4 * j + 3] = v.w;
         }
@@ -216,26 +243,23 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (!warp_wait(p_done, (uint32_t)(c & 1), abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
         const int sub = i >> 5, col = i & 31;
-        uint8_t *uh = sU + sub * L::kSub, *ul = sU + (2 + sub) * L::kSub;
-        uint8_t *ch = sCf + sub * L::kSub, *cl = sCf + (2 + sub) * L::kSub;
+        uint8_t *uh = sU + 2 * sub * L::kSub, *ul = uh + L::kSub;
+        uint8_t *ch = sCf + 2 * sub * L::kSub, *cl = ch + L::kSub;
+        uint32_t pr[RH], pr1[RH];
+        tmem_ld16(lane_base, pr);
+        tmem_ld16(lane_base + R, pr1);
+        tmem_ld_wait();
 #pragma unroll
-        for (int p0 = 0; p0 < R; p0 += 16) {
-          uint32_t pr[16];
-          tmem_ld16(lane_base + p0, pr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int r = p0 + k;
-            const float u = ut[r] - __uint_as_float(pr[k]);
-            const uint32_t off = sw_off(r, col);
-            uint32_t vh, vl;
-            split_hi_lo(u, vh, vl);
-            *reinterpret_cast<uint32_t *>(uh + off) = vh;
-            *reinterpret_cast<uint32_t *>(ul + off) = vl;
-            split_hi_lo(dc * u, vh, vl);
-            *reinterpret_cast<uint32_t *>(ch + off) = vh;
-            *reinterpret_cast<uint32_t *>(cl + off) = vl;
-          }
+        for (int k = 0; k < RH; ++k) {
+          const float u = ut[k] - (__uint_as_float(pr[k]) + __uint_as_float(pr1[k]));
+          const uint32_t off = sw_off(RH * hf + k, col);
+          uint32_t vh, vl;
+          split_hi_lo(u, vh, vl);
+          *reinterpret_cast<uint32_t *>(uh + off) = vh;
+          *reinterpret_cast<uint32_t *>(ul + off) = vl;
+          split_hi_lo(dc * u, vh, vl);
+          *reinterpret_cast<uint32_t *>(ch + off) = vh;
+          *reinterpret_cast<uint32_t *>(cl + off) = vl;
         }
         fence_async_shared();
       }
@@ -247,82 +271,83 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       if (e < 64) {
         const int t = c * kC + i;
         const float di = expf(gi);
-        float *op = a.o + ((size_t)t * a.Hv + h) * kD + r0;
+        uint32_t pq[RH], pq1[RH], oa[RH], oa1[RH];
+        tmem_ld16(lane_base, pq);
+        tmem_ld16(lane_base + R, pq1);
+        tmem_ld16(lane_base + 2 * R, oa);
+        tmem_ld16(lane_base + 3 * R, oa1);
+        tmem_ld_wait();
+        if (t < a.T) {
+          float *op = a.o + ((size_t)t * a.Hv + h) * kD + r0 + RH * hf;
+          float ov[RH];
 #pragma unroll
-        for (int p0 = 0; p0 < R; p0 += 16) {
-          uint32_t pq[16], oa[16];
-          tmem_ld16(lane_base + p0, pq);
-          tmem_ld16(lane_base + R + p0, oa);
-          tmem_ld_wait();
-          if (t < a.T) {
+          for (int k = 0; k < RH; ++k)
+            ov[k] = fmaf(di, __uint_as_float(pq[k]) + __uint_as_float(pq1[k]),
+                         __uint_as_float(oa[k]) + __uint_as_float(oa1[k]));
 #pragma unroll
-            for (int k = 0; k < 16; k += 4)
-              *reinterpret_cast<float4 *>(op + p0 + k) =
-                  make_float4(fmaf(di, __uint_as_float(pq[k]), __uint_as_float(oa[k])),
-                              fmaf(di, __uint_as_float(pq[k + 1]), __uint_as_float(oa[k + 1])),
-                              fmaf(di, __uint_as_float(pq[k + 2]), __uint_as_float(oa[k + 2])),
-                              fmaf(di, __uint_as_float(pq[k + 3]), __uint_as_float(oa[k + 3])));
-          }
+          for (int k = 0; k < RH; k += 4)
+            *reinterpret_cast<float4 *>(op + k) = make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
         }
       }
       const float dC = expf(gC);
-#pragma unroll
-      for (int p0 = 0; p0 < R; p0 += 16) {
-        uint32_t sa[16];
-        tmem_ld16(lane_base + 2 * R + p0, sa);
+      {
+        uint32_t sa[RH], sa1[RH];
+        tmem_ld16(lane_base + 4 * R, sa);
+        tmem_ld16(lane_base + 5 * R, sa1);
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) Sv[p0 + k] = fmaf(dC, Sv[p0 + k], __uint_as_float(sa[k]));
+        for (int k = 0; k < RH; ++k) Sv[k] = fmaf(dC, Sv[k], __uint_as_float(sa[k]) + __uint_as_float(sa1[k]));
       }
     }
     if (ok) {
 #pragma unroll
-      for (int r = 0; r < R; ++r) state_store(a.ssm, a.state_bf16, ((size_t)h * kD + r0 + r) * kD + e, Sv[r]);
+      for (int r = 0; r < RH; ++r)
+        state_store(a.ssm, a.state_bf16, ((size_t)h * kD + r0 + RH * hf + r) * kD + e, Sv[r]);
     }
-  } else if (warp == 4) {
+  } else if (warp == kEpiWarps) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_tf32(R);
+      const uint32_t idesc = idesc_tf32(2 * R);
+      const uint32_t bS = smem_u32(sS), bU = smem_u32(sU), bC = smem_u32(sCf);
       uint32_t u = 0;
       bool ok = true;
+      // use u: A operand in tensor-memory slot u % kTSlots, filled by the splitters
+      auto take = [&](uint32_t &col) -> bool {
+        const int t = (int)(u % kTSlots);
+        if (!wait_or_abort(tfull + t, (u / kTSlots) & 1u, abort_flag, a.status)) return false;
+        tc_fence_after();
+        col = tmem + kTSlot0 + t * kTSlotCols;
+        return true;
+      };
+      auto give = [&]() {
+        tc_commit(tempty + (u % kTSlots));
+        ++u;
+      };
       for (int c = 0; c < nc && ok; ++c) {
         if (!wait_or_abort(s_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
         tc_fence_after();
-        // P = [Q; W] S^T over four 32-wide d_k sub-tiles
-        for (int q = 0; q < 4; ++q, ++u) {
-          const int s = (int)(u % kSlots);
-          if (!wait_or_abort(full + s, (u / kSlots) & 1u, abort_flag, a.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(ring + s * 2 * kHalf);
-          const uint32_t sb = smem_u32(sS + q * L::kSub);
-          mma_split_sub(tmem, desc_sw128(sa), desc_sw128(sa + kHalf), desc_sw128(sb), desc_sw128(sb + 4 * L::kSub),
-                        idesc, q == 0);
-          tc_commit(empty + s);
+        // P = [Q; W] S^T: d_k 0..63, then 64..127 (S sub-tiles 2 i + j / 4)
+        for (int i = 0; i < 2; ++i) {
+          uint32_t acol;
+          if (!take(acol)) { ok = false; break; }
+          mma_split_ts(
+              tmem, acol, [&](int j) { return desc_sw128(bS + 2 * (2 * i + j / 4) * L::kSub) + 2 * (j & 3); }, idesc,
+              i == 0);
+          give();
         }
         if (!ok) break;
         tc_commit(p_done);
         if (!wait_or_abort(u_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
         tc_fence_after();
-        // O = A U (one slot: A's token halves as rows 0..63 and 64..127), then
-        // S_acc = K^T Cf (K^T in two token halves)
-        for (int q = 0; q < 3; ++q, ++u) {
-          const int s = (int)(u % kSlots);
-          if (!wait_or_abort(full + s, (u / kSlots) & 1u, abort_flag, a.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(ring + s * 2 * kHalf);
-          if (q == 0) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t ar = sa + hh * (64 * 128), sb = smem_u32(sU + hh * L::kSub);
-              mma_split_sub(tmem + R, desc_sw128(ar), desc_sw128(ar + kHalf), desc_sw128(sb),
-                            desc_sw128(sb + 2 * L::kSub), idesc, hh == 0);
-            }
-          } else {
-            const uint32_t sb = smem_u32(sCf + (q - 1) * L::kSub);
-            mma_split_sub(tmem + 2 * R, desc_sw128(sa), desc_sw128(sa + kHalf), desc_sw128(sb),
-                          desc_sw128(sb + 2 * L::kSub), idesc, q == 1);
-          }
-          tc_commit(empty + s);
+        // O = A U (A's rows in lanes 0..63), then S_acc = K^T Cf
+        for (int i = 0; i < 2; ++i) {
+          uint32_t acol;
+          if (!take(acol)) { ok = false; break; }
+          const uint32_t bb = i == 0 ? bU : bC;
+          mma_split_ts(
+              tmem + (i == 0 ? 2 * R : 4 * R), acol, [&](int j) { return desc_sw128(bb + 2 * (j / 4) * L::kSub) + 2 * (j & 3); },
+              idesc, true);
+          give();
         }
         if (!ok) break;
         tc_commit(acc_done);
@@ -331,13 +356,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       tc_commit(fin);
       mbar_wait(fin, 0u);
     }
-  } else if (warp == 5) {
+  } else if (warp == kEpiWarps + 1) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint32_t total = (uint32_t)nc * kUsesPerChunk;
       for (uint32_t u = 0; u < total; ++u) {
-        const int s = (int)(u % kSlots);
-        if (u >= (uint32_t)kSlots && !wait_or_abort(empty + s, ((u / kSlots) - 1u) & 1u, abort_flag, a.status)) break;
+        const int s = (int)(u % kLand);
+        if (u >= (uint32_t)kLand && !wait_or_abort(sfree + s, ((u / kLand) - 1u) & 1u, abort_flag, a.status)) break;
         const int c = (int)(u / kUsesPerChunk), q = (int)(u % kUsesPerChunk);
         if (q == 0 && c + 1 < nc) {  // the next chunk's operands and Ut rows into L2
           const int n = c + 1;
@@ -347,51 +372,66 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           prefetch_l2(a.KT + ((size_t)kh * nc + n) * kD * kC, kD * kC * 4);
           prefetch_l2(a.Ut + ((size_t)h * nc + n) * kC * kD, kC * kD * 4);
         }
-        uint8_t *hi = ring + s * 2 * kHalf;
-        mbar_arrive_expect_tx(landed + s, kHalf);
-        if (q < 4) {         // [Q; W], d_k columns 32 q .. 32 q + 31
-          tma_load_2d(hi, &tmQ, q * 128, kh * a.Tp + c * kC, landed + s);
-          tma_load_2d(hi + 64 * 128, &tmW, q * 128, (h * nc + c) * kC, landed + s);
-        } else if (q == 4) { // A, token halves as rows 0..63 and 64..127
-          tma_load_2d(hi, &tmA, 0, (h * nc + c) * kC, landed + s);
-          tma_load_2d(hi + 64 * 128, &tmA, 128, (h * nc + c) * kC, landed + s);
-        } else {             // K^T, tokens 32 (q - 5) .. + 31
-          tma_load_2d(hi, &tmKT, (q - 5) * 128, (kh * nc + c) * kD, landed + s);
+        // two [128 rows][32 floats] sub-tiles: K columns 0..31 and 32..63 of the use
+        uint8_t *d0 = ring + s * kLandBytes, *d1 = d0 + kLandBytes / 2;
+        mbar_arrive_expect_tx(landed + s, q == 2 ? kLandBytes / 2 : kLandBytes);
+        if (q < 2) {         // [Q; W], d_k columns 64 q .. 64 q + 63
+          const int yq = kh * a.Tp + c * kC, yw = (h * nc + c) * kC;
+          tma_load_2d(d0, &tmQ, 256 * q, yq, landed + s);
+          tma_load_2d(d0 + 64 * 128, &tmW, 256 * q, yw, landed + s);
+          tma_load_2d(d1, &tmQ, 256 * q + 128, yq, landed + s);
+          tma_load_2d(d1 + 64 * 128, &tmW, 256 * q + 128, yw, landed + s);
+        } else if (q == 2) { // A: 64 rows
+          tma_load_2d(d0, &tmA, 0, (h * nc + c) * kC, landed + s);
+          tma_load_2d(d1, &tmA, 128, (h * nc + c) * kC, landed + s);
+        } else {             // K^T: 128 rows of d_k
+          tma_load_2d(d0, &tmKT, 0, (kh * nc + c) * kD, landed + s);
+          tma_load_2d(d1, &tmKT, 128, (kh * nc + c) * kD, landed + s);
         }
       }
     }
   } else {
-    // ------------------------------------------------ splitters (warps 6..13)
-    // each thread takes the 16-byte pieces id = lt + 256 k of the slot's
-    // [128 rows][32 floats] tile (row id / 8, 16-byte chunk id % 8) and writes
-    // lo = x - trunc(x) at the same place of the lo tile
-    const int lt = tid - 192;
+    // ------------------------------------------------ splitters (one warp per TMEM lane quarter)
+    // thread = row m of the use (its TMEM lane); both 32-wide halves of the
+    // use's K columns in turn
+    const int qt = warp & 3;
+    const int m = 32 * qt + lane;
+    const uint32_t tlane = (uint32_t)(qt * 32) << 16;
     const uint32_t total = (uint32_t)nc * kUsesPerChunk;
     for (uint32_t u = 0; u < total; ++u) {
-      const int s = (int)(u % kSlots);
-      if (!warp_wait(landed + s, (u / kSlots) & 1u, abort_flag, a.status)) break;
-      uint8_t *hi = ring + s * 2 * kHalf, *lo = hi + kHalf;
+      const int s = (int)(u % kLand), t = (int)(u % kTSlots), q = (int)(u % kUsesPerChunk);
+      const bool live = !(q == 2 && m >= kC);  // A has 64 rows; lanes 64..127 of its slot are never read out
+      if (u >= (uint32_t)kTSlots && !warp_wait(tempty + t, ((u / kTSlots) - 1u) & 1u, abort_flag, a.status)) break;
+      if (!warp_wait(landed + s, (u / kLand) & 1u, abort_flag, a.status)) break;
+      if (live) {
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t vh[32], vl[32];
+          const uint8_t *src = ring + s * kLandBytes + hf * (kLandBytes / 2) + m * 128;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int id = lt + 256 * k, row = id >> 3, c4 = id & 7;
-        const uint32_t off = (uint32_t)(row * 128 + ((c4 ^ (row & 7)) << 4));
-        const float4 x = *reinterpret_cast<const float4 *>(hi + off);
-        uint4 vl;
-        vl.x = __float_as_uint(x.x - __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u));
-        vl.y = __float_as_uint(x.y - __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u));
-        vl.z = __float_as_uint(x.z - __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u));
-        vl.w = __float_as_uint(x.w - __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
-        *reinterpret_cast<uint4 *>(lo + off) = vl;
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 x = *reinterpret_cast<const float4 *>(src + ((c4 ^ (m & 7)) << 4));
+            split_hi_lo(x.x, vh[4 * c4], vl[4 * c4]);
+            split_hi_lo(x.y, vh[4 * c4 + 1], vl[4 * c4 + 1]);
+            split_hi_lo(x.z, vh[4 * c4 + 2], vl[4 * c4 + 2]);
+            split_hi_lo(x.w, vh[4 * c4 + 3], vl[4 * c4 + 3]);
+          }
+          const uint32_t col = tmem + tlane + kTSlot0 + t * kTSlotCols + 32 * hf;
+          tmem_st32(col, vh);
+          tmem_st32(col + 64, vl);
+        }
       }
-      fence_async_shared();
-      mbar_arrive(full + s);
+      mbar_arrive(sfree + s);  // the landing slot has been read
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(tfull + t);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kEpiWarps) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 512);
   }
 }
 
