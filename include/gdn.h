@@ -323,11 +323,13 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * gated norm + quantisation -- with bit-identical results (0 and 1 = never,
  * the default: the one mixing kernel, whose state streams through registers
  * when its grid exceeds two CTAs per SM, measured faster at every batch size;
- * 2 = always). knob 10: the prefill chunk scan's products (W S^T, Q S^T,
- * A U, the state update) in split TF32 (hi.hi + hi.lo + lo.hi): 0 = automatic
- * (tcgen05 MMAs with TMEM accumulators for d = 128, else FP32 on the CUDA
- * cores), 1 = FP32 on the CUDA cores, 2 = warp-level MMA (d = 128), 3 =
- * tcgen05 (d = 128); the three tensor-core forms agree to FP32 rounding. knob 11: tensor-core projections with
+ * 2 = always). knob 10: the prefill chunk stages' products -- K K^T and
+ * Q K^T per chunk, then the scan's W S^T, Q S^T, A U and state update -- in
+ * split precision: 0 = automatic (tcgen05 MMAs with TMEM accumulators for
+ * d = 128, else FP32 on the CUDA cores), 1 = the scan in FP32 on the CUDA
+ * cores, 2 = warp-level MMA in split TF32 (d = 128), 3 = tcgen05 (d = 128:
+ * K K^T, Q K^T in split FP16 of the unit-norm k and q, the scan in split
+ * TF32); the forms agree to FP32 rounding. knob 11: tensor-core projections with
  * 128-token activation tiles, tiled scales and BF16 output as one persistent
  * CTA per SM with two TMEM accumulators, so that the epilogue of one output
  * tile overlaps the MMAs of the next. Two forms: streaming (both operands

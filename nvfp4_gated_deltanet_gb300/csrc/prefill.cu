@@ -16,13 +16,16 @@
 //
 //   prep        (32 tokens, head)   conv + SiLU, q/k L2 norm, beta, g
 //   chunk_prep  (chunk, value head) k.k and q.k, the triangular solve, W, Ut
+//               (for d = 128 with the tcgen05 scan: k.k and q.k as one tcgen05
+//               product in split FP16, K^T of the chunk for the scan)
 //   chunk_scan  (value head, 32 rows of d_v), sequential over chunks: U, O,
-//               and the state slice, kept in shared memory across chunks
+//               and the state slice, kept on chip across chunks (scan_tc.cu:
+//               the tcgen05 form)
 //   gnorm       (token)             z-gated RMSNorm + NVFP4 quantisation of y
 //   conv_tail   (channel)           the slot's conv state after the last token
 // The chunk products run on warp-level tensor-core MMA in split TF32 (d = 128;
 // FP32 on the CUDA cores for the smaller head sizes and on request).
-#include "common.cuh"
+#include "tc.cuh"
 
 namespace gdn {
 
@@ -175,6 +178,74 @@ GDN_DEV void mma3(float (&d)[4], const float (&af)[4], const float (&bf)[2]) {
 }
 
 
+// (I + L) X = R by forward substitution, one column per thread (no barriers):
+// columns 0..D-1 give W (R = beta e^Gamma k), D..2D-1 give Ut (R = beta v).
+// All right-hand sides are loaded first; rows of L are read 4 at a time.
+// K and v rows in shared memory with row stride XLD; L strictly lower, rows
+// LLD floats apart (a multiple of 4). BLOCKED: in blocks of 16 rows -- the
+// block's own rows in order, then every later row takes the block's
+// contribution (independent rows, no dependent chain in the long update);
+// else row by row with four partial sums (the warp-MMA kernel's form, which
+// measured faster beside that kernel's other phases).
+template <int D, int XLD, int LLD = kC, bool BLOCKED = false>
+GDN_DEV void chunk_solve(const PrefillArgs &a, const float *KR, const float *VR, const float *Lm, const float *bek,
+                         const float *bet, int h, int c, int nc, int tid) {
+  if (tid < 2 * D) {
+    const int col = tid;
+    float X[kC];
+#pragma unroll
+    for (int i = 0; i < kC; ++i) X[i] = col < D ? bek[i] * KR[i * XLD + col] : bet[i] * VR[i * XLD + (col - D)];
+    if constexpr (BLOCKED) {
+#pragma unroll
+      for (int b0 = 0; b0 < kC; b0 += 16) {
+#pragma unroll
+        for (int i = b0 + 1; i < b0 + 16; ++i) {
+          float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+          for (int j = b0; j < i; j += 2) {
+            p0 = fmaf(Lm[i * LLD + j], X[j], p0);
+            if (j + 1 < i) p1 = fmaf(Lm[i * LLD + j + 1], X[j + 1], p1);
+          }
+          X[i] -= p0 + p1;
+        }
+#pragma unroll
+        for (int i = b0 + 16; i < kC; ++i) {
+          float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+          for (int j = b0; j < b0 + 16; j += 4) {
+            const float4 l = *reinterpret_cast<const float4 *>(Lm + i * LLD + j);
+            p0 = fmaf(l.x, X[j], p0);
+            p1 = fmaf(l.y, X[j + 1], p1);
+            p0 = fmaf(l.z, X[j + 2], p0);
+            p1 = fmaf(l.w, X[j + 3], p1);
+          }
+          X[i] -= p0 + p1;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 1; i < kC; ++i) {
+        // four independent partial sums shorten the dependent FMA chain 4x
+        float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+#pragma unroll
+        for (int j = 0; j + 3 < i; j += 4) {
+          const float4 l = *reinterpret_cast<const float4 *>(Lm + i * LLD + j);
+          p0 = fmaf(l.x, X[j], p0);
+          p1 = fmaf(l.y, X[j + 1], p1);
+          p2 = fmaf(l.z, X[j + 2], p2);
+          p3 = fmaf(l.w, X[j + 3], p3);
+        }
+#pragma unroll
+        for (int j = i & ~3; j < i; ++j) p0 = fmaf(Lm[i * LLD + j], X[j], p0);
+        X[i] = X[i] - ((p0 + p1) + (p2 + p3));
+      }
+    }
+    float *dst = (col < D ? a.W : a.Ut) + ((size_t)h * nc + c) * kC * D + (col < D ? col : col - D);
+#pragma unroll
+    for (int i = 0; i < kC; ++i) dst[(size_t)i * D] = X[i];
+  }
+}
+
 // ---------------------------------------------------------------- chunk_prep
 // 16-byte asynchronous copy global -> shared; zero-filled when !valid.
 GDN_DEV void cp_async16(void *dst, const void *src, bool valid) {
@@ -292,34 +363,209 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
   cp_async_wait_all();
   __syncthreads();
 
-  // (I + L) X = R by forward substitution, one column per thread (no barriers):
-  // columns 0..D-1 give W (R = beta e^Gamma k), D..2D-1 give Ut (R = beta v).
-  // All right-hand sides are loaded first; rows of L are read 4 at a time.
-  if (tid < 2 * D) {
-    const int col = tid;
-    float X[kC];
-#pragma unroll
-    for (int i = 0; i < kC; ++i) X[i] = col < D ? bek[i] * KR[i * XLD + col] : bet[i] * VR[i * XLD + (col - D)];
-#pragma unroll
-    for (int i = 1; i < kC; ++i) {
-      // four independent partial sums shorten the dependent FMA chain 4x
-      float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
-#pragma unroll
-      for (int j = 0; j + 3 < i; j += 4) {
-        const float4 l = *reinterpret_cast<const float4 *>(Lm + i * kC + j);
-        p0 = fmaf(l.x, X[j], p0);
-        p1 = fmaf(l.y, X[j + 1], p1);
-        p2 = fmaf(l.z, X[j + 2], p2);
-        p3 = fmaf(l.w, X[j + 3], p3);
-      }
-#pragma unroll
-      for (int j = i & ~3; j < i; ++j) p0 = fmaf(Lm[i * kC + j], X[j], p0);
-      X[i] = X[i] - ((p0 + p1) + (p2 + p3));
-    }
-    float *dst = (col < D ? a.W : a.Ut) + ((size_t)h * nc + c) * kC * D + (col < D ? col : col - D);
-#pragma unroll
-    for (int i = 0; i < kC; ++i) dst[(size_t)i * D] = X[i];
+  chunk_solve<D, XLD>(a, KR, VR, Lm, bek, bet, h, c, nc, tid);
+}
+
+// ---------------------------------------------------------------- chunk_prep on tcgen05
+// The same outputs as chunk_prep_kernel<128> (W, Ut, A, Gamma, and K^T for the
+// tcgen05 scan), with K K^T and Q K^T as one tcgen05 product in split FP16:
+// k and q are L2-normalised (|k_i| <= 1, |q_i| <= d^-1/2), so the fixed
+// power-of-two scales 2^12 (k) and 2^14 (q) keep every element below FP16's
+// largest value and every lo part x - FP16(x) of an element larger than 2^-12
+// normal; x = hi + lo then carries 22 significant bits and
+//   D = [K_hi; Q_hi] [K_hi; K_lo]^T + [K_lo; Q_lo] [K_hi; K_lo]^T
+// (M = 128, N = 128, K = 128; FP32 accumulators in tensor memory) gives in its
+// two column halves hi.hi + lo.hi and hi.lo + lo.lo of every k_i . k_j and
+// q_i . k_j, which the epilogue adds and scales back exactly (2^-24, 2^-26).
+// Operands are K-major with the 128-byte swizzle: per 64-wide d_k half a
+// [128 rows][64 FP16] sub-tile of 16 KB. After the product their 96 KB hold
+// K and v in FP32 and L for the substitution. 256 threads, two CTAs per SM.
+constexpr int kPrepSub = 128 * 128;           // one [128 rows][64 FP16] sub-tile
+constexpr int kPrepTile = 2 * kPrepSub;       // a 128 x 128 FP16 operand
+constexpr int kPrepSmem = 1024 + 3 * kPrepTile + 4 * kC * 4 + 64;
+
+GDN_DEV uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+// x = hi + lo in FP16 (x already scaled), four values
+GDN_DEV void split_h4(float4 x, uint2 &hi, uint2 &lo) {
+  const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
+  const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+  hi = make_uint2(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1));
+  lo = make_uint2(pack_h2(x.x - f0.x, x.y - f0.y), pack_h2(x.z - f1.x, x.w - f1.y));
+}
+GDN_DEV void mma_f16_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
+  constexpr int D = 128, XLD = D + 4;
+  constexpr int kLLD = kC + 4;  // L's row stride: a lane writes one row, 4-way bank spread
+  static_assert((2 * kC * XLD + kC * kLLD) * 4 <= 3 * kPrepTile, "K, v and L fit in the operand tiles");
+  extern __shared__ uint8_t smraw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  uint8_t *Ahi = sm, *Alo = sm + kPrepTile, *Bp = sm + 2 * kPrepTile;
+  // after the product: K, v (FP32, row stride XLD) and L in the same bytes
+  float *KR = reinterpret_cast<float *>(sm);
+  float *VR = KR + kC * XLD;
+  float *Lm = VR + kC * XLD;
+  float *gam = reinterpret_cast<float *>(sm + 3 * kPrepTile);
+  float *bet = gam + kC, *bek = bet + kC;
+  uint64_t *done = reinterpret_cast<uint64_t *>(bek + kC);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(done + 1);
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int kh = h / (a.Hv / a.Hk);
+  const int t0 = c * kC;
+  const int nc = a.Tp / kC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid < kC) {
+    const bool live = t0 + tid < a.T;
+    bet[tid] = live ? a.beta[(size_t)h * a.Tp + t0 + tid] : 0.0f;
+    gam[tid] = live ? a.gl[(size_t)h * a.Tp + t0 + tid] : 0.0f;
   }
+  if (tid == 0) {
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_holder, 128);
+    tmem_relinquish();
+  }
+  // k and q rows -> scaled FP16 hi / lo operand tiles; every load first
+  {
+    float4 x[8][2];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int idx = tid + 256 * k;         // 2048 eight-element pieces: k rows, then q rows
+      const int isq = idx >> 10, r = (idx >> 4) & 63, c8 = idx & 15;
+      const float *src = (isq ? a.qn : a.kn) + ((size_t)kh * a.Tp + t0 + r) * D + c8 * 8;
+      const bool live = t0 + r < a.T;
+      x[k][0] = live ? reinterpret_cast<const float4 *>(src)[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[k][1] = live ? reinterpret_cast<const float4 *>(src)[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int idx = tid + 256 * k;
+      const int isq = idx >> 10, r = (idx >> 4) & 63, c8 = idx & 15;
+      const float sc = isq ? 16384.0f : 4096.0f;
+      float4 v0 = x[k][0], v1 = x[k][1];
+      v0.x *= sc; v0.y *= sc; v0.z *= sc; v0.w *= sc;
+      v1.x *= sc; v1.y *= sc; v1.z *= sc; v1.w *= sc;
+      uint2 h0, l0, h1, l1;
+      split_h4(v0, h0, l0);
+      split_h4(v1, h1, l1);
+      const uint4 hv = make_uint4(h0.x, h0.y, h1.x, h1.y), lv = make_uint4(l0.x, l0.y, l1.x, l1.y);
+      const int sub = c8 >> 3, cc = c8 & 7;
+      const int row = isq * kC + r;
+      const uint32_t off = (uint32_t)(sub * kPrepSub + row * 128 + ((cc ^ (row & 7)) << 4));
+      *reinterpret_cast<uint4 *>(Ahi + off) = hv;
+      *reinterpret_cast<uint4 *>(Alo + off) = lv;
+      if (!isq) {  // B' = [K_hi; K_lo]: rows r and 64 + r (the same swizzle phase)
+        const uint32_t ob = (uint32_t)(sub * kPrepSub + r * 128 + ((cc ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4 *>(Bp + ob) = hv;
+        *reinterpret_cast<uint4 *>(Bp + ob + 64 * 128) = lv;
+      }
+    }
+  }
+  fence_async_shared();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  if (tid == 32) {  // the product: eight K = 16 steps, two MMAs each
+    const uint32_t idesc = (1u << 4) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t o = (uint32_t)((k >> 2) * kPrepSub + (k & 3) * 32);
+      const uint64_t bd = desc_sw128(smem_u32(Bp + o));
+      mma_f16_ss(tmem, desc_sw128(smem_u32(Ahi + o)), bd, idesc, k ? 1u : 0u);
+      mma_f16_ss(tmem, desc_sw128(smem_u32(Alo + o)), bd, idesc, 1u);
+    }
+    tc_commit(done);
+  }
+  if (tid == 0) {  // cumulative log-decay, in token order, while the product runs
+    float acc = 0.0f;
+    for (int i = 0; i < kC; ++i) {
+      acc += gam[i];
+      gam[i] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < kC) {
+    a.Gam[((size_t)h * nc + c) * kC + tid] = gam[tid];
+    bek[tid] = bet[tid] * expf(gam[tid]);
+  }
+  // one thread per warp waits; the warp follows it (collective TMEM loads)
+  const int ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(done, 0u) : 0, 0);
+  if (!ok && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+  tc_fence_after();
+  // the operand tiles are free: k and v (FP32) into them, L beside them
+  for (int e = tid; e < kC * D / 4; e += 256) {
+    const int i = (4 * e) / D, d = (4 * e) % D;
+    const bool live = t0 + i < a.T;
+    cp_async16(KR + i * XLD + d, a.kn + ((size_t)kh * a.Tp + t0 + i) * D + d, live);
+    cp_async16(VR + i * XLD + d, a.v + ((size_t)h * a.Tp + t0 + i) * D + d, live);
+  }
+  cp_async_commit();
+  // L (rows 0..63, k_i . k_j) and A (rows 64..127, q_i . k_j) from the
+  // accumulator: thread = row 32 (warp & 3) + lane, columns 32 (warp >> 2) ..
+  if (ok) {
+    const int qt = warp & 3, hf = warp >> 2;
+    const int m = 32 * qt + lane, j0 = 32 * hf;
+    const uint32_t tb = tmem + ((uint32_t)(qt * 32) << 16);
+    uint32_t d0[16], d1[16], e0[16], e1[16];
+    tmem_ld16(tb + j0, d0);
+    tmem_ld16(tb + j0 + 16, d1);
+    tmem_ld16(tb + 64 + j0, e0);
+    tmem_ld16(tb + 64 + j0 + 16, e1);
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      v[k] = __uint_as_float(d0[k]) + __uint_as_float(e0[k]);
+      v[16 + k] = __uint_as_float(d1[k]) + __uint_as_float(e1[k]);
+    }
+    if (m < kC) {
+      const int i = m;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int j = j0 + k;
+        Lm[i * kLLD + j] = j < i ? bet[i] * expf(gam[i] - gam[j]) * (v[k] * 0x1p-24f) : 0.0f;
+      }
+    } else {
+      const int i = m - kC;
+      float *Ag = a.Am + (((size_t)h * nc + c) * kC + i) * kC + j0;
+#pragma unroll
+      for (int k = 0; k < 32; k += 4) {
+        float w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = j0 + k + e;
+          w4[e] = j <= i ? expf(gam[i] - gam[j]) * (v[k + e] * 0x1p-26f) : 0.0f;
+        }
+        *reinterpret_cast<float4 *>(Ag + k) = make_float4(w4[0], w4[1], w4[2], w4[3]);
+      }
+    }
+  }
+  cp_async_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+  if (a.KT && h % (a.Hv / a.Hk) == 0) {  // K^T of the chunk, once per key head
+    float *kt = a.KT + ((size_t)kh * nc + c) * D * kC;
+    for (int e = tid; e < D * kC; e += 256) kt[e] = KR[(e % kC) * XLD + e / kC];
+  }
+  chunk_solve<D, XLD, kLLD, true>(a, KR, VR, Lm, bek, bet, h, c, nc, tid);
 }
 
 // ---------------------------------------------------------------- chunk_scan
@@ -745,10 +991,20 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
     configured = true;
   }
   const int nc = a.Tp / kC;
-  chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
-  if (D == 128 && a.scan_tc == 2) {
+  if (D == 128 && a.scan_tc == 2) {  // both chunk stages on tcgen05
+    static bool configured_p = false;
+    if (!configured_p) {
+      cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+      if (e != cudaSuccess) return e;
+      configured_p = true;
+    }
+    chunk_prep_tc_kernel<<<dim3(nc, a.Hv), 256, kPrepSmem, lc.stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     return launch_chunk_scan_umma(a, lc.stream);
-  } else if (D == 128 && a.scan_tc) {
+  }
+  chunk_prep_kernel<D><<<dim3(nc, a.Hv), 256, sm_prep, lc.stream>>>(a);
+  if (D == 128 && a.scan_tc) {
     const size_t sm_tc = (size_t)(2 * kC * (D + 4) + kC * (D + 8) + kC * 40 + kC * (kC + 4) + kC + 32 * (D + 4) + 2 * kC * 33 +
                                   2 * kC * 40 + 2 * 32 * (D + 4)) * sizeof(float);
     static bool configured_tc = false;
