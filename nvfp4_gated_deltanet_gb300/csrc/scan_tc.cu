@@ -69,11 +69,10 @@ struct ScanLayout {
   static_assert(6 * R <= kTSlot0, "accumulators (2R columns each) below the A slots");
 };
 
-GDN_DEV uint32_t tf32_bits(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+// TF32 rounding of x (nearest, ties away from zero) on the bit pattern: add
+// half a unit of the 13 dropped bits to the magnitude, then clear them -- two
+// integer operations instead of a conversion instruction of lower throughput.
+GDN_DEV uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
 GDN_DEV void split_hi_lo(float x, uint32_t &hi, uint32_t &lo) {
   hi = tf32_bits(x);
   lo = tf32_bits(x - __uint_as_float(hi));
