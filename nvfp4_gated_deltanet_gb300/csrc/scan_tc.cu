@@ -53,7 +53,7 @@ constexpr int kTSlot0 = 192;              // first slot column; accumulators bel
 constexpr int kEpiWarps = 8;              // two per TMEM lane quarter
 constexpr int kSplitWarps = 4;            // one per TMEM lane quarter
 constexpr int kScanThreads = 32 * (kEpiWarps + 2 + kSplitWarps);
-constexpr int kUsesPerChunk = 4;          // [Q; W] d_k 0..63 and 64..127, A, K^T (K = 64 each)
+constexpr int kUsesPerChunk = 4;          // [Q; W] d_k 0..63 and 64..127, K^T, A (K = 64 each)
 
 template <int R>
 struct ScanLayout {
@@ -161,9 +161,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   uint64_t *sfree = landed + kLand;                                  // splitters -> TMA
   uint64_t *tfull = sfree + kLand;                                   // splitters -> MMA
   uint64_t *tempty = tfull + kTSlots;                                // MMA -> splitters
-  uint64_t *s_ready = tempty + kTSlots, *p_done = s_ready + 1, *u_ready = s_ready + 2, *acc_done = s_ready + 3,
-           *fin = s_ready + 4;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(s_ready + 5);
+  // per chunk: S tile written (all epilogue warps) -> P = [Q; W] S^T done ->
+  // Cf tile written (W-row warps) -> state update product done; U tile
+  // written (W-row warps) and the previous chunk's output read (Q-row warps)
+  // -> A U done
+  uint64_t *s_ready = tempty + kTSlots, *p_done = s_ready + 1, *cf_ready = s_ready + 2, *s_acc_done = s_ready + 3,
+           *u_ready = s_ready + 4, *o_free = s_ready + 5, *o_done = s_ready + 6, *fin = s_ready + 7;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(s_ready + 8);
   volatile uint32_t *abort_flag = tmem_holder + 1;
 
   constexpr int NSL = kD / R;
@@ -183,8 +187,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
     mbar_init(s_ready, 32 * kEpiWarps);
     mbar_init(p_done, 1);
-    mbar_init(u_ready, 32 * kEpiWarps);
-    mbar_init(acc_done, 1);
+    mbar_init(cf_ready, 16 * kEpiWarps);
+    mbar_init(s_acc_done, 1);
+    mbar_init(u_ready, 16 * kEpiWarps);
+    mbar_init(o_free, 16 * kEpiWarps);
+    mbar_init(o_done, 1);
     mbar_init(fin, 1);
     *abort_flag = 0u;
     fence_barrier_init();
@@ -200,16 +207,42 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
   if (warp < kEpiWarps) {
     // ------------------------------------------------ epilogue: thread = TMEM lane e of its warp's
-    // quarter, and one half of the slice's rows (accumulator columns) hf
+    // quarter, and one half of the slice's rows (accumulator columns) hf.
+    // Lanes 0..63 are the q rows of P and of O, lanes 64..127 the W rows of P;
+    // every lane is d_k = e of the state update.
     constexpr int RH = R / 2;
     const int qt = warp & 3, hf = warp >> 2;
-    const int e = 32 * qt + lane;
+    const bool wrow = qt >= 2;
+    const int e = 32 * qt + lane, i = e & 63;
     const uint32_t lane_base = tmem + ((uint32_t)(qt * 32) << 16) + RH * hf;
     float Sv[RH];  // S[r0 + RH hf + r][e]
 #pragma unroll
     for (int r = 0; r < RH; ++r)
       Sv[r] = state_load(a.ssm, a.state_bf16, ((size_t)h * kD + r0 + RH * hf + r) * kD + e);
+    float pq[RH];  // q rows: e^Gamma_i (S q_i) of the chunk whose output is pending
     bool ok = true;
+    // q rows: the output of chunk cc = e^Gamma (S q) + A U, once A U is done
+    auto emit_o = [&](int cc) -> bool {
+      if (!warp_wait(o_done, (uint32_t)(cc & 1), abort_flag, a.status)) return false;
+      tc_fence_after();
+      uint32_t oa[RH], oa1[RH];
+      tmem_ld16(lane_base + 2 * R, oa);
+      tmem_ld16(lane_base + 3 * R, oa1);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(o_free);
+      const int t = cc * kC + i;
+      if (t < a.T) {
+        float *op = a.o + ((size_t)t * a.Hv + h) * kD + r0 + RH * hf;
+        float ov[RH];
+#pragma unroll
+        for (int k = 0; k < RH; ++k) ov[k] = pq[k] + (__uint_as_float(oa[k]) + __uint_as_float(oa1[k]));
+#pragma unroll
+        for (int k = 0; k < RH; k += 4)
+          *reinterpret_cast<float4 *>(op + k) = make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
+      }
+      return true;
+    };
     for (int c = 0; c < nc; ++c) {
       // (a) S -> the B operand of P (thread e owns column e of its rows)
       {
@@ -226,11 +259,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         tc_fence_before();
         mbar_arrive(s_ready);
       }
+      if (!wrow && c > 0 && !emit_o(c - 1)) { ok = false; break; }
       const float *gam = a.Gam + ((size_t)h * nc + c) * kC;
-      const int i = e & 63;
       const float gi = gam[i], gC = gam[kC - 1];
-      // (b) rows 64..127 of P are W S^T: U = Ut - W S^T and the update coefficients
-      if (e >= 64) {
+      if (wrow) {
+        // (b) W rows: U = Ut - W S^T, the update coefficients Cf = e^(Gamma_64 - Gamma_i) U
         float ut[RH];
         const float4 *up = reinterpret_cast<const float4 *>(a.Ut + (((size_t)h * nc + c) * kC + i) * kD + r0 + RH * hf);
 #pragma unroll
@@ -241,53 +274,56 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const float dc = expf(gC - gi);
         if (!warp_wait(p_done, (uint32_t)(c & 1), abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
+        uint32_t pr[RH], pr1[RH];
+        tmem_ld16(lane_base, pr);
+        tmem_ld16(lane_base + R, pr1);
+        tmem_ld_wait();
         const int sub = i >> 5, col = i & 31;
-        uint8_t *uh = sU + 2 * sub * L::kSub, *ul = uh + L::kSub;
-        uint8_t *ch = sCf + 2 * sub * L::kSub, *cl = ch + L::kSub;
+        float u[RH];
+#pragma unroll
+        for (int k = 0; k < RH; ++k) u[k] = ut[k] - (__uint_as_float(pr[k]) + __uint_as_float(pr1[k]));
+        {  // Cf first: the state update is the next chunk's dependency
+          uint8_t *ch = sCf + 2 * sub * L::kSub, *cl = ch + L::kSub;
+#pragma unroll
+          for (int k = 0; k < RH; ++k) {
+            uint32_t vh, vl;
+            split_hi_lo(dc * u[k], vh, vl);
+            const uint32_t off = sw_off(RH * hf + k, col);
+            *reinterpret_cast<uint32_t *>(ch + off) = vh;
+            *reinterpret_cast<uint32_t *>(cl + off) = vl;
+          }
+          fence_async_shared();
+          tc_fence_before();
+          mbar_arrive(cf_ready);
+        }
+        {
+          uint8_t *uh = sU + 2 * sub * L::kSub, *ul = uh + L::kSub;
+#pragma unroll
+          for (int k = 0; k < RH; ++k) {
+            uint32_t vh, vl;
+            split_hi_lo(u[k], vh, vl);
+            const uint32_t off = sw_off(RH * hf + k, col);
+            *reinterpret_cast<uint32_t *>(uh + off) = vh;
+            *reinterpret_cast<uint32_t *>(ul + off) = vl;
+          }
+          fence_async_shared();
+          mbar_arrive(u_ready);
+        }
+      } else {
+        // (b) q rows: e^Gamma_i (S q_i), kept until the chunk's A U is done
+        const float di = expf(gi);
+        if (!warp_wait(p_done, (uint32_t)(c & 1), abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
         uint32_t pr[RH], pr1[RH];
         tmem_ld16(lane_base, pr);
         tmem_ld16(lane_base + R, pr1);
         tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < RH; ++k) {
-          const float u = ut[k] - (__uint_as_float(pr[k]) + __uint_as_float(pr1[k]));
-          const uint32_t off = sw_off(RH * hf + k, col);
-          uint32_t vh, vl;
-          split_hi_lo(u, vh, vl);
-          *reinterpret_cast<uint32_t *>(uh + off) = vh;
-          *reinterpret_cast<uint32_t *>(ul + off) = vl;
-          split_hi_lo(dc * u, vh, vl);
-          *reinterpret_cast<uint32_t *>(ch + off) = vh;
-          *reinterpret_cast<uint32_t *>(cl + off) = vl;
-        }
-        fence_async_shared();
+        for (int k = 0; k < RH; ++k) pq[k] = di * (__uint_as_float(pr[k]) + __uint_as_float(pr1[k]));
       }
-      tc_fence_before();
-      mbar_arrive(u_ready);
-      // (c) outputs of rows 0..63 and the state update
-      if (!warp_wait(acc_done, (uint32_t)(c & 1), abort_flag, a.status)) { ok = false; break; }
+      // (c) the state update
+      if (!warp_wait(s_acc_done, (uint32_t)(c & 1), abort_flag, a.status)) { ok = false; break; }
       tc_fence_after();
-      if (e < 64) {
-        const int t = c * kC + i;
-        const float di = expf(gi);
-        uint32_t pq[RH], pq1[RH], oa[RH], oa1[RH];
-        tmem_ld16(lane_base, pq);
-        tmem_ld16(lane_base + R, pq1);
-        tmem_ld16(lane_base + 2 * R, oa);
-        tmem_ld16(lane_base + 3 * R, oa1);
-        tmem_ld_wait();
-        if (t < a.T) {
-          float *op = a.o + ((size_t)t * a.Hv + h) * kD + r0 + RH * hf;
-          float ov[RH];
-#pragma unroll
-          for (int k = 0; k < RH; ++k)
-            ov[k] = fmaf(di, __uint_as_float(pq[k]) + __uint_as_float(pq1[k]),
-                         __uint_as_float(oa[k]) + __uint_as_float(oa1[k]));
-#pragma unroll
-          for (int k = 0; k < RH; k += 4)
-            *reinterpret_cast<float4 *>(op + k) = make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
-        }
-      }
       const float dC = expf(gC);
       {
         uint32_t sa[RH], sa1[RH];
@@ -298,6 +334,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         for (int k = 0; k < RH; ++k) Sv[k] = fmaf(dC, Sv[k], __uint_as_float(sa[k]) + __uint_as_float(sa1[k]));
       }
     }
+    if (ok && !wrow && nc > 0 && !emit_o(nc - 1)) ok = false;
     if (ok) {
 #pragma unroll
       for (int r = 0; r < RH; ++r)
@@ -336,20 +373,31 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         if (!ok) break;
         tc_commit(p_done);
-        if (!wait_or_abort(u_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
+        // S_acc = K^T Cf (the next chunk's dependency), then O = A U (A's rows
+        // in lanes 0..63) once the q rows have read the previous O
+        if (!wait_or_abort(cf_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
         tc_fence_after();
-        // O = A U (A's rows in lanes 0..63), then S_acc = K^T Cf
-        for (int i = 0; i < 2; ++i) {
+        {
           uint32_t acol;
-          if (!take(acol)) { ok = false; break; }
-          const uint32_t bb = i == 0 ? bU : bC;
+          if (!take(acol)) break;
           mma_split_ts(
-              tmem + (i == 0 ? 2 * R : 4 * R), acol, [&](int j) { return desc_sw128(bb + 2 * (j / 4) * L::kSub) + 2 * (j & 3); },
-              idesc, true);
+              tmem + 4 * R, acol, [&](int j) { return desc_sw128(bC + 2 * (j / 4) * L::kSub) + 2 * (j & 3); }, idesc,
+              true);
           give();
         }
-        if (!ok) break;
-        tc_commit(acc_done);
+        tc_commit(s_acc_done);
+        if (!wait_or_abort(u_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
+        if (c > 0 && !wait_or_abort(o_free, (uint32_t)((c - 1) & 1), abort_flag, a.status)) break;
+        tc_fence_after();
+        {
+          uint32_t acol;
+          if (!take(acol)) break;
+          mma_split_ts(
+              tmem + 2 * R, acol, [&](int j) { return desc_sw128(bU + 2 * (j / 4) * L::kSub) + 2 * (j & 3); }, idesc,
+              true);
+          give();
+        }
+        tc_commit(o_done);
       }
       // every MMA issued has completed before the CTA may leave
       tc_commit(fin);
@@ -373,19 +421,19 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         // two [128 rows][32 floats] sub-tiles: K columns 0..31 and 32..63 of the use
         uint8_t *d0 = ring + s * kLandBytes, *d1 = d0 + kLandBytes / 2;
-        mbar_arrive_expect_tx(landed + s, q == 2 ? kLandBytes / 2 : kLandBytes);
+        mbar_arrive_expect_tx(landed + s, q == 3 ? kLandBytes / 2 : kLandBytes);
         if (q < 2) {         // [Q; W], d_k columns 64 q .. 64 q + 63
           const int yq = kh * a.Tp + c * kC, yw = (h * nc + c) * kC;
           tma_load_2d(d0, &tmQ, 256 * q, yq, landed + s);
           tma_load_2d(d0 + 64 * 128, &tmW, 256 * q, yw, landed + s);
           tma_load_2d(d1, &tmQ, 256 * q + 128, yq, landed + s);
           tma_load_2d(d1 + 64 * 128, &tmW, 256 * q + 128, yw, landed + s);
-        } else if (q == 2) { // A: 64 rows
-          tma_load_2d(d0, &tmA, 0, (h * nc + c) * kC, landed + s);
-          tma_load_2d(d1, &tmA, 128, (h * nc + c) * kC, landed + s);
-        } else {             // K^T: 128 rows of d_k
+        } else if (q == 2) { // K^T: 128 rows of d_k
           tma_load_2d(d0, &tmKT, 0, (kh * nc + c) * kD, landed + s);
           tma_load_2d(d1, &tmKT, 128, (kh * nc + c) * kD, landed + s);
+        } else {             // A: 64 rows
+          tma_load_2d(d0, &tmA, 0, (h * nc + c) * kC, landed + s);
+          tma_load_2d(d1, &tmA, 128, (h * nc + c) * kC, landed + s);
         }
       }
     }
@@ -399,7 +447,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const uint32_t total = (uint32_t)nc * kUsesPerChunk;
     for (uint32_t u = 0; u < total; ++u) {
       const int s = (int)(u % kLand), t = (int)(u % kTSlots), q = (int)(u % kUsesPerChunk);
-      const bool live = !(q == 2 && m >= kC);  // A has 64 rows; lanes 64..127 of its slot are never read out
+      const bool live = !(q == 3 && m >= kC);  // A has 64 rows; lanes 64..127 of its slot are never read out
       if (u >= (uint32_t)kTSlots && !warp_wait(tempty + t, ((u / kTSlots) - 1u) & 1u, abort_flag, a.status)) break;
       if (!warp_wait(landed + s, (u / kLand) & 1u, abort_flag, a.status)) break;
       if (live) {
