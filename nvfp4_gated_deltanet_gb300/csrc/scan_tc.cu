@@ -119,6 +119,25 @@ GDN_DEV void mma_split_ts(uint32_t d, uint32_t a, BD b, uint32_t idesc, bool fir
     mma_tf32_ts(d, a + 8 * j, bd, idesc, 1u);
   }
 }
+// The ring's use u in the MMA thread's order: chunk c consumes [Q; W] d_k
+// 0..63 and 64..127, then (from c = 1) the previous chunk's A, then its own
+// K^T; the last chunk's A comes last. kind: 0, 1 = [Q; W] halves, 2 = K^T,
+// 3 = A.
+GDN_DEV void ring_use(uint32_t u, int nc, int &kind, int &chunk) {
+  if (u < 3) {
+    kind = u < 2 ? (int)u : 2;
+    chunk = 0;
+    return;
+  }
+  const int c = 1 + (int)((u - 3) / 4), q = (int)((u - 3) % 4);
+  if (c == nc) {
+    kind = 3;
+    chunk = nc - 1;
+  } else {
+    kind = q < 2 ? q : (q == 2 ? 3 : 2);
+    chunk = q == 2 ? c - 1 : c;
+  }
+}
 GDN_DEV void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -296,6 +315,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           tc_fence_before();
           mbar_arrive(cf_ready);
         }
+        // the U tile is free once the previous chunk's A U is done
+        if (c > 0 && !warp_wait(o_done, (uint32_t)((c - 1) & 1), abort_flag, a.status)) { ok = false; break; }
         {
           uint8_t *uh = sU + 2 * sub * L::kSub, *ul = uh + L::kSub;
 #pragma unroll
@@ -359,6 +380,21 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         tc_commit(tempty + (u % kTSlots));
         ++u;
       };
+      // O = A U of chunk cc, once its U tile is written and the q rows have
+      // read chunk cc - 1's O
+      auto au = [&](int cc) -> bool {
+        if (!wait_or_abort(u_ready, (uint32_t)(cc & 1), abort_flag, a.status)) return false;
+        if (cc > 0 && !wait_or_abort(o_free, (uint32_t)((cc - 1) & 1), abort_flag, a.status)) return false;
+        tc_fence_after();
+        uint32_t acol;
+        if (!take(acol)) return false;
+        mma_split_ts(
+            tmem + 2 * R, acol, [&](int j) { return desc_sw128(bU + 2 * (j / 4) * L::kSub) + 2 * (j & 3); }, idesc,
+            true);
+        give();
+        tc_commit(o_done);
+        return true;
+      };
       for (int c = 0; c < nc && ok; ++c) {
         if (!wait_or_abort(s_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
         tc_fence_after();
@@ -373,8 +409,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         if (!ok) break;
         tc_commit(p_done);
-        // S_acc = K^T Cf (the next chunk's dependency), then O = A U (A's rows
-        // in lanes 0..63) once the q rows have read the previous O
+        // the previous chunk's O = A U (A's rows in lanes 0..63), while the
+        // W-row warps compute this chunk's Cf
+        if (c > 0 && !au(c - 1)) break;
+        // S_acc = K^T Cf: the next chunk's dependency
         if (!wait_or_abort(cf_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
         tc_fence_after();
         {
@@ -386,18 +424,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           give();
         }
         tc_commit(s_acc_done);
-        if (!wait_or_abort(u_ready, (uint32_t)(c & 1), abort_flag, a.status)) break;
-        if (c > 0 && !wait_or_abort(o_free, (uint32_t)((c - 1) & 1), abort_flag, a.status)) break;
-        tc_fence_after();
-        {
-          uint32_t acol;
-          if (!take(acol)) break;
-          mma_split_ts(
-              tmem + 2 * R, acol, [&](int j) { return desc_sw128(bU + 2 * (j / 4) * L::kSub) + 2 * (j & 3); }, idesc,
-              true);
-          give();
-        }
-        tc_commit(o_done);
+        if (c == nc - 1) au(c);
       }
       // every MMA issued has completed before the CTA may leave
       tc_commit(fin);
@@ -410,7 +437,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       for (uint32_t u = 0; u < total; ++u) {
         const int s = (int)(u % kLand);
         if (u >= (uint32_t)kLand && !wait_or_abort(sfree + s, ((u / kLand) - 1u) & 1u, abort_flag, a.status)) break;
-        const int c = (int)(u / kUsesPerChunk), q = (int)(u % kUsesPerChunk);
+        int q, c;
+        ring_use(u, nc, q, c);
         if (q == 0 && c + 1 < nc) {  // the next chunk's operands and Ut rows into L2
           const int n = c + 1;
           prefetch_l2(a.qn + ((size_t)kh * a.Tp + (size_t)n * kC) * kD, kC * kD * 4);
@@ -446,7 +474,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const uint32_t tlane = (uint32_t)(qt * 32) << 16;
     const uint32_t total = (uint32_t)nc * kUsesPerChunk;
     for (uint32_t u = 0; u < total; ++u) {
-      const int s = (int)(u % kLand), t = (int)(u % kTSlots), q = (int)(u % kUsesPerChunk);
+      const int s = (int)(u % kLand), t = (int)(u % kTSlots);
+      int q, cq;
+      ring_use(u, nc, q, cq);
       const bool live = !(q == 3 && m >= kC);  // A has 64 rows; lanes 64..127 of its slot are never read out
       if (u >= (uint32_t)kTSlots && !warp_wait(tempty + t, ((u / kTSlots) - 1u) & 1u, abort_flag, a.status)) break;
       if (!warp_wait(landed + s, (u / kLand) & 1u, abort_flag, a.status)) break;
