@@ -33,18 +33,18 @@ namespace {
 
 constexpr int kC = 64;  // chunk length
 
-// prep: one CTA (128 threads) per (32-token tile, group of D channels): the
+// prep: one CTA (128 threads) per (64-token tile, group of D channels): the
 // group is the q or k channels of one key head, or the v channels of one value
 // head; group index 2*Hk + Hv .. handles beta and g. The conv window (tile +
-// K-1 earlier tokens) is read once with 16-byte loads; q and k rows are
-// L2-normalised by one warp per token with lane-local sums over D/32
-// consecutive elements and the warp butterfly -- the decode kernel's order.
-constexpr int kPrepTT = 32;
+// K-1 earlier tokens) is read once with 16-byte loads; a warp takes a token:
+// conv + SiLU of its D channels straight from the window, then (q, k) the L2
+// norm with lane-local sums over D/32 consecutive elements and the warp
+// butterfly -- the decode kernel's order.
+constexpr int kPrepTT = 64;
 
 template <int D>
 __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
   __shared__ __align__(16) uint16_t win[kPrepTT + 3][D];
-  __shared__ __align__(16) float outv[kPrepTT][D + 4];  // rows 16-byte aligned for vector reads
   const int t0 = blockIdx.x * kPrepTT, grp = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ngrp = 2 * a.Hk + a.Hv;
@@ -86,51 +86,47 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
     }
   }
   __syncthreads();
-  // conv + SiLU: thread -> channel, loop over the tile's tokens
-  for (int c = tid; c < D; c += blockDim.x) {
-    float w[4];
+  // warp -> token, lane -> EPL consecutive channels: conv + SiLU straight from
+  // the window, then (q, k) the L2 norm with lane-local sums and the warp
+  // butterfly -- the decode kernel's order
+  constexpr int EPL = D / 32;
+  float w[EPL][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) w[j] = j < Kc ? bf16_bits_to_f32(a.conv_w[(size_t)(ch0 + c) * Kc + j]) : 0.0f;
-    for (int i = 0; i < kPrepTT; ++i) {
+  for (int e = 0; e < EPL; ++e)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[e][j] = j < Kc ? bf16_bits_to_f32(a.conv_w[(size_t)(ch0 + lane * EPL + e) * Kc + j]) : 0.0f;
+  const int nq = a.Hk;  // groups 0..Hk-1: q, Hk..2Hk-1: k, then v
+  const bool isq = grp < nq, isk = !isq && grp < 2 * nq;
+  float *dst = isq ? a.qn + ((size_t)grp * a.Tp) * D
+                   : isk ? a.kn + ((size_t)(grp - nq) * a.Tp) * D : a.v + ((size_t)(grp - 2 * nq) * a.Tp) * D;
+  for (int i = warp; i < kPrepTT; i += blockDim.x / 32) {
+    const int t = t0 + i;
+    float o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
       float pre = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (j < Kc) pre = fmaf(w[j], bf16_bits_to_f32(win[i + j][c]), pre);
-      outv[i][c] = siluf_(pre);
+        if (j < Kc) pre = fmaf(w[e][j], bf16_bits_to_f32(win[i + j][lane * EPL + e]), pre);
+      o[e] = siluf_(pre);
     }
-  }
-  __syncthreads();
-  const int nq = a.Hk;  // groups 0..Hk-1: q, Hk..2Hk-1: k, then v
-  if (grp < 2 * nq) {
-    const bool isq = grp < nq;
-    const int kh = isq ? grp : grp - nq;
-    float *dst = (isq ? a.qn : a.kn) + ((size_t)kh * a.Tp) * D;
-    constexpr int EPL = D / 32;
-    for (int i = warp; i < kPrepTT; i += blockDim.x / 32) {
-      const int t = t0 + i;
+    float r = 1.0f;
+    if (isq || isk) {
       float p = 0.0f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) p = fmaf(outv[i][lane * EPL + e], outv[i][lane * EPL + e], p);
+      for (int e = 0; e < EPL; ++e) p = fmaf(o[e], o[e], p);
       p = warp_sum(p);
-      const float r = isq ? (1.0f / sqrtf(p + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(p + a.l2_eps);
-      if (t < a.T) {
-        if constexpr (EPL == 4) {  // one 16-byte store per lane
-          const float4 o4 = *reinterpret_cast<const float4 *>(&outv[i][lane * 4]);
-          *reinterpret_cast<float4 *>(dst + (size_t)t * D + lane * 4) = make_float4(o4.x * r, o4.y * r, o4.z * r, o4.w * r);
-        } else {
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) dst[(size_t)t * D + lane * EPL + e] = outv[i][lane * EPL + e] * r;
-        }
-      }
+      r = isq ? (1.0f / sqrtf(p + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(p + a.l2_eps);
     }
-  } else {
-    const int h = grp - 2 * nq;
-    constexpr int V4 = D / 4;
-    for (int e = tid; e < kPrepTT * V4; e += blockDim.x) {
-      const int i = e / V4, c = 4 * (e % V4);
-      if (t0 + i < a.T)
-        *reinterpret_cast<float4 *>(a.v + ((size_t)h * a.Tp + t0 + i) * D + c) =
-            *reinterpret_cast<const float4 *>(&outv[i][c]);
+    if (t < a.T) {
+      float *row = dst + (size_t)t * D + lane * EPL;
+      if constexpr (EPL == 4) {  // one 16-byte store per lane
+        *reinterpret_cast<float4 *>(row) = (isq || isk) ? make_float4(o[0] * r, o[1] * r, o[2] * r, o[3] * r)
+                                                        : make_float4(o[0], o[1], o[2], o[3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) row[e] = (isq || isk) ? o[e] * r : o[e];
+      }
     }
   }
 }
