@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(512) chunk_scan_tc_kernel(PrefillArgs a) {
 }
 
 // one CTA per token; thread i owns 16-block i of y (head i / (D/16))
-__global__ void gnorm_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(256, 5) gnorm_kernel(PrefillArgs a) {
   const int t = blockIdx.x;
   const int D = a.D, vd = a.Hv * D;
   const int nblk = vd / 16;
@@ -915,41 +915,44 @@ __global__ void gnorm_kernel(PrefillArgs a) {
   const int h = i / per_head, e0 = (i % per_head) * 16;
   const float *op = a.o + ((size_t)t * a.Hv + h) * D + e0;
   const uint16_t *zp = a.proj + (size_t)t * a.ld + 2 * a.Hk * D + vd + h * D + e0;
-  float ov[16], zv[16], nw[16];
+  // o and the z bits first (z kept packed); the norm weight is read at use
+  float y[16];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {  // o rows and the norm weight are 64-byte aligned per 16-block
+  for (int q = 0; q < 4; ++q) {  // o rows are 64-byte aligned per 16-block
     const float4 o4 = reinterpret_cast<const float4 *>(op)[q];
-    const float4 w4 = reinterpret_cast<const float4 *>(a.norm_w + e0)[q];
-    ov[4 * q] = o4.x; ov[4 * q + 1] = o4.y; ov[4 * q + 2] = o4.z; ov[4 * q + 3] = o4.w;
-    nw[4 * q] = w4.x; nw[4 * q + 1] = w4.y; nw[4 * q + 2] = w4.z; nw[4 * q + 3] = w4.w;
+    y[4 * q] = o4.x; y[4 * q + 1] = o4.y; y[4 * q + 2] = o4.z; y[4 * q + 3] = o4.w;
   }
+  uint32_t zw[8];
   if (a.ld % 8 == 0) {  // z rows 16-byte aligned
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const uint4 z4 = reinterpret_cast<const uint4 *>(zp)[q];
-      const uint32_t w[4] = {z4.x, z4.y, z4.z, z4.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        zv[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
-        zv[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-      }
+      zw[4 * q] = z4.x; zw[4 * q + 1] = z4.y; zw[4 * q + 2] = z4.z; zw[4 * q + 3] = z4.w;
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) zv[k] = bf16_bits_to_f32(zp[k]);
+    for (int k = 0; k < 8; ++k) zw[k] = uint32_t(zp[2 * k]) | (uint32_t(zp[2 * k + 1]) << 16);
   }
   float p = 0.0f;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) p = fmaf(ov[k], ov[k], p);
+  for (int k = 0; k < 16; ++k) p = fmaf(y[k], y[k], p);
   // the head's 16-element group sums added in group order (as in decode)
   const int first = (threadIdx.x & 31) & ~(per_head - 1);
   float tot = 0.0f;
   for (int m = 0; m < per_head; ++m) tot += __shfl_sync(0xffffffffu, p, first + m);
   p = tot;
   const float rstd = 1.0f / sqrtf(p / (float)D + a.rms_eps);
-  float y[16];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) y[k] = ov[k] * rstd * nw[k] * siluf_(zv[k]);
+  for (int q = 0; q < 4; ++q) {  // the norm weight is 64-byte aligned per 16-block
+    const float4 w4 = reinterpret_cast<const float4 *>(a.norm_w + e0)[q];
+    const float nw[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = 4 * q + k;
+      const float zv = __uint_as_float((j & 1) ? (zw[j >> 1] & 0xFFFF0000u) : (zw[j >> 1] << 16));
+      y[j] = y[j] * rstd * nw[k] * siluf_(zv);
+    }
+  }
   uint32_t lo, hi, s;
   const bool ok = quant_block16(y, a.ts_out, inv6ts_of(a.ts_out), lo, hi, s);
   if ((int)threadIdx.x >= nblk) return;
