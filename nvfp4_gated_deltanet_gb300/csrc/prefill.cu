@@ -401,16 +401,20 @@ GDN_DEV void mma_f16_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t ide
 }
 
 __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
-  constexpr int D = 128, XLD = D + 4;
-  constexpr int kLLD = kC + 4;  // L's row stride: a lane writes one row, 4-way bank spread
-  static_assert((2 * kC * XLD + kC * kLLD) * 4 <= 3 * kPrepTile, "K, v and L fit in the operand tiles");
+  constexpr int D = 128;
+  constexpr int kLLD = kC + 4;  // row stride of L and of (I + L)^-1: a lane writes one row, 4-way bank spread
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t *Ahi = sm, *Alo = sm + kPrepTile, *Bp = sm + 2 * kPrepTile;
-  // after the product: K, v (FP32, row stride XLD) and L in the same bytes
-  float *KR = reinterpret_cast<float *>(sm);
-  float *VR = KR + kC * XLD;
-  float *Lm = VR + kC * XLD;
+  // after the first product the same bytes hold L, Z = (I + L)^-1, a scratch
+  // of three 16 x 16 blocks and Z as the split B operand [Z_hi; Z_lo] of the
+  // second product (two [128 rows][32 FP32] sub-tiles, 1024-byte aligned)
+  float *Lm = reinterpret_cast<float *>(sm);
+  float *Zm = Lm + kC * kLLD;
+  float *Mt = Zm + kC * kLLD;
+  uint8_t *Zb = sm + 38 * 1024;
+  static_assert(38 * 1024 >= (2 * kC * kLLD + 3 * 256) * 4 && 38 * 1024 + 2 * 128 * 128 <= 3 * kPrepTile,
+                "L, Z, the scratch and the B operand fit in the operand tiles");
   float *gam = reinterpret_cast<float *>(sm + 3 * kPrepTile);
   float *bet = gam + kC, *bek = bet + kC;
   uint64_t *done = reinterpret_cast<uint64_t *>(bek + kC);
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
     fence_barrier_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_holder, 128);
+    tmem_alloc(tmem_holder, 256);
     tmem_relinquish();
   }
   // k and q rows -> scaled FP16 hi / lo operand tiles; every load first
@@ -502,14 +506,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
   const int ok = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(done, 0u) : 0, 0);
   if (!ok && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
   tc_fence_after();
-  // the operand tiles are free: k and v (FP32) into them, L beside them
-  for (int e = tid; e < kC * D / 4; e += 256) {
-    const int i = (4 * e) / D, d = (4 * e) % D;
-    const bool live = t0 + i < a.T;
-    cp_async16(KR + i * XLD + d, a.kn + ((size_t)kh * a.Tp + t0 + i) * D + d, live);
-    cp_async16(VR + i * XLD + d, a.v + ((size_t)h * a.Tp + t0 + i) * D + d, live);
-  }
-  cp_async_commit();
   // L (rows 0..63, k_i . k_j) and A (rows 64..127, q_i . k_j) from the
   // accumulator: thread = row 32 (warp & 3) + lane, columns 32 (warp >> 2) ..
   if (ok) {
@@ -534,6 +530,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
       for (int k = 0; k < 32; ++k) {
         const int j = j0 + k;
         Lm[i * kLLD + j] = j < i ? bet[i] * expf(gam[i] - gam[j]) * (v[k] * 0x1p-24f) : 0.0f;
+        Zm[i * kLLD + j] = 0.0f;
       }
     } else {
       const int i = m - kC;
@@ -550,18 +547,126 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
       }
     }
   }
-  cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
+  // Z = (I + L)^-1 by 16 x 16 blocks: the diagonal blocks D_b by forward
+  // substitution (one column per thread), then Z_ib = -D_i sum_{k=b}^{i-1}
+  // L_ik Z_kb level by level (i - b = 1, 2, 3), from the equation
+  // (I + L) Z = I read block row by block row
+  if (tid < kC) {
+    const int b = tid >> 4, cc = tid & 15, o = 16 * b;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = r == cc ? 1.0f : 0.0f;
+#pragma unroll
+      for (int s2 = 0; s2 < r; ++s2) acc = fmaf(-Lm[(o + r) * kLLD + o + s2], x[s2], acc);
+      x[r] = acc;
+      Zm[(o + r) * kLLD + o + cc] = acc;
+    }
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int lv = 1; lv < 4; ++lv) {
+    const int nb = 4 - lv;
+    for (int e = tid; e < nb * 256; e += 256) {  // M = sum_k L_ik Z_kb
+      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15, i = b + lv;
+      float acc = 0.0f;
+      for (int k = b; k < i; ++k)
+#pragma unroll
+        for (int s2 = 0; s2 < 16; ++s2) acc = fmaf(Lm[(16 * i + r) * kLLD + 16 * k + s2], Zm[(16 * k + s2) * kLLD + 16 * b + cc], acc);
+      Mt[e] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += 256) {  // Z_ib = -D_i M
+      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15, i = b + lv;
+      float acc = 0.0f;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) acc = fmaf(Zm[(16 * i + r) * kLLD + 16 * i + t], Mt[(b << 8) + t * 16 + cc], acc);
+      Zm[(16 * i + r) * kLLD + 16 * b + cc] = -acc;
+    }
+    __syncthreads();
+  }
+  // Z as the B operand [Z_hi; Z_lo] (N = 128 rows: row n < 64 is Z_hi[n], row
+  // 64 + n is Z_lo[n]; K = the 64 tokens j in two 32-wide swizzled sub-tiles)
+  for (int e = tid; e < kC * kC; e += 256) {
+    const int n = e >> 6, j = e & 63;
+    uint32_t zh, zl;
+    split_hi_lo(Zm[n * kLLD + j], zh, zl);
+    uint8_t *sub = Zb + (j >> 5) * (128 * 128);
+    *reinterpret_cast<uint32_t *>(sub + sw_off(n, j & 31)) = zh;
+    *reinterpret_cast<uint32_t *>(sub + sw_off(64 + n, j & 31)) = zl;
+  }
+  fence_async_shared();
+  __syncthreads();
+  // [W | Ut]^T = R^T Z^T, R = [diag(beta e^Gamma) K | diag(beta) v], one
+  // 128-row part at a time: the part's R^T (lanes = d, columns = tokens j) as
+  // hi and lo in TMEM columns 128..255 (the MMAs' A operand), the product
+  // D[d][n] = R^T Z_hi^T | R^T Z_lo^T in columns 0..127, whose halves the
+  // epilogue adds. Tokens past T are zero.
+  {
+    const int qt = warp & 3, hf = warp >> 2;
+    const int d = 32 * qt + lane, j0 = 32 * hf;
+    const uint32_t tl = tmem + ((uint32_t)(qt * 32) << 16);
+    const uint32_t idesc = idesc_tf32(128);
+    const bool write_kt = a.KT && h % (a.Hv / a.Hk) == 0;
+#pragma unroll 1
+    for (int part = 0; part < 2; ++part) {
+      const float *src = part == 0 ? a.kn + ((size_t)kh * a.Tp + t0) * D : a.v + ((size_t)h * a.Tp + t0) * D;
+      float x[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int j = j0 + k;
+        x[k] = t0 + j < a.T ? src[(size_t)j * D + d] : 0.0f;
+      }
+      if (part == 0 && write_kt) {  // K^T of the chunk for the scan, once per key head
+        float4 *kt = reinterpret_cast<float4 *>(a.KT + (((size_t)kh * nc + c) * D + d) * kC + j0);
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) kt[k / 4] = make_float4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+      }
+      uint32_t xh[32], xl[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) split_hi_lo(x[k] * (part == 0 ? bek[j0 + k] : bet[j0 + k]), xh[k], xl[k]);
+      tmem_st32(tl + 128 + j0, xh);
+      tmem_st32(tl + 192 + j0, xl);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 32) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = desc_sw128(smem_u32(Zb + (kk >> 2) * (128 * 128))) + 2 * (kk & 3);
+          mma_tf32_ts(tmem, tmem + 192 + 8 * kk, bd, idesc, kk ? 1u : 0u);
+          mma_tf32_ts(tmem, tmem + 128 + 8 * kk, bd, idesc, 1u);
+        }
+        tc_commit(done);
+      }
+      const int ok2 = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(done, (uint32_t)(1 + part) & 1u) : 0, 0);
+      if (!ok2 && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+      tc_fence_after();
+      if (ok2) {
+        uint32_t p0[16], p1[16], q0[16], q1[16];
+        tmem_ld16(tl + j0, p0);
+        tmem_ld16(tl + j0 + 16, p1);
+        tmem_ld16(tl + 64 + j0, q0);
+        tmem_ld16(tl + 64 + j0 + 16, q1);
+        tmem_ld_wait();
+        float *dst = (part == 0 ? a.W : a.Ut) + (((size_t)h * nc + c) * kC + j0) * D + d;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          dst[(size_t)k * D] = __uint_as_float(p0[k]) + __uint_as_float(q0[k]);
+          dst[(size_t)(16 + k) * D] = __uint_as_float(p1[k]) + __uint_as_float(q1[k]);
+        }
+      }
+      tc_fence_before();
+      __syncthreads();  // the accumulator and the A columns are read before the next part
+    }
+  }
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
-  if (a.KT && h % (a.Hv / a.Hk) == 0) {  // K^T of the chunk, once per key head
-    float *kt = a.KT + ((size_t)kh * nc + c) * D * kC;
-    for (int e = tid; e < D * kC; e += 256) kt[e] = KR[(e % kC) * XLD + e / kC];
-  }
-  chunk_solve<D, XLD, kLLD, true>(a, KR, VR, Lm, bek, bet, h, c, nc, tid);
 }
 
 // ---------------------------------------------------------------- chunk_scan

@@ -69,41 +69,6 @@ struct ScanLayout {
   static_assert(6 * R <= kTSlot0, "accumulators (2R columns each) below the A slots");
 };
 
-// TF32 rounding of x (nearest, ties away from zero) on the bit pattern: add
-// half a unit of the 13 dropped bits to the magnitude, then clear them -- two
-// integer operations instead of a conversion instruction of lower throughput.
-GDN_DEV uint32_t tf32_bits(float x) { return (__float_as_uint(x) + 0x1000u) & 0xFFFFE000u; }
-GDN_DEV void split_hi_lo(float x, uint32_t &hi, uint32_t &lo) {
-  hi = tf32_bits(x);
-  lo = tf32_bits(x - __uint_as_float(hi));
-}
-// byte offset of element (row, col) in a [rows][32 floats] tile, 128-byte swizzle
-GDN_DEV uint32_t sw_off(int row, int col) {
-  return (uint32_t)(row * 128 + ((((col >> 2) ^ (row & 7)) << 4) | ((col & 3) << 2)));
-}
-// Instruction descriptor of kind::tf32: FP32 accumulator, TF32 A and B, both
-// K-major, M = 128, N = n.
-GDN_DEV uint32_t idesc_tf32(int n) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-GDN_DEV void mma_tf32_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-GDN_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 // D (+)= A B'^T over K = 64 (eight K = 8 steps) with A = hi + lo in tensor
 // memory (hi at column a, lo at a + 64) and B' = [B_hi; B_lo] from shared
 // memory (N = 2R rows: the hi rows, then the lo rows; b(j) gives the
