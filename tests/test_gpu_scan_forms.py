@@ -69,3 +69,36 @@ def test_tcgen05_scan_matches_oracle_from_state(api):
     want = oracle_layer("FULL", 1).prefill(x, c, s, init_zero=False)
     assert rel_l2(_bf(out), _bf(want)) <= 2e-3
     assert rel_l2(st, s) <= 2e-3
+
+
+@pytest.mark.parametrize("pattern", ["constant", "alternating"])
+def test_chunk_forms_on_repeated_tokens(api, pattern):
+    """Prompts of one repeated token (every key the same, so L is as large as
+    it gets: L_ij = beta_i e^(Gamma_i - Gamma_j)) or of two alternating
+    tokens: the tcgen05 chunk stages (W and U~ from an explicit (I + L)^-1)
+    against the forward substitution of the warp-MMA form and against the
+    oracle's token recurrence."""
+    shape = synth.FULL
+    T = 200
+    base = synth.x_tokens(shape, 7, 2)
+    x = np.stack([base[0] if (pattern == "constant" or t % 2 == 0) else base[1] for t in range(T)])
+    L = api.lib()
+    outs = {}
+    try:
+        for form in (3, 2):
+            assert L.gdn_set_tuning(10, form) == 0
+            layer = api.layer_from_synth(weights("FULL", 1), max_batch=1, max_prefill_tokens=T)
+            conv_d, ssm_d = layer.new_states(2)
+            ssm_d[1].copy_(to_dev(synth.ssm_state(shape, 7)))
+            o = to_host(layer.prefill(to_dev(x), 1, False, conv_d, ssm_d))
+            assert layer.check() == 0
+            outs[form] = (o, to_host(ssm_d)[1].copy())
+    finally:
+        L.gdn_set_tuning(10, 0)
+    assert rel_l2(_bf(outs[3][0]), _bf(outs[2][0])) <= 1e-3
+    assert rel_l2(outs[3][1], outs[2][1]) <= 1e-5
+    c = np.zeros((shape.conv_kernel - 1, shape.conv_channels), np.uint16)
+    s = synth.ssm_state(shape, 7).copy()
+    want = oracle_layer("FULL", 1).prefill(x, c, s, init_zero=False)
+    assert rel_l2(_bf(outs[3][0]), _bf(want)) <= 2e-3
+    assert rel_l2(outs[3][1], s) <= 2e-3
