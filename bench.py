@@ -701,23 +701,21 @@ def main():
                          "achieved_gbs": round(gbs, 1), "frac": round(gbs / peaks()[0], 4)}
     dom = max(stages, key=stages.get)
 
-    # ---- e2e: the Python API with host buffers, copies inside the timed region
-    import numpy as np
+    # ---- e2e: the Python API with host buffers, copies inside the timed region:
+    # the layer stack's c1 step as one graph (DecodeStackGraph), x of every
+    # layer from pinned host memory in, every layer's output back
+    from nvfp4_gated_deltanet_gb300.graphs import DecodeStackGraph
     xh = torch.empty(n_layers, 1, layers[0].H, dtype=torch.int16).pin_memory()
     xh.copy_(xd[:1].cpu().expand(n_layers, 1, -1))
     oh = torch.empty(n_layers, 1, layers[0].H, dtype=torch.int16).pin_memory()
-    xdev = torch.empty_like(xh, device="cuda")
-    odev = torch.empty_like(oh, device="cuda")
-    ids = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sg = DecodeStackGraph(layers, states, 1)
     e2e_steps = max(5, args.steps // 10)
     for it in range(e2e_steps + 2):
         if it == 2:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        xdev.copy_(xh, non_blocking=True)
-        for i, (L, (c, m)) in enumerate(zip(layers, states)):
-            L.decode_step(xdev[i], ids, c, m, out=odev[i])
-        oh.copy_(odev, non_blocking=True)
+        out = sg.step(xh)
+        oh.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
     e2e_us = (time.perf_counter() - t0) / e2e_steps * 1e6 / n_layers
 
@@ -800,7 +798,7 @@ def main():
                      "kernels": kernels},
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": int(xh.numel() * 2),
                 "d2h_bytes_per_step": int(oh.numel() * 2),
-                "path": "GatedDeltaNetLayer.decode_step (ctypes -> C ABI), pinned host x in / out back, eager launches"},
+                "path": "DecodeStackGraph (one CUDA graph of every layer's gdn_decode_step through the C ABI), pinned host x in / out back"},
         "gpu_launches": 3 * n_layers * args.steps,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,

@@ -59,3 +59,43 @@ class DecodeGraphs:
             self.slot_ids[n:B].fill_(-1)
         self.replay(B)
         return self.out[:n]
+
+
+class DecodeStackGraph:
+    """One CUDA graph of a decode step through several layers (each with its
+    own weights and states), for a fixed row count B: layer i reads x[i] and
+    writes out[i]. A step is: write x (e.g. from pinned host memory), replay,
+    read out -- one graph launch instead of three kernel launches per layer
+    from the host, as in a served stack whose per-bucket graph holds every
+    layer."""
+
+    def __init__(self, layers, states, B: int, device="cuda"):
+        self.layers, self.states, self.B = list(layers), list(states), B
+        H = self.layers[0].H
+        n = len(self.layers)
+        self.x = torch.zeros(n, B, H, dtype=torch.int16, device=device)
+        self.out = torch.zeros(n, B, H, dtype=torch.int16, device=device)
+        self.slot_ids = torch.arange(B, dtype=torch.int32, device=device)
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):  # warm-up launch outside capture
+            self._launch()
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._launch()
+        torch.cuda.synchronize()
+
+    def _launch(self):
+        for i, (L, (c, m)) in enumerate(zip(self.layers, self.states)):
+            L.decode_step(self.x[i], self.slot_ids, c, m, out=self.out[i])
+
+    def replay(self):
+        self.graph.replay()
+
+    def step(self, x: torch.Tensor) -> torch.Tensor:
+        """x [n_layers][B][H] (any device; copied without a host sync) -> out."""
+        self.x.copy_(x, non_blocking=True)
+        self.replay()
+        return self.out

@@ -109,3 +109,34 @@ def test_negative_control_wrong_slot_changes_hash(setup):
         torch.cuda.synchronize()
         res.append(_hashes(graphs.out[:1], conv_d, ssm_d))
     assert res[0][0] != res[1][0] and res[0][2] != res[1][2]
+
+
+def test_stack_graph_equals_eager_steps():
+    """DecodeStackGraph (one graph of several layers' decode steps, each layer
+    with its own weights and states) gives bit-identically the outputs and
+    states of the same steps launched one by one, over two steps."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import nvfp4_gated_deltanet_gb300 as pkg
+    from nvfp4_gated_deltanet_gb300.graphs import DecodeStackGraph
+    n, B = 3, 2
+    layers = [pkg.layer_from_synth(weights("TINY", 0), max_batch=4) for _ in range(n)]
+    x, conv0, ssm0 = slot_inputs(synth.TINY, list(range(B)), 2)
+    st_g = [(to_dev(conv0), to_dev(ssm0)) for _ in range(n)]
+    st_e = [(to_dev(conv0), to_dev(ssm0)) for _ in range(n)]
+    sg = DecodeStackGraph(layers, st_g, B)
+    # the capture's warm-up launch stepped the graph states once from zero
+    # input rows; put them back
+    for (c, m) in st_g:
+        c.copy_(to_dev(conv0))
+        m.copy_(to_dev(ssm0))
+    ids = torch.arange(B, dtype=torch.int32, device="cuda")
+    for step in range(2):
+        xs = torch.stack([to_dev(x[step]) for _ in range(n)])
+        got = sg.step(xs).clone()
+        for i, (L, (c, m)) in enumerate(zip(layers, st_e)):
+            want = L.decode_step(xs[i], ids, c, m)
+            np.testing.assert_array_equal(to_host(got[i]), to_host(want))
+    for (cg, mg), (ce, me) in zip(st_g, st_e):
+        np.testing.assert_array_equal(to_host(cg), to_host(ce))
+        np.testing.assert_array_equal(to_host(mg), to_host(me))
