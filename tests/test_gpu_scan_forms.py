@@ -44,7 +44,7 @@ def _prefill(api, shape_name, T, form):
         L.gdn_set_tuning(10, 0)
 
 
-@pytest.mark.parametrize("shape_name,T", [("FULL", 333), ("FULL", 1024), ("TP2", 130)])
+@pytest.mark.parametrize("shape_name,T", [("FULL", 1), ("FULL", 64), ("FULL", 333), ("FULL", 1024), ("TP2", 130)])
 def test_scan_forms_agree(api, shape_name, T):
     o3, s3 = _prefill(api, shape_name, T, 3)
     o2, s2 = _prefill(api, shape_name, T, 2)
