@@ -328,8 +328,8 @@ gdn_status gdn_decode_step_static(const gdn_config *cfg, const gdn_weights *w, c
  * split precision: 0 = automatic (tcgen05 MMAs with TMEM accumulators for
  * d = 128, else FP32 on the CUDA cores), 1 = the scan in FP32 on the CUDA
  * cores, 2 = warp-level MMA in split TF32 (d = 128), 3 = tcgen05 (d = 128:
- * K K^T, Q K^T in split FP16 of the unit-norm k and q, the scan in split
- * TF32); the forms agree to FP32 rounding. knob 11: tensor-core projections with
+ * K K^T, Q K^T and the scan's products in split FP16 with power-of-two
+ * block scales); the forms agree to FP32 rounding. knob 11: tensor-core projections with
  * 128-token activation tiles, tiled scales and BF16 output as one persistent
  * CTA per SM with two TMEM accumulators, so that the epilogue of one output
  * tile overlaps the MMAs of the next. Two forms: streaming (both operands

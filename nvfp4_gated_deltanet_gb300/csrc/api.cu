@@ -24,7 +24,10 @@ struct gdn_ctx {
   float *qn, *kn, *v, *beta, *gl, *o;     // prefill intermediates (head-major, chunk-padded)
   BatchWs bws;                          // large-batch decode intermediates, max_batch rows
   float *W, *Ut, *Am, *Gam;               // per (value head, 64-token chunk) products
-  float *KT = nullptr;                    // per (key head, chunk) K^T for the tcgen05 chunk scan
+  uint16_t *KTs = nullptr;                // per (key head, chunk) K^T for the tcgen05 chunk scan, split FP16
+  uint16_t *Qs = nullptr;                 // q for the tcgen05 chunk scan, split FP16
+  float *Wsc = nullptr;                   // per (value head, chunk) FP16 scale of W
+  float *Umax = nullptr;                  // per (value head, chunk) largest |Ut|
   uint16_t *conv_tmp;                   // [K-1][C]
   uint8_t *xq_codes, *xq_scales;        // [prow][H/2] and tiled scales: x as NVFP4 for the tensor-core GEMM
   uint8_t *w_in_sf_t, *w_out_sf_t;      // the weights' scales in the tiled layout tcgen05.cp reads
@@ -584,7 +587,10 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Ut, Tp * Hv * D);
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Am, Tp * Hv * 64);
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Gam, Tp * Hv);
-    if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->KT, Tp * Hk * D);
+    if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->KTs, 2 * Tp * Hk * D);
+    if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->Qs, 2 * Tp * Hk * D);
+    if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->Wsc, Tp / 64 * Hv);
+    if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->Umax, Tp / 64 * Hv);
   }
   // weights into the kernels' layout: [qkvz; ba] as one matrix for one pass over x
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->w_in_codes, w->qkvz.codes, Nqkvz * H / 2, cudaMemcpyDeviceToDevice, s);
@@ -940,7 +946,13 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.Ut = ctx->Ut;
   p.Am = ctx->Am;
   p.Gam = ctx->Gam;
-  p.KT = p.scan_tc == 2 ? ctx->KT : nullptr;
+  // the tcgen05 path writes its split W and A over the FP32 ones (same bytes)
+  p.Qs = p.scan_tc == 2 ? ctx->Qs : nullptr;
+  p.Ws = p.scan_tc == 2 ? reinterpret_cast<uint16_t *>(ctx->W) : nullptr;
+  p.As = p.scan_tc == 2 ? reinterpret_cast<uint16_t *>(ctx->Am) : nullptr;
+  p.KTs = p.scan_tc == 2 ? ctx->KTs : nullptr;
+  p.Wsc = p.scan_tc == 2 ? ctx->Wsc : nullptr;
+  p.Umax = p.scan_tc == 2 ? ctx->Umax : nullptr;
   p.o = ctx->o;
   p.y_codes = ctx->y_codes;
   p.y_scales = ctx->y_scales;

@@ -495,7 +495,14 @@ struct PrefillArgs {
   float *W, *Ut;         // [Hv][nc][64][D]: per chunk T diag(beta e^Gamma) K and T diag(beta) V
   float *Am;             // [Hv][nc][64][64]: exp(Gamma_i - Gamma_j) q_i.k_j, j <= i
   float *Gam;            // [Hv][nc][64]: in-chunk cumulative log-decay
-  float *KT;             // [Hk][nc][D][64]: per chunk K^T (the tcgen05 chunk scan's operand), or null
+  // The tcgen05 chunk scan's operands in split FP16, x s = hi + lo with a
+  // power-of-two scale s (the hi block first, the lo block after it), or null:
+  uint16_t *Qs;          // [2][Hk][Tp][D]: q, s = 2^14
+  uint16_t *Ws;          // [2][Hv][Tp][D]: W, s = Wsc of its chunk (may alias W)
+  uint16_t *As;          // [2][Hv][Tp][64]: A, s = 2^14 (may alias Am)
+  uint16_t *KTs;         // [2][Hk][nc][D][64]: per chunk K^T, s = 2^14
+  float *Wsc;            // [Hv][nc]: power-of-two scale of each chunk's W
+  float *Umax;           // [Hv][nc]: largest |Ut| of each chunk
   float *o;              // [T][Hv][D]
   uint8_t *y_codes;      // [T][Hv*D/2]
   uint8_t *y_scales;     // [T][Hv*D/16] row-major, or tiled when y_sf_tiled

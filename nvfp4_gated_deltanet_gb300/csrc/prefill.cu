@@ -287,10 +287,6 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
     gam[tid] = live ? a.gl[(size_t)h * a.Tp + t0 + tid] : 0.0f;
   }
   __syncthreads();
-  if (a.KT && h % (a.Hv / a.Hk) == 0) {  // K^T of the chunk, once per key head
-    float *kt = a.KT + ((size_t)kh * nc + c) * D * kC;
-    for (int e = tid; e < D * kC; e += 256) kt[e] = KR[(e % kC) * XLD + e / kC];
-  }
   if (tid == 0) {  // cumulative log-decay, in token order, from shared memory
     float acc = 0.0f;
     for (int i = 0; i < kC; ++i) {
@@ -363,8 +359,10 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- chunk_prep on tcgen05
-// The same outputs as chunk_prep_kernel<128> (W, Ut, A, Gamma, and K^T for the
-// tcgen05 scan), with K K^T and Q K^T as one tcgen05 product in split FP16:
+// The products of chunk_prep_kernel<128> (Ut and Gamma in FP32; W and A, and q
+// and K^T, as the tcgen05 scan's split FP16 operands x s = hi + lo -- W with a
+// power-of-two scale per chunk from its largest |W|, the rest 2^14), with
+// K K^T and Q K^T as one tcgen05 product in split FP16:
 // k and q are L2-normalised (|k_i| <= 1, |q_i| <= d^-1/2), so the fixed
 // power-of-two scales 2^12 (k) and 2^14 (q) keep every element below FP16's
 // largest value and every lo part x - FP16(x) of an element larger than 2^-12
@@ -419,11 +417,13 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
   float *bet = gam + kC, *bek = bet + kC;
   uint64_t *done = reinterpret_cast<uint64_t *>(bek + kC);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(done + 1);
+  __shared__ float wred[8];
   const int c = blockIdx.x, h = blockIdx.y;
   const int kh = h / (a.Hv / a.Hk);
   const int t0 = c * kC;
   const int nc = a.Tp / kC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid < 8) wred[tid] = 0.0f;
 
   if (tid < kC) {
     const bool live = t0 + tid < a.T;
@@ -438,6 +438,8 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
     tmem_alloc(tmem_holder, 256);
     tmem_relinquish();
   }
+  // one CTA per key head writes the scan's q and K^T operands
+  const bool write_q = h % (a.Hv / a.Hk) == 0;
   // k and q rows -> scaled FP16 hi / lo operand tiles; every load first
   {
     float4 x[8][2];
@@ -467,6 +469,11 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
       const uint32_t off = (uint32_t)(sub * kPrepSub + row * 128 + ((cc ^ (row & 7)) << 4));
       *reinterpret_cast<uint4 *>(Ahi + off) = hv;
       *reinterpret_cast<uint4 *>(Alo + off) = lv;
+      if (isq && write_q) {  // the scan's q operand (the same split), once per key head
+        uint16_t *qs = a.Qs + ((size_t)kh * a.Tp + t0 + r) * D + c8 * 8;
+        *reinterpret_cast<uint4 *>(qs) = hv;
+        *reinterpret_cast<uint4 *>(qs + (size_t)a.Hk * a.Tp * D) = lv;
+      }
       if (!isq) {  // B' = [K_hi; K_lo]: rows r and 64 + r (the same swizzle phase)
         const uint32_t ob = (uint32_t)(sub * kPrepSub + r * 128 + ((cc ^ (r & 7)) << 4));
         *reinterpret_cast<uint4 *>(Bp + ob) = hv;
@@ -533,17 +540,22 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
         Zm[i * kLLD + j] = 0.0f;
       }
     } else {
+      // A 2^14 = e^(Gamma_i - Gamma_j) (q_i . k_j 2^26) 2^-12, split for the scan
       const int i = m - kC;
-      float *Ag = a.Am + (((size_t)h * nc + c) * kC + i) * kC + j0;
+      uint16_t *Ag = a.As + ((size_t)h * a.Tp + t0 + i) * kC + j0;
+      uint32_t hw[16], lw[16];
 #pragma unroll
-      for (int k = 0; k < 32; k += 4) {
-        float w4[4];
+      for (int k = 0; k < 32; k += 2) {
+        const int j = j0 + k;
+        const float x0 = j <= i ? expf(gam[i] - gam[j]) * (v[k] * 0x1p-12f) : 0.0f;
+        const float x1 = j + 1 <= i ? expf(gam[i] - gam[j + 1]) * (v[k + 1] * 0x1p-12f) : 0.0f;
+        split_f16x2(x0, x1, hw[k / 2], lw[k / 2]);
+      }
+      uint4 *gh = reinterpret_cast<uint4 *>(Ag), *gl = reinterpret_cast<uint4 *>(Ag + (size_t)a.Hv * a.Tp * kC);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = j0 + k + e;
-          w4[e] = j <= i ? expf(gam[i] - gam[j]) * (v[k + e] * 0x1p-26f) : 0.0f;
-        }
-        *reinterpret_cast<float4 *>(Ag + k) = make_float4(w4[0], w4[1], w4[2], w4[3]);
+      for (int k = 0; k < 4; ++k) {
+        gh[k] = make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+        gl[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
       }
     }
   }
@@ -609,7 +621,6 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
     const int d = 32 * qt + lane, j0 = 32 * hf;
     const uint32_t tl = tmem + ((uint32_t)(qt * 32) << 16);
     const uint32_t idesc = idesc_tf32(128);
-    const bool write_kt = a.KT && h % (a.Hv / a.Hk) == 0;
 #pragma unroll 1
     for (int part = 0; part < 2; ++part) {
       const float *src = part == 0 ? a.kn + ((size_t)kh * a.Tp + t0) * D : a.v + ((size_t)h * a.Tp + t0) * D;
@@ -619,10 +630,17 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
         const int j = j0 + k;
         x[k] = t0 + j < a.T ? src[(size_t)j * D + d] : 0.0f;
       }
-      if (part == 0 && write_kt) {  // K^T of the chunk for the scan, once per key head
-        float4 *kt = reinterpret_cast<float4 *>(a.KT + (((size_t)kh * nc + c) * D + d) * kC + j0);
+      if (part == 0 && write_q) {  // K^T 2^14 of the chunk, split, for the scan
+        uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) kt[k / 4] = make_float4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+        for (int k = 0; k < 32; k += 2) split_f16x2(x[k] * 16384.0f, x[k + 1] * 16384.0f, hw[k / 2], lw[k / 2]);
+        uint16_t *kt = a.KTs + (((size_t)kh * nc + c) * D + d) * kC + j0;
+        uint4 *gh = reinterpret_cast<uint4 *>(kt), *gl = reinterpret_cast<uint4 *>(kt + (size_t)a.Hk * nc * D * kC);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          gh[k] = make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+          gl[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+        }
       }
       uint32_t xh[32], xl[32];
 #pragma unroll
@@ -645,6 +663,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
       const int ok2 = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(done, (uint32_t)(1 + part) & 1u) : 0, 0);
       if (!ok2 && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
       tc_fence_after();
+      float wv[32];  // W (part 0): tokens j0 + k, kept until the chunk's largest |W| is known
       if (ok2) {
         uint32_t p0[16], p1[16], q0[16], q1[16];
         tmem_ld16(tl + j0, p0);
@@ -652,15 +671,48 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
         tmem_ld16(tl + 64 + j0, q0);
         tmem_ld16(tl + 64 + j0 + 16, q1);
         tmem_ld_wait();
-        float *dst = (part == 0 ? a.W : a.Ut) + (((size_t)h * nc + c) * kC + j0) * D + d;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          dst[(size_t)k * D] = __uint_as_float(p0[k]) + __uint_as_float(q0[k]);
-          dst[(size_t)(16 + k) * D] = __uint_as_float(p1[k]) + __uint_as_float(q1[k]);
+          wv[k] = __uint_as_float(p0[k]) + __uint_as_float(q0[k]);
+          wv[16 + k] = __uint_as_float(p1[k]) + __uint_as_float(q1[k]);
         }
+        if (part == 1) {
+          float *dst = a.Ut + (((size_t)h * nc + c) * kC + j0) * D + d;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) dst[(size_t)k * D] = wv[k];
+        }
+        // the chunk's largest |W| (its split scale) or |Ut| (the scan's bound on |U|)
+        float mx = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fabsf(wv[k]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) wred[warp] = mx;
       }
       tc_fence_before();
       __syncthreads();  // the accumulator and the A columns are read before the next part
+      if (part == 1 && tid == 0) {
+        float m = wred[0];
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, wred[w]);
+        a.Umax[(size_t)h * nc + c] = m;
+      }
+      if (part == 0 && ok2) {  // W s = hi + lo, s from the chunk's largest |W|
+        float m = wred[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, wred[w]);
+        const float sw = fp16_scale_for(m);
+        if (tid == 0) a.Wsc[(size_t)h * nc + c] = sw;
+        uint16_t *wh = a.Ws + ((size_t)h * a.Tp + t0 + j0) * D + d, *wl = wh + (size_t)a.Hv * a.Tp * D;
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          uint32_t hi, lo;
+          split_f16x2(wv[k] * sw, wv[k + 1] * sw, hi, lo);
+          wh[(size_t)k * D] = (uint16_t)hi;
+          wh[(size_t)(k + 1) * D] = (uint16_t)(hi >> 16);
+          wl[(size_t)k * D] = (uint16_t)lo;
+          wl[(size_t)(k + 1) * D] = (uint16_t)(lo >> 16);
+        }
+      }
     }
   }
   if (warp == 0) {
@@ -1096,6 +1148,7 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
   }
   const int nc = a.Tp / kC;
   if (D == 128 && a.scan_tc == 2) {  // both chunk stages on tcgen05
+    if (!a.Qs || !a.Ws || !a.As || !a.KTs || !a.Wsc || !a.Umax) return cudaErrorInvalidValue;
     static bool configured_p = false;
     if (!configured_p) {
       cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);

@@ -100,6 +100,29 @@ GDN_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// ---------------------------------------------------------------- split FP16 on tcgen05
+// Power-of-two scale s for a block whose largest magnitude is m: m s < 2^14,
+// so every scaled value and its FP16 hi part stay far below FP16's largest
+// finite value (65504), and the lo part x s - FP16(x s) of any element above
+// 2^-11 m is a normal FP16 number (22 significant bits in hi + lo). s is at
+// most 2^60 (m below 2^-47, or 0), so that the product of two inverse scales
+// stays a normal FP32 number. s and 1 / s are exact.
+GDN_DEV float fp16_scale_for(float m) {
+  const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu);  // biased exponent of m
+  const int p = min(140 - e, 60);                            // m s = 2^13 (1.f) for e >= 80
+  return __uint_as_float((uint32_t)(p + 127) << 23);
+}
+// x0, x1 (already scaled) -> FP16 hi and lo pairs (x0 in the low halves)
+GDN_DEV void split_f16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(x1), "f"(x0));
+  const __half2 hh = *reinterpret_cast<const __half2 *>(&h);
+  const float2 f = __half22float2(hh);
+  uint32_t l;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(l) : "f"(x1 - f.y), "f"(x0 - f.x));
+  hi = h;
+  lo = l;
+}
 // 2-D byte tensor [rows][row_bytes] (row stride = row_bytes), box
 // [box_rows][box_bytes], optionally with the 128-byte swizzle (host side).
 bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t row_bytes, uint32_t box_rows,

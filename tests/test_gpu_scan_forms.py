@@ -1,6 +1,6 @@
 """The three forms of the prefill chunk stages (tuning knob 10) compute the
 same chunk recurrence: tcgen05 MMAs with TMEM accumulators (the default for
-d = 128; K K^T and Q K^T in split FP16, the scan in split TF32), warp-level
+d = 128; every product in split FP16 with power-of-two block scales), warp-level
 MMA in split TF32, and FP32 on the CUDA cores. They must agree to FP32
 rounding on ragged prompts from a non-zero state, and the tcgen05 form must
 match the oracle's token recurrence on its own."""
