@@ -404,14 +404,14 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t *Ahi = sm, *Alo = sm + kPrepTile, *Bp = sm + 2 * kPrepTile;
-  // after the first product the same bytes hold L, Z = (I + L)^-1, a scratch
-  // of three 16 x 16 blocks and Z as the split B operand [Z_hi; Z_lo] of the
+  // after the first product the same bytes hold L, Z = (I + L)^-1, a 16 x 8
+  // scratch per warp and Z as the split B operand [Z_hi; Z_lo] of the
   // second product (two [128 rows][32 FP32] sub-tiles, 1024-byte aligned)
   float *Lm = reinterpret_cast<float *>(sm);
   float *Zm = Lm + kC * kLLD;
   float *Mt = Zm + kC * kLLD;
   uint8_t *Zb = sm + 38 * 1024;
-  static_assert(38 * 1024 >= (2 * kC * kLLD + 3 * 256) * 4 && 38 * 1024 + 2 * 128 * 128 <= 3 * kPrepTile,
+  static_assert(38 * 1024 >= (2 * kC * kLLD + 8 * 128) * 4 && 38 * 1024 + 2 * 128 * 128 <= 3 * kPrepTile,
                 "L, Z, the scratch and the B operand fit in the operand tiles");
   float *gam = reinterpret_cast<float *>(sm + 3 * kPrepTile);
   float *bet = gam + kC, *bek = bet + kC;
@@ -534,10 +534,14 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
     if (m < kC) {
       const int i = m;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int j = j0 + k;
-        Lm[i * kLLD + j] = j < i ? bet[i] * expf(gam[i] - gam[j]) * (v[k] * 0x1p-24f) : 0.0f;
-        Zm[i * kLLD + j] = 0.0f;
+      for (int k = 0; k < 32; k += 4) {
+        float l4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = j0 + k + e;
+          l4[e] = j < i ? bet[i] * expf(gam[i] - gam[j]) * (v[k + e] * 0x1p-24f) : 0.0f;
+        }
+        *reinterpret_cast<float4 *>(Lm + i * kLLD + j0 + k) = make_float4(l4[0], l4[1], l4[2], l4[3]);
       }
     } else {
       // A 2^14 = e^(Gamma_i - Gamma_j) (q_i . k_j 2^26) 2^-12, split for the scan
@@ -564,7 +568,8 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
   // Z = (I + L)^-1 by 16 x 16 blocks: the diagonal blocks D_b by forward
   // substitution (one column per thread), then Z_ib = -D_i sum_{k=b}^{i-1}
   // L_ik Z_kb level by level (i - b = 1, 2, 3), from the equation
-  // (I + L) Z = I read block row by block row
+  // (I + L) Z = I read block row by block row. Blocks above the diagonal are
+  // zero and never written.
   if (tid < kC) {
     const int b = tid >> 4, cc = tid & 15, o = 16 * b;
     float x[16];
@@ -578,33 +583,52 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
     }
   }
   __syncthreads();
+  // a level's blocks on split-TF32 warp MMA: warp w takes block b = w / 2,
+  // columns 8 (w & 1) .. + 7 of it, while b < 4 - lv; M = sum_k L_ik Z_kb
+  // (16 x 8) goes through the warp's scratch into B fragments of -D_i M
+  {
+    const int g = lane >> 2, t = lane & 3;
+    float *Ms = Mt + warp * 128;
 #pragma unroll 1
-  for (int lv = 1; lv < 4; ++lv) {
-    const int nb = 4 - lv;
-    for (int e = tid; e < nb * 256; e += 256) {  // M = sum_k L_ik Z_kb
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15, i = b + lv;
-      float acc = 0.0f;
-      for (int k = b; k < i; ++k)
+    for (int lv = 1; lv < 4; ++lv) {
+      const int b = warp >> 1;
+      if (b < 4 - lv) {
+        const int i = b + lv, cb = 16 * b + 8 * (warp & 1), ri = 16 * i;
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int kc = 16 * b; kc < ri; kc += 8) {
+          const float af[4] = {Lm[(ri + g) * kLLD + kc + t], Lm[(ri + g + 8) * kLLD + kc + t],
+                               Lm[(ri + g) * kLLD + kc + t + 4], Lm[(ri + g + 8) * kLLD + kc + t + 4]};
+          const float bf[2] = {Zm[(kc + t) * kLLD + cb + g], Zm[(kc + t + 4) * kLLD + cb + g]};
+          mma3(d, af, bf);
+        }
+        Ms[g * 8 + 2 * t] = d[0];
+        Ms[g * 8 + 2 * t + 1] = d[1];
+        Ms[(g + 8) * 8 + 2 * t] = d[2];
+        Ms[(g + 8) * 8 + 2 * t + 1] = d[3];
+        __syncwarp();
+        float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2) acc = fmaf(Lm[(16 * i + r) * kLLD + 16 * k + s2], Zm[(16 * k + s2) * kLLD + 16 * b + cc], acc);
-      Mt[e] = acc;
+        for (int s2 = 0; s2 < 16; s2 += 8) {
+          const float af[4] = {Zm[(ri + g) * kLLD + ri + s2 + t], Zm[(ri + g + 8) * kLLD + ri + s2 + t],
+                               Zm[(ri + g) * kLLD + ri + s2 + t + 4], Zm[(ri + g + 8) * kLLD + ri + s2 + t + 4]};
+          const float bf[2] = {Ms[(s2 + t) * 8 + g], Ms[(s2 + t + 4) * 8 + g]};
+          mma3(z, af, bf);
+        }
+        Zm[(ri + g) * kLLD + cb + 2 * t] = -z[0];
+        Zm[(ri + g) * kLLD + cb + 2 * t + 1] = -z[1];
+        Zm[(ri + g + 8) * kLLD + cb + 2 * t] = -z[2];
+        Zm[(ri + g + 8) * kLLD + cb + 2 * t + 1] = -z[3];
+        __syncwarp();
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    for (int e = tid; e < nb * 256; e += 256) {  // Z_ib = -D_i M
-      const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15, i = b + lv;
-      float acc = 0.0f;
-#pragma unroll
-      for (int t = 0; t < 16; ++t) acc = fmaf(Zm[(16 * i + r) * kLLD + 16 * i + t], Mt[(b << 8) + t * 16 + cc], acc);
-      Zm[(16 * i + r) * kLLD + 16 * b + cc] = -acc;
-    }
-    __syncthreads();
   }
   // Z as the B operand [Z_hi; Z_lo] (N = 128 rows: row n < 64 is Z_hi[n], row
   // 64 + n is Z_lo[n]; K = the 64 tokens j in two 32-wide swizzled sub-tiles)
   for (int e = tid; e < kC * kC; e += 256) {
     const int n = e >> 6, j = e & 63;
     uint32_t zh, zl;
-    split_hi_lo(Zm[n * kLLD + j], zh, zl);
+    split_hi_lo((j >> 4) > (n >> 4) ? 0.0f : Zm[n * kLLD + j], zh, zl);
     uint8_t *sub = Zb + (j >> 5) * (128 * 128);
     *reinterpret_cast<uint32_t *>(sub + sw_off(n, j & 31)) = zh;
     *reinterpret_cast<uint32_t *>(sub + sw_off(64 + n, j & 31)) = zl;
