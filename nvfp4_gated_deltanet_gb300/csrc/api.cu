@@ -25,7 +25,6 @@ struct gdn_ctx {
   BatchWs bws;                          // large-batch decode intermediates, max_batch rows
   float *W, *Ut, *Am, *Gam;               // per (value head, 64-token chunk) products
   uint16_t *KTs = nullptr;                // per (key head, chunk) K^T for the tcgen05 chunk scan, split FP16
-  uint16_t *Qs = nullptr;                 // q for the tcgen05 chunk scan, split FP16
   float *Wsc = nullptr;                   // per (value head, chunk) FP16 scale of W
   float *Umax = nullptr;                  // per (value head, chunk) largest |Ut|
   uint16_t *conv_tmp;                   // [K-1][C]
@@ -588,7 +587,6 @@ gdn_status gdn_create(const gdn_config *cfg, const gdn_weights *w, void *stream,
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Am, Tp * Hv * 64);
     if (e == cudaSuccess) e = ctx_alloc(ctx, &ctx->Gam, Tp * Hv);
     if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->KTs, 2 * Tp * Hk * D);
-    if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->Qs, 2 * Tp * Hk * D);
     if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->Wsc, Tp / 64 * Hv);
     if (e == cudaSuccess && D == 128) e = ctx_alloc(ctx, &ctx->Umax, Tp / 64 * Hv);
   }
@@ -946,8 +944,9 @@ gdn_status gdn_prefill(gdn_ctx *ctx, const uint16_t *x, int T, int slot, int ini
   p.Ut = ctx->Ut;
   p.Am = ctx->Am;
   p.Gam = ctx->Gam;
-  // the tcgen05 path writes its split W and A over the FP32 ones (same bytes)
-  p.Qs = p.scan_tc == 2 ? ctx->Qs : nullptr;
+  // the tcgen05 path writes its split q, k, W and A over the FP32 ones (same bytes)
+  p.Qs = p.scan_tc == 2 ? reinterpret_cast<uint16_t *>(ctx->qn) : nullptr;
+  p.Ks = p.scan_tc == 2 ? reinterpret_cast<uint16_t *>(ctx->kn) : nullptr;
   p.Ws = p.scan_tc == 2 ? reinterpret_cast<uint16_t *>(ctx->W) : nullptr;
   p.As = p.scan_tc == 2 ? reinterpret_cast<uint16_t *>(ctx->Am) : nullptr;
   p.KTs = p.scan_tc == 2 ? ctx->KTs : nullptr;

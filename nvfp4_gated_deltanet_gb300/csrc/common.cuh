@@ -497,7 +497,8 @@ struct PrefillArgs {
   float *Gam;            // [Hv][nc][64]: in-chunk cumulative log-decay
   // The tcgen05 chunk scan's operands in split FP16, x s = hi + lo with a
   // power-of-two scale s (the hi block first, the lo block after it), or null:
-  uint16_t *Qs;          // [2][Hk][Tp][D]: q, s = 2^14
+  uint16_t *Qs;          // [2][Hk][Tp][D]: q, s = 2^14 (written by prep; may alias qn)
+  uint16_t *Ks;          // [2][Hk][Tp][D]: k, s = 2^14 (written by prep; may alias kn)
   uint16_t *Ws;          // [2][Hv][Tp][D]: W, s = Wsc of its chunk (may alias W)
   uint16_t *As;          // [2][Hv][Tp][64]: A, s = 2^14 (may alias Am)
   uint16_t *KTs;         // [2][Hk][nc][D][64]: per chunk K^T, s = 2^14

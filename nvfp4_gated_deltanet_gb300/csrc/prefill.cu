@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
     for (int j = 0; j < 4; ++j) w[e][j] = j < Kc ? bf16_bits_to_f32(a.conv_w[(size_t)(ch0 + lane * EPL + e) * Kc + j]) : 0.0f;
   const int nq = a.Hk;  // groups 0..Hk-1: q, Hk..2Hk-1: k, then v
   const bool isq = grp < nq, isk = !isq && grp < 2 * nq;
+  const bool split_qk = D == 128 && a.Qs && a.Ks;
   float *dst = isq ? a.qn + ((size_t)grp * a.Tp) * D
                    : isk ? a.kn + ((size_t)(grp - nq) * a.Tp) * D : a.v + ((size_t)(grp - 2 * nq) * a.Tp) * D;
   for (int i = warp; i < kPrepTT; i += blockDim.x / 32) {
@@ -118,7 +119,20 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
       p = warp_sum(p);
       r = isq ? (1.0f / sqrtf(p + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(p + a.l2_eps);
     }
-    if (t < a.T) {
+    if (split_qk && (isq || isk)) {
+      // the tcgen05 chunk stages' q / k operand: x 2^14 = hi + lo in FP16,
+      // zero for the padding tokens past T
+      if constexpr (EPL == 4) {
+        uint16_t *sp = (isq ? a.Qs + (size_t)grp * a.Tp * D : a.Ks + (size_t)(grp - nq) * a.Tp * D) + (size_t)t * D +
+                       lane * EPL;
+        const float sc = t < a.T ? r * 16384.0f : 0.0f;
+        uint32_t h0, l0, h1, l1;
+        split_f16x2(o[0] * sc, o[1] * sc, h0, l0);
+        split_f16x2(o[2] * sc, o[3] * sc, h1, l1);
+        *reinterpret_cast<uint2 *>(sp) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2 *>(sp + (size_t)a.Hk * a.Tp * D) = make_uint2(l0, l1);
+      }
+    } else if (t < a.T) {
       float *row = dst + (size_t)t * D + lane * EPL;
       if constexpr (EPL == 4) {  // one 16-byte store per lane
         *reinterpret_cast<float4 *>(row) = (isq || isk) ? make_float4(o[0] * r, o[1] * r, o[2] * r, o[3] * r)
@@ -359,36 +373,26 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(PrefillArgs a) {
 }
 
 // ---------------------------------------------------------------- chunk_prep on tcgen05
-// The products of chunk_prep_kernel<128> (Ut and Gamma in FP32; W and A, and q
-// and K^T, as the tcgen05 scan's split FP16 operands x s = hi + lo -- W with a
-// power-of-two scale per chunk from its largest |W|, the rest 2^14), with
-// K K^T and Q K^T as one tcgen05 product in split FP16:
-// k and q are L2-normalised (|k_i| <= 1, |q_i| <= d^-1/2), so the fixed
-// power-of-two scales 2^12 (k) and 2^14 (q) keep every element below FP16's
-// largest value and every lo part x - FP16(x) of an element larger than 2^-12
-// normal; x = hi + lo then carries 22 significant bits and
+// The products of chunk_prep_kernel<128> (Ut and Gamma in FP32; W, A and K^T
+// as the tcgen05 scan's split FP16 operands x s = hi + lo -- W with a
+// power-of-two scale per chunk from its largest |W|, A and K^T 2^14), with
+// K K^T and Q K^T as one tcgen05 product in split FP16 of prep's q and k:
+// they are L2-normalised (|k_i| <= 1, |q_i| <= d^-1/2), so the fixed scale
+// 2^14 keeps every element below FP16's largest value and every lo part
+// x - FP16(x) of an element larger than 2^-14 normal; x = hi + lo then
+// carries 22 significant bits and
 //   D = [K_hi; Q_hi] [K_hi; K_lo]^T + [K_lo; Q_lo] [K_hi; K_lo]^T
 // (M = 128, N = 128, K = 128; FP32 accumulators in tensor memory) gives in its
 // two column halves hi.hi + lo.hi and hi.lo + lo.lo of every k_i . k_j and
-// q_i . k_j, which the epilogue adds and scales back exactly (2^-24, 2^-26).
-// Operands are K-major with the 128-byte swizzle: per 64-wide d_k half a
-// [128 rows][64 FP16] sub-tile of 16 KB. After the product their 96 KB hold
-// K and v in FP32 and L for the substitution. 256 threads, two CTAs per SM.
+// q_i . k_j, which the epilogue adds and scales back exactly (2^-28).
+// Operands are K-major with the 128-byte swizzle, loaded by TMA: per 64-wide
+// d_k half a [128 rows][64 FP16] sub-tile of 16 KB. After the product the
+// [K; Q] tiles hold L and Z = (I + L)^-1, while B' keeps k for the W part.
+// 256 threads, two CTAs per SM.
 constexpr int kPrepSub = 128 * 128;           // one [128 rows][64 FP16] sub-tile
 constexpr int kPrepTile = 2 * kPrepSub;       // a 128 x 128 FP16 operand
 constexpr int kPrepSmem = 1024 + 3 * kPrepTile + 4 * kC * 4 + 64;
 
-GDN_DEV uint32_t pack_h2(float a, float b) {
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-// x = hi + lo in FP16 (x already scaled), four values
-GDN_DEV void split_h4(float4 x, uint2 &hi, uint2 &lo) {
-  const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
-  const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
-  hi = make_uint2(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1));
-  lo = make_uint2(pack_h2(x.x - f0.x, x.y - f0.y), pack_h2(x.z - f1.x, x.w - f1.y));
-}
 GDN_DEV void mma_f16_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -398,25 +402,36 @@ GDN_DEV void mma_f16_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t ide
       : "memory");
 }
 
-__global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
+// byte offset of FP16 element (row, col) in a [rows][64 FP16] tile, 128-byte swizzle
+GDN_DEV uint32_t sw16(int row, int col) {
+  return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1)));
+}
+
+__global__ void __launch_bounds__(256, 2)
+    chunk_prep_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         PrefillArgs a) {
   constexpr int D = 128;
   constexpr int kLLD = kC + 4;  // row stride of L and of (I + L)^-1: a lane writes one row, 4-way bank spread
   extern __shared__ uint8_t smraw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   uint8_t *Ahi = sm, *Alo = sm + kPrepTile, *Bp = sm + 2 * kPrepTile;
-  // after the first product the same bytes hold L, Z = (I + L)^-1, a 16 x 8
-  // scratch per warp and Z as the split B operand [Z_hi; Z_lo] of the
-  // second product (two [128 rows][32 FP32] sub-tiles, 1024-byte aligned)
+  // after the first product the [K; Q] tiles hold L, Z = (I + L)^-1, a 16 x 8
+  // scratch per warp and Z as the split B operand [Z_hi; Z_lo] of the second
+  // product (two [128 rows][32 FP32] sub-tiles, 1024-byte aligned: the first
+  // over L once Z is complete, the second after the scratch); B' = [K_hi; K_lo]
+  // stays for the W part
   float *Lm = reinterpret_cast<float *>(sm);
   float *Zm = Lm + kC * kLLD;
   float *Mt = Zm + kC * kLLD;
-  uint8_t *Zb = sm + 38 * 1024;
-  static_assert(38 * 1024 >= (2 * kC * kLLD + 8 * 128) * 4 && 38 * 1024 + 2 * 128 * 128 <= 3 * kPrepTile,
-                "L, Z, the scratch and the B operand fit in the operand tiles");
+  uint8_t *Zb0 = sm, *Zb1 = sm + 38 * 1024;
+  static_assert(38 * 1024 >= (2 * kC * kLLD + 8 * 128) * 4 && kC * kLLD * 4 >= 128 * 128 &&
+                    38 * 1024 + 128 * 128 <= 2 * kPrepTile,
+                "L, Z, the scratch and the B operand fit in the [K; Q] tiles");
   float *gam = reinterpret_cast<float *>(sm + 3 * kPrepTile);
   float *bet = gam + kC, *bek = bet + kC;
   uint64_t *done = reinterpret_cast<uint64_t *>(bek + kC);
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(done + 1);
+  uint64_t *ld = done + 1;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(done + 2);
   __shared__ float wred[8];
   const int c = blockIdx.x, h = blockIdx.y;
   const int kh = h / (a.Hv / a.Hk);
@@ -432,61 +447,38 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
   }
   if (tid == 0) {
     mbar_init(done, 1);
+    mbar_init(ld, 1);
     fence_barrier_init();
+    // the [K; Q] operand tiles (hi and lo) and B' = [K_hi; K_lo] by TMA from
+    // prep's split q and k (x 2^14 = hi + lo, zero past T): per 64-wide d
+    // half, rows 0..63 k and 64..127 q of the A tiles, rows 0..63 k_hi and
+    // 64..127 k_lo of B'
+    const int yq = kh * a.Tp + t0, ylo = a.Hk * a.Tp;
+    mbar_arrive_expect_tx(ld, 12 * 64 * 128);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint8_t *ah = Ahi + q * kPrepSub, *al = Alo + q * kPrepSub, *bp = Bp + q * kPrepSub;
+      tma_load_2d(ah, &tmK, 128 * q, yq, ld);
+      tma_load_2d(ah + 64 * 128, &tmQ, 128 * q, yq, ld);
+      tma_load_2d(al, &tmK, 128 * q, ylo + yq, ld);
+      tma_load_2d(al + 64 * 128, &tmQ, 128 * q, ylo + yq, ld);
+      tma_load_2d(bp, &tmK, 128 * q, yq, ld);
+      tma_load_2d(bp + 64 * 128, &tmK, 128 * q, ylo + yq, ld);
+    }
   }
   if (warp == 0) {
     tmem_alloc(tmem_holder, 256);
     tmem_relinquish();
   }
-  // one CTA per key head writes the scan's q and K^T operands
+  // one CTA per key head writes the scan's K^T operand
   const bool write_q = h % (a.Hv / a.Hk) == 0;
-  // k and q rows -> scaled FP16 hi / lo operand tiles; every load first
-  {
-    float4 x[8][2];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int idx = tid + 256 * k;         // 2048 eight-element pieces: k rows, then q rows
-      const int isq = idx >> 10, r = (idx >> 4) & 63, c8 = idx & 15;
-      const float *src = (isq ? a.qn : a.kn) + ((size_t)kh * a.Tp + t0 + r) * D + c8 * 8;
-      const bool live = t0 + r < a.T;
-      x[k][0] = live ? reinterpret_cast<const float4 *>(src)[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-      x[k][1] = live ? reinterpret_cast<const float4 *>(src)[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int idx = tid + 256 * k;
-      const int isq = idx >> 10, r = (idx >> 4) & 63, c8 = idx & 15;
-      const float sc = isq ? 16384.0f : 4096.0f;
-      float4 v0 = x[k][0], v1 = x[k][1];
-      v0.x *= sc; v0.y *= sc; v0.z *= sc; v0.w *= sc;
-      v1.x *= sc; v1.y *= sc; v1.z *= sc; v1.w *= sc;
-      uint2 h0, l0, h1, l1;
-      split_h4(v0, h0, l0);
-      split_h4(v1, h1, l1);
-      const uint4 hv = make_uint4(h0.x, h0.y, h1.x, h1.y), lv = make_uint4(l0.x, l0.y, l1.x, l1.y);
-      const int sub = c8 >> 3, cc = c8 & 7;
-      const int row = isq * kC + r;
-      const uint32_t off = (uint32_t)(sub * kPrepSub + row * 128 + ((cc ^ (row & 7)) << 4));
-      *reinterpret_cast<uint4 *>(Ahi + off) = hv;
-      *reinterpret_cast<uint4 *>(Alo + off) = lv;
-      if (isq && write_q) {  // the scan's q operand (the same split), once per key head
-        uint16_t *qs = a.Qs + ((size_t)kh * a.Tp + t0 + r) * D + c8 * 8;
-        *reinterpret_cast<uint4 *>(qs) = hv;
-        *reinterpret_cast<uint4 *>(qs + (size_t)a.Hk * a.Tp * D) = lv;
-      }
-      if (!isq) {  // B' = [K_hi; K_lo]: rows r and 64 + r (the same swizzle phase)
-        const uint32_t ob = (uint32_t)(sub * kPrepSub + r * 128 + ((cc ^ (r & 7)) << 4));
-        *reinterpret_cast<uint4 *>(Bp + ob) = hv;
-        *reinterpret_cast<uint4 *>(Bp + ob + 64 * 128) = lv;
-      }
-    }
-  }
-  fence_async_shared();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  if (tid == 32) {  // the product: eight K = 16 steps, two MMAs each
+  const bool staged = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(ld, 0u) : 0, 0) != 0;
+  if (!staged && tid == 0) flag_status(a.status, GDN_E_TIMEOUT);
+  if (tid == 32 && staged) {  // the product: eight K = 16 steps, two MMAs each
     const uint32_t idesc = (1u << 4) | ((uint32_t)(128 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -539,20 +531,20 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = j0 + k + e;
-          l4[e] = j < i ? bet[i] * expf(gam[i] - gam[j]) * (v[k + e] * 0x1p-24f) : 0.0f;
+          l4[e] = j < i ? bet[i] * expf(gam[i] - gam[j]) * (v[k + e] * 0x1p-28f) : 0.0f;
         }
         *reinterpret_cast<float4 *>(Lm + i * kLLD + j0 + k) = make_float4(l4[0], l4[1], l4[2], l4[3]);
       }
     } else {
-      // A 2^14 = e^(Gamma_i - Gamma_j) (q_i . k_j 2^26) 2^-12, split for the scan
+      // A 2^14 = e^(Gamma_i - Gamma_j) (q_i . k_j 2^28) 2^-14, split for the scan
       const int i = m - kC;
       uint16_t *Ag = a.As + ((size_t)h * a.Tp + t0 + i) * kC + j0;
       uint32_t hw[16], lw[16];
 #pragma unroll
       for (int k = 0; k < 32; k += 2) {
         const int j = j0 + k;
-        const float x0 = j <= i ? expf(gam[i] - gam[j]) * (v[k] * 0x1p-12f) : 0.0f;
-        const float x1 = j + 1 <= i ? expf(gam[i] - gam[j + 1]) * (v[k + 1] * 0x1p-12f) : 0.0f;
+        const float x0 = j <= i ? expf(gam[i] - gam[j]) * (v[k] * 0x1p-14f) : 0.0f;
+        const float x1 = j + 1 <= i ? expf(gam[i] - gam[j + 1]) * (v[k + 1] * 0x1p-14f) : 0.0f;
         split_f16x2(x0, x1, hw[k / 2], lw[k / 2]);
       }
       uint4 *gh = reinterpret_cast<uint4 *>(Ag), *gl = reinterpret_cast<uint4 *>(Ag + (size_t)a.Hv * a.Tp * kC);
@@ -629,7 +621,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
     const int n = e >> 6, j = e & 63;
     uint32_t zh, zl;
     split_hi_lo((j >> 4) > (n >> 4) ? 0.0f : Zm[n * kLLD + j], zh, zl);
-    uint8_t *sub = Zb + (j >> 5) * (128 * 128);
+    uint8_t *sub = (j >> 5) ? Zb1 : Zb0;
     *reinterpret_cast<uint32_t *>(sub + sw_off(n, j & 31)) = zh;
     *reinterpret_cast<uint32_t *>(sub + sw_off(64 + n, j & 31)) = zl;
   }
@@ -647,23 +639,42 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
     const uint32_t idesc = idesc_tf32(128);
 #pragma unroll 1
     for (int part = 0; part < 2; ++part) {
-      const float *src = part == 0 ? a.kn + ((size_t)kh * a.Tp + t0) * D : a.v + ((size_t)h * a.Tp + t0) * D;
       float x[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const int j = j0 + k;
-        x[k] = t0 + j < a.T ? src[(size_t)j * D + d] : 0.0f;
-      }
-      if (part == 0 && write_q) {  // K^T 2^14 of the chunk, split, for the scan
+      if (part == 0) {
+        // k from B' (k 2^14 = hi + lo, exact in FP32); its hi and lo are the
+        // scan's K^T operand as they stand
+        const uint8_t *bp = Bp + (d >> 6) * kPrepSub;
         uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) split_f16x2(x[k] * 16384.0f, x[k + 1] * 16384.0f, hw[k / 2], lw[k / 2]);
-        uint16_t *kt = a.KTs + (((size_t)kh * nc + c) * D + d) * kC + j0;
-        uint4 *gh = reinterpret_cast<uint4 *>(kt), *gl = reinterpret_cast<uint4 *>(kt + (size_t)a.Hk * nc * D * kC);
+        for (int k = 0; k < 32; k += 2) {
+          const int j = j0 + k;
+          const uint16_t h0 = *reinterpret_cast<const uint16_t *>(bp + sw16(j, d & 63));
+          const uint16_t h1 = *reinterpret_cast<const uint16_t *>(bp + sw16(j + 1, d & 63));
+          const uint16_t l0 = *reinterpret_cast<const uint16_t *>(bp + sw16(64 + j, d & 63));
+          const uint16_t l1 = *reinterpret_cast<const uint16_t *>(bp + sw16(65 + j, d & 63));
+          x[k] = (__half2float(__ushort_as_half(h0)) + __half2float(__ushort_as_half(l0))) * 0x1p-14f;
+          x[k + 1] = (__half2float(__ushort_as_half(h1)) + __half2float(__ushort_as_half(l1))) * 0x1p-14f;
+          hw[k / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+          lw[k / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+        }
+        if (write_q) {  // K^T 2^14 of the chunk, split, for the scan
+          uint16_t *kt = a.KTs + (((size_t)kh * nc + c) * D + d) * kC + j0;
+          uint4 *gh = reinterpret_cast<uint4 *>(kt), *gl = reinterpret_cast<uint4 *>(kt + (size_t)a.Hk * nc * D * kC);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          gh[k] = make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
-          gl[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+          for (int k = 0; k < 4; ++k) {
+            gh[k] = make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+            gl[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+          }
+        }
+      } else {
+        // v of the chunk, bulk-copied into B' during the W part
+        const bool vin = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(ld, 1u) : 0, 0) != 0;
+        if (!vin && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+        const float *vs = reinterpret_cast<const float *>(Bp);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int j = j0 + k;
+          x[k] = vin && t0 + j < a.T ? vs[j * D + d] : 0.0f;
         }
       }
       uint32_t xh[32], xl[32];
@@ -674,11 +685,16 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_tc_kernel(PrefillArgs a) {
       tmem_st_wait();
       tc_fence_before();
       __syncthreads();
+      if (part == 0 && tid == 0) {  // k has been read from B': the chunk's v rows (32 KB) over it
+        fence_async_shared();
+        mbar_arrive_expect_tx(ld, kC * D * 4);
+        bulk_g2s(Bp, a.v + ((size_t)h * a.Tp + t0) * D, kC * D * 4, ld);
+      }
       if (tid == 32) {
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = desc_sw128(smem_u32(Zb + (kk >> 2) * (128 * 128))) + 2 * (kk & 3);
+          const uint64_t bd = desc_sw128(smem_u32((kk >> 2) ? Zb1 : Zb0)) + 2 * (kk & 3);
           mma_tf32_ts(tmem, tmem + 192 + 8 * kk, bd, idesc, kk ? 1u : 0u);
           mma_tf32_ts(tmem, tmem + 128 + 8 * kk, bd, idesc, 1u);
         }
@@ -1172,14 +1188,19 @@ cudaError_t launch_chunks(const PrefillArgs &a, const LaunchCtx &lc) {
   }
   const int nc = a.Tp / kC;
   if (D == 128 && a.scan_tc == 2) {  // both chunk stages on tcgen05
-    if (!a.Qs || !a.Ws || !a.As || !a.KTs || !a.Wsc || !a.Umax) return cudaErrorInvalidValue;
+    if (!a.Qs || !a.Ks || !a.Ws || !a.As || !a.KTs || !a.Wsc || !a.Umax) return cudaErrorInvalidValue;
     static bool configured_p = false;
     if (!configured_p) {
       cudaError_t e = cudaFuncSetAttribute(chunk_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
       if (e != cudaSuccess) return e;
       configured_p = true;
     }
-    chunk_prep_tc_kernel<<<dim3(nc, a.Hv), 256, kPrepSmem, lc.stream>>>(a);
+    // prep's split q and k as 2-D byte tensors [2 Hk Tp][2 D]; 64-row boxes of 128 bytes
+    CUtensorMap mQ, mK;
+    if (!make_map(&mQ, a.Qs, 2ull * a.Hk * a.Tp, (uint64_t)D * 2, kC, 128, true) ||
+        !make_map(&mK, a.Ks, 2ull * a.Hk * a.Tp, (uint64_t)D * 2, kC, 128, true))
+      return cudaErrorInvalidValue;
+    chunk_prep_tc_kernel<<<dim3(nc, a.Hv), 256, kPrepSmem, lc.stream>>>(mQ, mK, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_chunk_scan_umma(a, lc.stream);
