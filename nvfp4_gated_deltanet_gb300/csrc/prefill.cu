@@ -62,16 +62,27 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
   const int Kc = a.Kc;
   // window rows r = 0 .. TT+Kc-2 hold tokens t0 - (Kc-1) + r (state rows for t < 0)
   constexpr int VPR = D / 8;  // 16-byte vectors per row
-  if (a.ld % 8 == 0 && a.C % 8 == 0) {  // every row starts 16-byte aligned
-    for (int e = tid; e < (kPrepTT + Kc - 1) * VPR; e += blockDim.x) {
+  if (a.ld % 8 == 0 && a.C % 8 == 0 && blockDim.x == 128) {  // every row starts 16-byte aligned
+    // every load of the window issued before any is stored (read-only loads,
+    // so they need not wait for the shared-memory stores)
+    constexpr int kWin = ((kPrepTT + 3) * VPR + 127) / 128;
+    const int nv = (kPrepTT + Kc - 1) * VPR;
+    uint4 val[kWin];
+#pragma unroll
+    for (int q = 0; q < kWin; ++q) {
+      const int e = tid + 128 * q;
       const int r = e / VPR, v = e % VPR;
       const int tau = t0 - (Kc - 1) + r;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (tau >= 0 && tau < a.T)
-        val = *reinterpret_cast<const uint4 *>(a.proj + (size_t)tau * a.ld + ch0 + v * 8);
-      else if (tau < 0)
-        val = *reinterpret_cast<const uint4 *>(a.conv_state + (size_t)(Kc - 1 + tau) * a.C + ch0 + v * 8);
-      *reinterpret_cast<uint4 *>(&win[r][v * 8]) = val;
+      val[q] = make_uint4(0, 0, 0, 0);
+      if (e < nv && tau >= 0 && tau < a.T)
+        val[q] = __ldg(reinterpret_cast<const uint4 *>(a.proj + (size_t)tau * a.ld + ch0 + v * 8));
+      else if (e < nv && tau < 0)
+        val[q] = __ldg(reinterpret_cast<const uint4 *>(a.conv_state + (size_t)(Kc - 1 + tau) * a.C + ch0 + v * 8));
+    }
+#pragma unroll
+    for (int q = 0; q < kWin; ++q) {
+      const int e = tid + 128 * q;
+      if (e < nv) *reinterpret_cast<uint4 *>(&win[e / VPR][(e % VPR) * 8]) = val[q];
     }
   } else {
     for (int e = tid; e < (kPrepTT + Kc - 1) * D; e += blockDim.x) {
@@ -103,13 +114,30 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
   for (int i = warp; i < kPrepTT; i += blockDim.x / 32) {
     const int t = t0 + i;
     float o[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      float pre = 0.0f;
+    if constexpr (EPL == 4) {
+      // four channels per lane: one 8-byte window load per tap; SiLU with the
+      // fast exponential and an IEEE reciprocal (the kernel is issue-bound)
+      float pre[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (j < Kc) pre = fmaf(w[e][j], bf16_bits_to_f32(win[i + j][lane * EPL + e]), pre);
-      o[e] = siluf_(pre);
+        if (j < Kc) {
+          const uint2 wv = *reinterpret_cast<const uint2 *>(&win[i + j][lane * 4]);
+          pre[0] = fmaf(w[0][j], __uint_as_float(wv.x << 16), pre[0]);
+          pre[1] = fmaf(w[1][j], __uint_as_float(wv.x & 0xFFFF0000u), pre[1]);
+          pre[2] = fmaf(w[2][j], __uint_as_float(wv.y << 16), pre[2]);
+          pre[3] = fmaf(w[3][j], __uint_as_float(wv.y & 0xFFFF0000u), pre[3]);
+        }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = pre[e] * __frcp_rn(1.0f + __expf(-pre[e]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        float pre = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < Kc) pre = fmaf(w[e][j], bf16_bits_to_f32(win[i + j][lane * EPL + e]), pre);
+        o[e] = siluf_(pre);
+      }
     }
     float r = 1.0f;
     if (isq || isk) {
@@ -117,7 +145,7 @@ __global__ void __launch_bounds__(128) prep_kernel(PrefillArgs a) {
 #pragma unroll
       for (int e = 0; e < EPL; ++e) p = fmaf(o[e], o[e], p);
       p = warp_sum(p);
-      r = isq ? (1.0f / sqrtf(p + a.l2_eps)) * (1.0f / sqrtf((float)D)) : 1.0f / sqrtf(p + a.l2_eps);
+      r = rsqrtf(p + a.l2_eps) * (isq ? rsqrtf((float)D) : 1.0f);
     }
     if (split_qk && (isq || isk)) {
       // the tcgen05 chunk stages' q / k operand: x 2^14 = hi + lo in FP16,
