@@ -585,11 +585,68 @@ __global__ void __launch_bounds__(256, 2)
   }
   tc_fence_before();
   __syncthreads();
+  // [W | Ut]^T = R^T Z^T, R = [diag(beta e^Gamma) K | diag(beta) v], one
+  // 128-row part at a time: the part's R^T (lanes = d, columns = tokens j) as
+  // hi and lo in TMEM columns 128..255 (the MMAs' A operand), the product
+  // D[d][n] = R^T Z_hi^T | R^T Z_lo^T in columns 0..127, whose halves the
+  // epilogue adds. Tokens past T are zero. A warp stages its lane quarter's
+  // rows d for one half of the tokens.
+  const int qt = warp & 3, hf = warp >> 2;
+  const int d = 32 * qt + lane, j0 = 32 * hf;
+  const uint32_t tl = tmem + ((uint32_t)(qt * 32) << 16);
+  auto stage_r = [&](int part) {
+    float x[32];
+    if (part == 0) {
+      // k from B' (k 2^14 = hi + lo, exact in FP32); its hi and lo are the
+      // scan's K^T operand as they stand
+      const uint8_t *bp = Bp + (d >> 6) * kPrepSub;
+      uint32_t hw[16], lw[16];
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        const int j = j0 + k;
+        const uint16_t h0 = *reinterpret_cast<const uint16_t *>(bp + sw16(j, d & 63));
+        const uint16_t h1 = *reinterpret_cast<const uint16_t *>(bp + sw16(j + 1, d & 63));
+        const uint16_t l0 = *reinterpret_cast<const uint16_t *>(bp + sw16(64 + j, d & 63));
+        const uint16_t l1 = *reinterpret_cast<const uint16_t *>(bp + sw16(65 + j, d & 63));
+        x[k] = (__half2float(__ushort_as_half(h0)) + __half2float(__ushort_as_half(l0))) * 0x1p-14f;
+        x[k + 1] = (__half2float(__ushort_as_half(h1)) + __half2float(__ushort_as_half(l1))) * 0x1p-14f;
+        hw[k / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lw[k / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+      }
+      if (write_q) {  // K^T 2^14 of the chunk, split, for the scan
+        uint16_t *kt = a.KTs + (((size_t)kh * nc + c) * D + d) * kC + j0;
+        uint4 *gh = reinterpret_cast<uint4 *>(kt), *gl = reinterpret_cast<uint4 *>(kt + (size_t)a.Hk * nc * D * kC);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          gh[k] = make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+          gl[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+        }
+      }
+    } else {
+      // v of the chunk, bulk-copied into B' once k had been read
+      const bool vin = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(ld, 1u) : 0, 0) != 0;
+      if (!vin && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+      const float *vs = reinterpret_cast<const float *>(Bp);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int j = j0 + k;
+        x[k] = vin && t0 + j < a.T ? vs[j * D + d] : 0.0f;
+      }
+    }
+    uint32_t xh[32], xl[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) split_hi_lo(x[k] * (part == 0 ? bek[j0 + k] : bet[j0 + k]), xh[k], xl[k]);
+    tmem_st32(tl + 128 + j0, xh);
+    tmem_st32(tl + 192 + j0, xl);
+    tmem_st_wait();
+    tc_fence_before();
+  };
   // Z = (I + L)^-1 by 16 x 16 blocks: the diagonal blocks D_b by forward
-  // substitution (one column per thread), then Z_ib = -D_i sum_{k=b}^{i-1}
-  // L_ik Z_kb level by level (i - b = 1, 2, 3), from the equation
-  // (I + L) Z = I read block row by block row. Blocks above the diagonal are
-  // zero and never written.
+  // substitution (one column per thread, warps 0-1), then Z_ib = -D_i
+  // sum_{k=b}^{i-1} L_ik Z_kb level by level (i - b = 1, 2, 3; warps 2-7), from
+  // the equation (I + L) Z = I read block row by block row. Blocks above the
+  // diagonal are zero and never written. The W part's R^T needs only k, so
+  // each warp stages it while the other warps work on the inverse.
   if (tid < kC) {
     const int b = tid >> 4, cc = tid & 15, o = 16 * b;
     float x[16];
@@ -601,30 +658,35 @@ __global__ void __launch_bounds__(256, 2)
       x[r] = acc;
       Zm[(o + r) * kLLD + o + cc] = acc;
     }
+  } else {
+    stage_r(0);
   }
   __syncthreads();
-  // a level's blocks on split-TF32 warp MMA: warp w takes block b = w / 2,
-  // columns 8 (w & 1) .. + 7 of it, while b < 4 - lv; M = sum_k L_ik Z_kb
-  // (16 x 8) goes through the warp's scratch into B fragments of -D_i M
-  {
-    const int g = lane >> 2, t = lane & 3;
+  if (warp < 2) {
+    stage_r(0);
+  } else {
+    // a level's blocks on split-TF32 warp MMA: warp w (2..7) takes block
+    // b = (w - 2) / 2, columns 8 ((w - 2) & 1) .. + 7 of it, while b < 4 - lv;
+    // M = sum_k L_ik Z_kb (16 x 8) goes through the warp's scratch into B
+    // fragments of -D_i M; a named barrier of warps 2-7 between levels
+    const int g = lane >> 2, t = lane & 3, wl = warp - 2;
     float *Ms = Mt + warp * 128;
 #pragma unroll 1
     for (int lv = 1; lv < 4; ++lv) {
-      const int b = warp >> 1;
+      const int b = wl >> 1;
       if (b < 4 - lv) {
-        const int i = b + lv, cb = 16 * b + 8 * (warp & 1), ri = 16 * i;
-        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const int i = b + lv, cb = 16 * b + 8 * (wl & 1), ri = 16 * i;
+        float dacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int kc = 16 * b; kc < ri; kc += 8) {
           const float af[4] = {Lm[(ri + g) * kLLD + kc + t], Lm[(ri + g + 8) * kLLD + kc + t],
                                Lm[(ri + g) * kLLD + kc + t + 4], Lm[(ri + g + 8) * kLLD + kc + t + 4]};
           const float bf[2] = {Zm[(kc + t) * kLLD + cb + g], Zm[(kc + t + 4) * kLLD + cb + g]};
-          mma3(d, af, bf);
+          mma3(dacc, af, bf);
         }
-        Ms[g * 8 + 2 * t] = d[0];
-        Ms[g * 8 + 2 * t + 1] = d[1];
-        Ms[(g + 8) * 8 + 2 * t] = d[2];
-        Ms[(g + 8) * 8 + 2 * t + 1] = d[3];
+        Ms[g * 8 + 2 * t] = dacc[0];
+        Ms[g * 8 + 2 * t + 1] = dacc[1];
+        Ms[(g + 8) * 8 + 2 * t] = dacc[2];
+        Ms[(g + 8) * 8 + 2 * t + 1] = dacc[3];
         __syncwarp();
         float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -640,8 +702,14 @@ __global__ void __launch_bounds__(256, 2)
         Zm[(ri + g + 8) * kLLD + cb + 2 * t + 1] = -z[3];
         __syncwarp();
       }
-      __syncthreads();
+      asm volatile("bar.sync 1, 192;" ::: "memory");
     }
+  }
+  __syncthreads();
+  if (tid == 0) {  // k has been read from B': the chunk's v rows (32 KB) over it
+    fence_async_shared();
+    mbar_arrive_expect_tx(ld, kC * D * 4);
+    bulk_g2s(Bp, a.v + ((size_t)h * a.Tp + t0) * D, kC * D * 4, ld);
   }
   // Z as the B operand [Z_hi; Z_lo] (N = 128 rows: row n < 64 is Z_hi[n], row
   // 64 + n is Z_lo[n]; K = the 64 tokens j in two 32-wide swizzled sub-tiles)
@@ -654,69 +722,15 @@ __global__ void __launch_bounds__(256, 2)
     *reinterpret_cast<uint32_t *>(sub + sw_off(64 + n, j & 31)) = zl;
   }
   fence_async_shared();
+  tc_fence_before();
   __syncthreads();
-  // [W | Ut]^T = R^T Z^T, R = [diag(beta e^Gamma) K | diag(beta) v], one
-  // 128-row part at a time: the part's R^T (lanes = d, columns = tokens j) as
-  // hi and lo in TMEM columns 128..255 (the MMAs' A operand), the product
-  // D[d][n] = R^T Z_hi^T | R^T Z_lo^T in columns 0..127, whose halves the
-  // epilogue adds. Tokens past T are zero.
   {
-    const int qt = warp & 3, hf = warp >> 2;
-    const int d = 32 * qt + lane, j0 = 32 * hf;
-    const uint32_t tl = tmem + ((uint32_t)(qt * 32) << 16);
     const uint32_t idesc = idesc_tf32(128);
 #pragma unroll 1
     for (int part = 0; part < 2; ++part) {
-      float x[32];
-      if (part == 0) {
-        // k from B' (k 2^14 = hi + lo, exact in FP32); its hi and lo are the
-        // scan's K^T operand as they stand
-        const uint8_t *bp = Bp + (d >> 6) * kPrepSub;
-        uint32_t hw[16], lw[16];
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int j = j0 + k;
-          const uint16_t h0 = *reinterpret_cast<const uint16_t *>(bp + sw16(j, d & 63));
-          const uint16_t h1 = *reinterpret_cast<const uint16_t *>(bp + sw16(j + 1, d & 63));
-          const uint16_t l0 = *reinterpret_cast<const uint16_t *>(bp + sw16(64 + j, d & 63));
-          const uint16_t l1 = *reinterpret_cast<const uint16_t *>(bp + sw16(65 + j, d & 63));
-          x[k] = (__half2float(__ushort_as_half(h0)) + __half2float(__ushort_as_half(l0))) * 0x1p-14f;
-          x[k + 1] = (__half2float(__ushort_as_half(h1)) + __half2float(__ushort_as_half(l1))) * 0x1p-14f;
-          hw[k / 2] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-          lw[k / 2] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-        }
-        if (write_q) {  // K^T 2^14 of the chunk, split, for the scan
-          uint16_t *kt = a.KTs + (((size_t)kh * nc + c) * D + d) * kC + j0;
-          uint4 *gh = reinterpret_cast<uint4 *>(kt), *gl = reinterpret_cast<uint4 *>(kt + (size_t)a.Hk * nc * D * kC);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            gh[k] = make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
-            gl[k] = make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
-          }
-        }
-      } else {
-        // v of the chunk, bulk-copied into B' during the W part
-        const bool vin = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(ld, 1u) : 0, 0) != 0;
-        if (!vin && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
-        const float *vs = reinterpret_cast<const float *>(Bp);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int j = j0 + k;
-          x[k] = vin && t0 + j < a.T ? vs[j * D + d] : 0.0f;
-        }
-      }
-      uint32_t xh[32], xl[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) split_hi_lo(x[k] * (part == 0 ? bek[j0 + k] : bet[j0 + k]), xh[k], xl[k]);
-      tmem_st32(tl + 128 + j0, xh);
-      tmem_st32(tl + 192 + j0, xl);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncthreads();
-      if (part == 0 && tid == 0) {  // k has been read from B': the chunk's v rows (32 KB) over it
-        fence_async_shared();
-        mbar_arrive_expect_tx(ld, kC * D * 4);
-        bulk_g2s(Bp, a.v + ((size_t)h * a.Tp + t0) * D, kC * D * 4, ld);
+      if (part == 1) {
+        stage_r(1);
+        __syncthreads();
       }
       if (tid == 32) {
         tc_fence_after();
