@@ -124,6 +124,9 @@ GDN_DEV void prefetch_l2(const void *p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// 1 / s for a power of two s = 2^k, |k| <= 126: the exponent negated (exact)
+GDN_DEV float inv_pow2(float s) { return __uint_as_float((254u << 23) - __float_as_uint(s)); }
+
 // Bounded wait that also gives up when another role has given up.
 GDN_DEV bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag, int32_t *status) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -321,7 +324,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       for (int j = 0; j < RH / 4; ++j) {
         ut[4 * j] = n_ut[j].x; ut[4 * j + 1] = n_ut[j].y; ut[4 * j + 2] = n_ut[j].z; ut[4 * j + 3] = n_ut[j].w;
       }
-      if (c + 1 < nc) load_next(c + 1);
       // (a) S -> the B operand of P (thread e owns column e of its rows), with
       // the scale of the slice's largest |S|. U's scale (Cf shares it) comes
       // from a bound known here, |U| <= max|Ut| + d max|W| max|S| with
@@ -339,17 +341,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           break;
         }
         sS = fp16_scale_for(smax);
-        sU = fp16_scale_for(fmaf((float)kD * kFixedScale / wsc, smax, umax));
+        sU = fp16_scale_for(fmaf((float)kD * kFixedScale * inv_pow2(wsc), smax, umax));
         put_split_rows<R, RH>(tS + (qt >> 1) * L::kSub, RH * hf, 32 * (qt & 1) + lane, Sv, sS, lane);
         fence_async_shared();
         tc_fence_before();
         mbar_arrive(s_ready);
       }
-      const float iS = 1.0f / sS;
+      if (c + 1 < nc) load_next(c + 1);
+      const float iS = inv_pow2(sS);
       if (!wrow && c > 0 && !emit_o(c - 1)) { ok = false; break; }
       if (wrow) {
         // (b) W rows: U = Ut - W S^T, the update coefficients Cf = e^(Gamma_64 - Gamma_i) U
-        const float iWS = iS * (1.0f / wsc);
+        const float iWS = iS * inv_pow2(wsc);
         const float dc = expf(gC - gi);
         if (!warp_wait(p_done, (uint32_t)(c & 1), abort_flag, a.status)) { ok = false; break; }
         tc_fence_after();
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
         for (int k = 0; k < RH; ++k) pq[k] = di * (__uint_as_float(pr[k]) + __uint_as_float(pr1[k]));
       }
-      const float iK = (1.0f / kFixedScale) / sU;  // K^T Cf and A U: 2^14 s_U
+      const float iK = (1.0f / kFixedScale) * inv_pow2(sU);  // K^T Cf and A U: 2^14 s_U
       iO = iK;
       // (c) the state update
       if (!warp_wait(s_acc_done, (uint32_t)(c & 1), abort_flag, a.status)) { ok = false; break; }
