@@ -460,13 +460,13 @@ __global__ void __launch_bounds__(256, 2)
   uint64_t *done = reinterpret_cast<uint64_t *>(bek + kC);
   uint64_t *ld = done + 1;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(done + 2);
-  __shared__ float wred[8];
+  __shared__ float wred[8], ured[8];
   const int c = blockIdx.x, h = blockIdx.y;
   const int kh = h / (a.Hv / a.Hk);
   const int t0 = c * kC;
   const int nc = a.Tp / kC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < 8) wred[tid] = 0.0f;
+  if (tid < 8) wred[tid] = ured[tid] = 0.0f;
 
   if (tid < kC) {
     const bool live = t0 + tid < a.T;
@@ -726,12 +726,7 @@ __global__ void __launch_bounds__(256, 2)
   __syncthreads();
   {
     const uint32_t idesc = idesc_tf32(128);
-#pragma unroll 1
-    for (int part = 0; part < 2; ++part) {
-      if (part == 1) {
-        stage_r(1);
-        __syncthreads();
-      }
+    auto issue = [&]() {  // D = R^T [Z_hi; Z_lo]^T: eight K = 8 steps, A lo then A hi
       if (tid == 32) {
         tc_fence_after();
 #pragma unroll
@@ -742,59 +737,80 @@ __global__ void __launch_bounds__(256, 2)
         }
         tc_commit(done);
       }
-      const int ok2 = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(done, (uint32_t)(1 + part) & 1u) : 0, 0);
-      if (!ok2 && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
-      tc_fence_after();
-      float wv[32];  // W (part 0): tokens j0 + k, kept until the chunk's largest |W| is known
-      if (ok2) {
-        uint32_t p0[16], p1[16], q0[16], q1[16];
-        tmem_ld16(tl + j0, p0);
-        tmem_ld16(tl + j0 + 16, p1);
-        tmem_ld16(tl + 64 + j0, q0);
-        tmem_ld16(tl + 64 + j0 + 16, q1);
-        tmem_ld_wait();
+    };
+    // this thread's row d of the product, tokens j0 .. j0 + 31 (the halves added)
+    auto read_acc = [&](float (&out)[32]) {
+      uint32_t p0[16], p1[16], q0[16], q1[16];
+      tmem_ld16(tl + j0, p0);
+      tmem_ld16(tl + j0 + 16, p1);
+      tmem_ld16(tl + 64 + j0, q0);
+      tmem_ld16(tl + 64 + j0 + 16, q1);
+      tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          wv[k] = __uint_as_float(p0[k]) + __uint_as_float(q0[k]);
-          wv[16 + k] = __uint_as_float(p1[k]) + __uint_as_float(q1[k]);
-        }
-        if (part == 1) {
-          float *dst = a.Ut + (((size_t)h * nc + c) * kC + j0) * D + d;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) dst[(size_t)k * D] = wv[k];
-        }
-        // the chunk's largest |W| (its split scale) or |Ut| (the scan's bound on |U|)
-        float mx = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fabsf(wv[k]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) wred[warp] = mx;
+      for (int k = 0; k < 16; ++k) {
+        out[k] = __uint_as_float(p0[k]) + __uint_as_float(q0[k]);
+        out[16 + k] = __uint_as_float(p1[k]) + __uint_as_float(q1[k]);
       }
-      tc_fence_before();
-      __syncthreads();  // the accumulator and the A columns are read before the next part
-      if (part == 1 && tid == 0) {
-        float m = wred[0];
-        for (int w = 1; w < 8; ++w) m = fmaxf(m, wred[w]);
-        a.Umax[(size_t)h * nc + c] = m;
-      }
-      if (part == 0 && ok2) {  // W s = hi + lo, s from the chunk's largest |W|
-        float m = wred[0];
+    };
+    auto warp_absmax = [&](const float (&v)[32]) -> float {
+      float mx = 0.0f;
 #pragma unroll
-        for (int w = 1; w < 8; ++w) m = fmaxf(m, wred[w]);
-        const float sw = fp16_scale_for(m);
-        if (tid == 0) a.Wsc[(size_t)h * nc + c] = sw;
-        uint16_t *wh = a.Ws + ((size_t)h * a.Tp + t0 + j0) * D + d, *wl = wh + (size_t)a.Hv * a.Tp * D;
+      for (int k = 0; k < 32; ++k) mx = fmaxf(mx, fabsf(v[k]));
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          uint32_t hi, lo;
-          split_f16x2(wv[k] * sw, wv[k + 1] * sw, hi, lo);
-          wh[(size_t)k * D] = (uint16_t)hi;
-          wh[(size_t)(k + 1) * D] = (uint16_t)(hi >> 16);
-          wl[(size_t)k * D] = (uint16_t)lo;
-          wl[(size_t)(k + 1) * D] = (uint16_t)(lo >> 16);
-        }
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      return mx;
+    };
+    // the W part
+    issue();
+    const int okw = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(done, 1u) : 0, 0);
+    if (!okw && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+    tc_fence_after();
+    float wv[32];  // W: tokens j0 + k, kept until the chunk's largest |W| is known
+    if (okw) read_acc(wv);
+    // the U part's R^T over the W part's (whose product has completed)
+    stage_r(1);
+    if (okw) {
+      const float mx = warp_absmax(wv);
+      if (lane == 0) wred[warp] = mx;
+    }
+    __syncthreads();  // every warp has read the W product and staged its U operand
+    issue();
+    if (okw) {  // W s = hi + lo, s from the chunk's largest |W|, while the U product runs
+      float m = wred[0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) m = fmaxf(m, wred[w]);
+      const float sw = fp16_scale_for(m);
+      if (tid == 0) a.Wsc[(size_t)h * nc + c] = sw;
+      uint16_t *wh = a.Ws + ((size_t)h * a.Tp + t0 + j0) * D + d, *wl = wh + (size_t)a.Hv * a.Tp * D;
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        uint32_t hi, lo;
+        split_f16x2(wv[k] * sw, wv[k + 1] * sw, hi, lo);
+        wh[(size_t)k * D] = (uint16_t)hi;
+        wh[(size_t)(k + 1) * D] = (uint16_t)(hi >> 16);
+        wl[(size_t)k * D] = (uint16_t)lo;
+        wl[(size_t)(k + 1) * D] = (uint16_t)(lo >> 16);
       }
+    }
+    // the U part: U~ in FP32 and the chunk's largest |U~| (the scan's bound on |U|)
+    const int oku = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(done, 0u) : 0, 0);
+    if (!oku && lane == 0) flag_status(a.status, GDN_E_TIMEOUT);
+    tc_fence_after();
+    if (oku) {
+      float uv[32];
+      read_acc(uv);
+      float *dst = a.Ut + (((size_t)h * nc + c) * kC + j0) * D + d;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) dst[(size_t)k * D] = uv[k];
+      const float mx = warp_absmax(uv);
+      if (lane == 0) ured[warp] = mx;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      float m = ured[0];
+      for (int w = 1; w < 8; ++w) m = fmaxf(m, ured[w]);
+      a.Umax[(size_t)h * nc + c] = m;
     }
   }
   if (warp == 0) {
