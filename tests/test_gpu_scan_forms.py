@@ -102,3 +102,36 @@ def test_chunk_forms_on_repeated_tokens(api, pattern):
     want = oracle_layer("FULL", 1).prefill(x, c, s, init_zero=False)
     assert rel_l2(_bf(outs[3][0]), _bf(want)) <= 2e-3
     assert rel_l2(outs[3][1], s) <= 2e-3
+
+
+@pytest.mark.parametrize("scale", [1e-6, 1e6])
+def test_tcgen05_scan_extreme_state_scales(api, scale):
+    """The split-FP16 products scale each operand block by a power of two:
+    S by its slice maximum, U and Cf by the bound max|U~| + d max|W| max|S|.
+    A prompt continuing from a state scaled by 1e-6 or 1e6 (the state's
+    contribution to U and to the output far below or far above the prompt's)
+    must still match the warp-MMA form and the oracle's token recurrence."""
+    shape = synth.FULL
+    T = 200
+    x = synth.x_tokens(shape, 7, T)
+    s0 = (synth.ssm_state(shape, 7) * np.float32(scale)).astype(np.float32)
+    L = api.lib()
+    outs = {}
+    try:
+        for form in (3, 2):
+            assert L.gdn_set_tuning(10, form) == 0
+            layer = api.layer_from_synth(weights("FULL", 1), max_batch=1, max_prefill_tokens=T)
+            conv_d, ssm_d = layer.new_states(2)
+            ssm_d[1].copy_(to_dev(s0))
+            o = to_host(layer.prefill(to_dev(x), 1, False, conv_d, ssm_d))
+            assert layer.check() == 0
+            outs[form] = (o, to_host(ssm_d)[1].copy())
+    finally:
+        L.gdn_set_tuning(10, 0)
+    assert rel_l2(_bf(outs[3][0]), _bf(outs[2][0])) <= 1e-3
+    assert rel_l2(outs[3][1], outs[2][1]) <= 1e-5
+    c = np.zeros((shape.conv_kernel - 1, shape.conv_channels), np.uint16)
+    s = s0.copy()
+    want = oracle_layer("FULL", 1).prefill(x, c, s, init_zero=False)
+    assert rel_l2(_bf(outs[3][0]), _bf(want)) <= 2e-3
+    assert rel_l2(outs[3][1], s) <= 2e-3
