@@ -510,7 +510,8 @@ struct PrefillArgs {
   int y_sf_tiled;
   int32_t *status;
 };
-// The prefill chunk scan on tcgen05 (scan_tc.cu), d = 128; needs a.KT.
+// The prefill chunk scan on tcgen05 (scan_tc.cu), d = 128; needs the split
+// operands Qs, Ws, As, KTs and the per-chunk Wsc, Umax of chunk_prep_tc.
 cudaError_t launch_chunk_scan_umma(const PrefillArgs &a, cudaStream_t stream);
 // Block-scaled W4A4 GEMM on tcgen05: D[m][n] = W_hat[m][:] . X_hat[n][:],
 // stored C[n][m] (ldc). W = weights (A operand, M = 128 rows per tile), X =

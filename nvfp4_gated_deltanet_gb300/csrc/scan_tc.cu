@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 }  // namespace
 
 // The tcgen05 chunk scan for d = 128 (slices of 32 rows of d_v per CTA).
-// Needs chunk_prep's W, Ut, Am, Gam and KT.
+// Needs chunk_prep_tc's split Qs (from prep), Ws, As, KTs, its FP32 Ut, Gam and the per-chunk Wsc, Umax.
 cudaError_t launch_chunk_scan_umma(const PrefillArgs &a, cudaStream_t stream) {
   constexpr int R = 32;
   if (a.D != kD || !a.Qs || !a.Ws || !a.As || !a.KTs || !a.Wsc || !a.Umax) return cudaErrorInvalidValue;
